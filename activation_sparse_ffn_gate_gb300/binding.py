@@ -1,0 +1,275 @@
+"""Thin ctypes binding over libtwell_gb300.so (the C ABI declared in include/twell.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels. PyTorch
+provides device memory and the current CUDA stream. The functions carry the C names; each
+allocates its outputs with torch when they are not given, passes raw device pointers and the
+current stream, and raises TwellError on a non-OK status. There is no fallback: without the
+built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtwell_gb300.so")
+
+TWELL_OK = 0
+TWELL_BF16 = 0
+TWELL_F32 = 1
+OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE = range(5)
+STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED", 3: "TWELL_ERR_BACKUP_FULL",
+                4: "TWELL_ERR_TIMEOUT", 5: "TWELL_ERR_DEVICE_CHECK", 6: "TWELL_ERR_CUDA",
+                7: "TWELL_ERR_WORKSPACE"}
+
+# Every function the header declares; the CPU tests check that the library exports each one.
+EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cnt_bytes", "twell_workspace_bytes",
+           "twell_gate_pack", "twell_ffn_fused_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
+           "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_gate_gemm", "twell_read_status",
+           "twell_status_string", "twell_device_info")
+
+
+class TwellError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_status_string(code)})")
+
+
+class _Packed(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("n_cols", ctypes.c_int32), ("tile", ctypes.c_int32),
+                ("cap", ctypes.c_int32), ("dtype", ctypes.c_int), ("vals", ctypes.c_void_p),
+                ("idx", ctypes.c_void_p), ("cnt", ctypes.c_void_p)]
+
+
+class _Hybrid(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("n_cols", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("backup_cap", ctypes.c_int32), ("dtype", ctypes.c_int), ("a", ctypes.c_void_p),
+                ("u", ctypes.c_void_p), ("col", ctypes.c_void_p), ("cnt", ctypes.c_void_p),
+                ("backup_rows", ctypes.c_void_p), ("n_backup", ctypes.c_void_p), ("A_b", ctypes.c_void_p),
+                ("U_b", ctypes.c_void_p), ("l1", ctypes.c_void_p), ("dev_status", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with activation_sparse_ffn_gate_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            st = ctypes.c_int
+            sig = {
+                "twell_packed_vals_bytes": (sz, [i32, i32, i32, ctypes.c_int]),
+                "twell_packed_idx_bytes": (sz, [i32, i32, i32]),
+                "twell_packed_cnt_bytes": (sz, [i32, i32, i32]),
+                "twell_workspace_bytes": (sz, [ctypes.c_int, i32, i32, i32, i32, i32, i32]),
+                "twell_gate_pack": (st, [vp, vp, i32, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Packed), vp, sz,
+                                         vp, vp]),
+                "twell_ffn_fused_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
+                                             sz, vp, vp]),
+                "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                          ctypes.POINTER(_Hybrid), vp, vp, sz, vp]),
+                "twell_hybrid_bwd": (st, [vp, vp, vp, vp, ctypes.POINTER(_Hybrid), vp, i32, i32, i32, ctypes.c_float,
+                                          vp, vp, vp, vp, vp, sz, vp]),
+                "twell_unpack": (st, [ctypes.POINTER(_Packed), vp, vp, vp]),
+                "twell_pack_from_gate": (st, [vp, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Packed), vp, vp]),
+                "twell_hybrid_route_from_gate": (st, [vp, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Hybrid), vp,
+                                                      sz, vp]),
+                "twell_gate_gemm": (st, [vp, vp, i32, i32, i32, vp, vp, vp]),
+                "twell_read_status": (st, [vp, vp]),
+                "twell_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+                "twell_device_info": (st, [ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load().twell_status_string(code).decode()
+    except Exception:  # the library itself failed to load
+        return "?"
+
+
+def _check(code: int, where: str):
+    if code != TWELL_OK:
+        raise TwellError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return TWELL_BF16
+    if dt == torch.float32:
+        return TWELL_F32
+    raise TypeError(f"unsupported element type {dt}")
+
+
+_status_bufs = {}
+
+
+def status_buffer(device=None) -> torch.Tensor:
+    """The per-device int32 status word the binding passes as dev_status."""
+    dev = torch.device(device if device is not None else torch.cuda.current_device())
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    buf = _status_bufs.get(dev.index)
+    if buf is None:
+        buf = torch.zeros(1, dtype=torch.int32, device=dev)
+        _status_bufs[dev.index] = buf
+    return buf
+
+
+def twell_read_status(status: Optional[torch.Tensor] = None, stream=None, reset: bool = True) -> int:
+    """Synchronise the stream and return the device status code (optionally clearing it)."""
+    status = status if status is not None else status_buffer()
+    code = load().twell_read_status(_ptr(status), _stream(stream))
+    if reset and code != TWELL_OK:
+        status.zero_()
+    return code
+
+
+def check_device_status(where: str = "device", status: Optional[torch.Tensor] = None, stream=None):
+    _check(twell_read_status(status, stream), where)
+
+
+# ------------------------------------------------------------------------------------------ TwELL
+
+@dataclasses.dataclass
+class TwELL:
+    """A TwELL matrix in device memory (see twell_packed in include/twell.h)."""
+
+    n_rows: int
+    n_cols: int
+    tile: int
+    vals: torch.Tensor  # [n_rows, nt, tile] element type
+    idx: torch.Tensor  # [n_rows, nt, tile] uint8
+    cnt: torch.Tensor  # [n_rows, nt] int16 storage of uint16 counts
+
+    @property
+    def nt(self) -> int:
+        return -(-self.n_cols // self.tile)
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.vals.dtype
+
+    @staticmethod
+    def empty(n_rows, n_cols, tile, dtype=torch.bfloat16, device=None):
+        nt = -(-n_cols // tile)
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        return TwELL(n_rows, n_cols, tile,
+                     torch.empty((n_rows, nt, tile), dtype=dtype, device=device),
+                     torch.empty((n_rows, nt, tile), dtype=torch.uint8, device=device),
+                     torch.empty((n_rows, nt), dtype=torch.int16, device=device))
+
+    def counts(self) -> torch.Tensor:
+        """Counts as non-negative integers (int32)."""
+        return self.cnt.to(torch.int32) & 0xFFFF
+
+    def c_struct(self) -> _Packed:
+        return _Packed(self.n_rows, self.n_cols, self.tile, self.tile, _dtype_code(self.vals.dtype),
+                       self.vals.data_ptr(), self.idx.data_ptr(), self.cnt.data_ptr())
+
+
+def twell_gate_pack(x: torch.Tensor, Wg_s: torch.Tensor, T: int = 128, out: Optional[TwELL] = None,
+                    status: Optional[torch.Tensor] = None, stream=None,
+                    vals_dtype: torch.dtype = torch.float32) -> TwELL:
+    """Gate GEMM with the ReLU + TwELL pack epilogue: returns the TwELL of ReLU(x Wg_s^T).
+
+    The packed values keep the fp32 accumulator by default (vals_dtype=torch.bfloat16 rounds them)."""
+    N, d = x.shape
+    f = Wg_s.shape[0]
+    out = out if out is not None else TwELL.empty(N, f, T, vals_dtype, x.device)
+    s = out.c_struct()
+    _check(load().twell_gate_pack(_ptr(x), _ptr(Wg_s), N, d, f, T, _dtype_code(x.dtype), ctypes.byref(s), None, 0,
+                                  _ptr(status if status is not None else status_buffer(x.device)), _stream(stream)),
+           "twell_gate_pack")
+    return out
+
+
+def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, a: TwELL,
+                        y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Fused up+down projection over the packed nonzeros: y = (a * (x Wu_s^T)) Wd_s."""
+    N, d = x.shape
+    f = Wu_s.shape[0]
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    s = a.c_struct()
+    _check(load().twell_ffn_fused_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), N, d, f,
+                                      _dtype_code(x.dtype), _ptr(y), None, 0,
+                                      _ptr(status if status is not None else status_buffer(x.device)),
+                                      _stream(stream)),
+           "twell_ffn_fused_fwd")
+    return y
+
+
+def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
+                vals_dtype: torch.dtype = torch.float32):
+    """The sparse inference FFN: twell_gate_pack then twell_ffn_fused_fwd (two kernels)."""
+    a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
+    return twell_ffn_fused_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
+
+
+def twell_unpack(a: TwELL, out: Optional[torch.Tensor] = None, status=None, stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty((a.n_rows, a.n_cols), dtype=a.dtype, device=a.vals.device)
+    s = a.c_struct()
+    _check(load().twell_unpack(ctypes.byref(s), _ptr(out),
+                               _ptr(status if status is not None else status_buffer(out.device)), _stream(stream)),
+           "twell_unpack")
+    return out
+
+
+def twell_pack_from_gate(G: torch.Tensor, T: int = 128, out: Optional[TwELL] = None, status=None,
+                         stream=None) -> TwELL:
+    N, f = G.shape
+    out = out if out is not None else TwELL.empty(N, f, T, G.dtype, G.device)
+    s = out.c_struct()
+    _check(load().twell_pack_from_gate(_ptr(G), N, f, T, _dtype_code(G.dtype), ctypes.byref(s),
+                                       _ptr(status if status is not None else status_buffer(G.device)),
+                                       _stream(stream)),
+           "twell_pack_from_gate")
+    return out
+
+
+def twell_gate_gemm(x: torch.Tensor, Wg_s: torch.Tensor, out: Optional[torch.Tensor] = None, status=None,
+                    stream=None) -> torch.Tensor:
+    N, d = x.shape
+    f = Wg_s.shape[0]
+    out = out if out is not None else torch.empty((N, f), dtype=torch.float32, device=x.device)
+    _check(load().twell_gate_gemm(_ptr(x), _ptr(Wg_s), N, d, f, _ptr(out),
+                                  _ptr(status if status is not None else status_buffer(x.device)), _stream(stream)),
+           "twell_gate_gemm")
+    return out
+
+
+def twell_workspace_bytes(op: int, N: int, d: int, f: int, tile: int = 128, K: int = 0, backup_cap: int = 0) -> int:
+    return int(load().twell_workspace_bytes(op, N, d, f, tile, K, backup_cap))
+
+
+def twell_device_info():
+    sm, ma, mi = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().twell_device_info(ctypes.byref(sm), ctypes.byref(ma), ctypes.byref(mi)), "twell_device_info")
+    return sm.value, ma.value, mi.value

@@ -1,0 +1,383 @@
+// twell_gemm.cuh -- persistent warp-specialised tcgen05 GEMM for sm_103a with pluggable epilogues.
+//
+//   C[M, N] = A[M, K] * B[K, N]     bf16 operands, fp32 accumulation in tensor memory (TMEM)
+//
+// A is K-major ([M, K] row-major) or MN-major ([K, M] row-major); B is K-major ([N, K] row-major,
+// i.e. the "rows of W" layout) or MN-major ([K, N] row-major). Tiles are 128 x BN x 64; TMA
+// writes each operand stage into shared memory with the 128-byte swizzle; one thread issues the
+// tcgen05.mma instructions into a double-buffered TMEM accumulator, so the epilogue of one tile
+// overlaps the main loop of the next.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. one row each).
+//
+// M and K may be read from device memory (rows of a device-side list, e.g. the hybrid backup
+// rows), so a launch sized for an upper bound does only the work that exists.
+//
+// Every mbarrier wait is bounded (twell::wait_bounded). On a timeout the CTA raises its abort
+// flag, every role leaves its loop, the producer waits (bounded) for the TMA copies it issued,
+// the MMA thread waits (bounded) for its last tcgen05 operations, and TMEM is freed before exit.
+#pragma once
+
+#include "twell_common.cuh"
+
+namespace twell {
+
+enum class Epi : int {
+    PackTwell = 0,   // ReLU + TwELL pack of the gate accumulator (fp32 or bf16 values)
+    StoreF32 = 1,    // out[m, n] = acc (fp32)
+    StoreBF16 = 2,   // out[m, n] = bf16(acc)
+    ScatterBF16 = 3, // out[rowmap[m], n] = bf16(acc)
+    AccumF32 = 4,    // out[m, n] += acc (fp32)
+};
+
+struct GemmArgs {
+    int M, N, K;             // extents; M and K are upper bounds when M_dyn / K_dyn are given
+    const int32_t* M_dyn;    // optional device scalar: M = min(M, *M_dyn)
+    const int32_t* K_dyn;    // optional device scalar: K = min(K, *K_dyn)
+    int kb_split;            // k-blocks >= kb_split read B from the second map, k restarting at 0
+    void* out;               // epilogue output
+    int64_t ldo;             // its leading dimension (elements)
+    const int32_t* rowmap;   // ScatterBF16: destination row of each m
+    // PackTwell
+    int vals_f32;  // packed values stored as fp32 (else bf16, rounded to nearest even)
+    void* vals;
+    uint8_t* idx;
+    uint16_t* cnt;
+    int T, nt;
+    // status
+    int32_t* status;
+    uint64_t wait_limit_ns;
+};
+
+constexpr int kGemmThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+};
+
+template <int BN, bool A_MN, bool B_MN, Epi EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const GemmArgs g)
+{
+    using C = GemmCfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int M = g.M;
+    if (g.M_dyn != nullptr) M = min(M, *g.M_dyn);
+    int K = g.K;
+    if (g.K_dyn != nullptr) K = min(K, *g.K_dyn);
+    const int m_tiles = M > 0 ? (M + kBM - 1) / kBM : 0;
+    const int n_tiles = (g.N + BN - 1) / BN;
+    const int kbs = K > 0 ? (K + kBK - 1) / kBK : 0;
+    const int tiles = kbs > 0 ? m_tiles * n_tiles : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (g.kb_split < kbs) tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+                const int m0 = (t / n_tiles) * kBM;
+                const int n0 = (t % n_tiles) * BN;
+                for (int kb = 0; kb < kbs; ++kb) {
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    uint8_t* a = sA + stage * C::A_BYTES;
+                    uint8_t* b = sB + stage * C::B_BYTES;
+                    const int k0 = kb * kBK;
+                    if constexpr (!A_MN) {
+                        tma_load_2d(a, &tmA, k0, m0, &full[stage]);
+                    } else {
+                        tma_load_2d(a, &tmA, m0, k0, &full[stage]);
+                        tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[stage]);
+                    }
+                    const CUtensorMap* tb = &tmB;
+                    int kk = k0;
+                    if (kb >= g.kb_split) {
+                        tb = &tmB2;
+                        kk = (kb - g.kb_split) * kBK;
+                    }
+                    if constexpr (!B_MN) {
+                        tma_load_2d(b, tb, kk, n0, &full[stage]);
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < BN / 64; ++s) tma_load_2d(b + s * 8192, tb, n0 + 64 * s, kk, &full[stage]);
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Wait (bounded, even after an abort) for every copy this thread issued to land, so
+            // no TMA write into shared memory is still in flight when the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded(&full[s], (issued_phase >> s) & 1u, nullptr, g.status, g.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+                if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < kbs; ++kb) {
+                    if (!wait_bounded(&full[stage], phase, abort_flag, g.status, g.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // one MMA consumes K = 16: 32 bytes along a K-major row, 16 rows of an MN-major tile
+                        const uint64_t da = A_MN ? desc_sw128(a_addr + k * 2048, 8192) : desc_sw128(a_addr + k * 32, 16);
+                        const uint64_t db = B_MN ? desc_sw128(b_addr + k * 2048, 8192) : desc_sw128(b_addr + k * 32, 16);
+                        tc_mma_f16(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(&empty[stage]);  // frees this stage once its MMAs have read it
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);  // accumulator complete
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // Wait (bounded) for every tcgen05 operation this thread issued before TMEM is freed.
+            tc_commit(drain);
+            wait_bounded(drain, 0, nullptr, g.status, g.wait_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, g.status, g.wait_limit_ns) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int m0 = (t / n_tiles) * kBM;
+            const int n0 = (t % n_tiles) * BN;
+            const int row = m0 + 32 * q + lane;
+            const bool row_ok = row < M;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+
+            if constexpr (EPI == Epi::PackTwell) {
+                // ReLU + TwELL: per (row, T-wide column tile) keep g > 0 in ascending column order.
+                const int T = g.T;
+                __nv_bfloat16* vals16 = static_cast<__nv_bfloat16*>(g.vals);
+                float* vals32 = static_cast<float*>(g.vals);
+                for (int tt = 0; tt < BN / T; ++tt) {
+                    const int tile = n0 / T + tt;
+                    const bool valid = row_ok && tile < g.nt;
+                    const size_t slot = (static_cast<size_t>(row) * g.nt + tile) * static_cast<size_t>(T);
+                    int c = 0;
+                    for (int ch = 0; ch < T / 32; ++ch) {
+                        float v[32];
+                        tmem_ld_32x32b_x32(taddr + tt * T + ch * 32, v);
+                        if (valid) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                if (v[k] > 0.0f) {
+                                    if (g.vals_f32) vals32[slot + c] = v[k];
+                                    else vals16[slot + c] = __float2bfloat16_rn(v[k]);
+                                    g.idx[slot + c] = static_cast<uint8_t>(ch * 32 + k);
+                                    ++c;
+                                }
+                            }
+                        }
+                    }
+                    if (valid) g.cnt[static_cast<size_t>(row) * g.nt + tile] = static_cast<uint16_t>(c);
+                }
+            } else {
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(taddr + ch * 32, v);
+                    const int col0 = n0 + ch * 32;
+                    if (!row_ok || col0 >= g.N) continue;
+                    const int nvalid = min(32, g.N - col0);
+                    if constexpr (EPI == Epi::StoreF32 || EPI == Epi::AccumF32) {
+                        float* o = static_cast<float*>(g.out) + static_cast<size_t>(row) * g.ldo + col0;
+                        if (nvalid == 32) {
+#pragma unroll
+                            for (int k = 0; k < 32; k += 4) {
+                                float4 w = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                                if constexpr (EPI == Epi::AccumF32) {
+                                    const float4 p = *reinterpret_cast<const float4*>(o + k);
+                                    w.x += p.x;
+                                    w.y += p.y;
+                                    w.z += p.z;
+                                    w.w += p.w;
+                                }
+                                *reinterpret_cast<float4*>(o + k) = w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                if (k < nvalid) {
+                                    if constexpr (EPI == Epi::AccumF32) o[k] += v[k];
+                                    else o[k] = v[k];
+                                }
+                            }
+                        }
+                    } else {
+                        const int orow = (EPI == Epi::ScatterBF16) ? g.rowmap[row] : row;
+                        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0;
+                        if (nvalid == 32) {
+#pragma unroll
+                            for (int k = 0; k < 32; k += 8) {
+                                float f8[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) f8[e] = v[k + e];
+                                *reinterpret_cast<uint4*>(o + k) = pack16(f8, static_cast<__nv_bfloat16*>(nullptr));
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                if (k < nvalid) o[k] = __float2bfloat16_rn(v[k]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace twell
+
+namespace twell_host {
+
+// Operand description for the host launcher.
+struct GemmOperand {
+    const void* ptr;  // bf16 row-major matrix
+    int64_t rows, cols, ld;
+};
+
+// Launch C = A * B with the tcgen05 kernel. A: [M, K] (a_mn = false) or [K, M] (a_mn = true);
+// B: [N, K] (b_mn = false) or [K, N] (b_mn = true); B2 (optional) continues B along K from
+// k-block kb_split on. Returns TWELL_ERR_CUDA on a tensor-map or launch failure.
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI>
+twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
+                         cudaStream_t stream);
+
+}  // namespace twell_host
+
+namespace twell_host {
+
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI>
+twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
+                         cudaStream_t stream)
+{
+    using Cfg = twell::GemmCfg<BN>;
+    DevInfo di;
+    if (dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    if (di.max_smem_optin < Cfg::SMEM_BYTES) return TWELL_ERR_UNSUPPORTED;
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return TWELL_OK;
+    CUtensorMap ta, tb, tb2;
+    twell_status st;
+    // A: K-major box = 64 (K) x 128 (M); MN-major box = 64 (M) x 64 (K), two per stage.
+    st = A_MN ? make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, 64)
+              : make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, twell::kBM);
+    if (st != TWELL_OK) return st;
+    // B: K-major box = 64 (K) x BN (N); MN-major box = 64 (N) x 64 (K), BN/64 per stage.
+    st = B_MN ? make_tmap_bf16(&tb, B.ptr, B.cols, B.rows, B.ld, 64, 64)
+              : make_tmap_bf16(&tb, B.ptr, B.cols, B.rows, B.ld, 64, BN);
+    if (st != TWELL_OK) return st;
+    if (B2 != nullptr) {
+        st = B_MN ? make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, 64)
+                  : make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, BN);
+        if (st != TWELL_OK) return st;
+    } else {
+        tb2 = tb;
+        g.kb_split = 1 << 30;
+    }
+    auto kern = twell::tc_gemm_kernel<BN, A_MN, B_MN, EPI>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM_BYTES)) !=
+        cudaSuccess)
+        return TWELL_ERR_CUDA;
+    const long long tiles = static_cast<long long>((g.M + twell::kBM - 1) / twell::kBM) * ((g.N + BN - 1) / BN);
+    const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
+    g.wait_limit_ns = wait_limit_ns();
+    kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
+    return launch_status();
+}
+
+}  // namespace twell_host

@@ -1,0 +1,125 @@
+// twell_pack.cu -- TwELL pack of a given gate matrix and TwELL unpack (test exports).
+//
+// One warp per (token row, column tile): the lanes test 32 columns at a time, a warp ballot marks
+// the kept entries (g > 0) and each kept lane finds its slot as the population count of the
+// ballot bits below it -- the same ascending-order compaction the gate epilogue performs
+// ([TG] "Вот тут и решает TwELL"; [TC] §2).
+#include "twell_common.cuh"
+
+namespace twell {
+
+template <typename E>
+__global__ void pack_from_gate_kernel(const E* __restrict__ G, int N, int f, int T, int nt, E* __restrict__ vals,
+                                      uint8_t* __restrict__ idx, uint16_t* __restrict__ cnt)
+{
+    const int lane = threadIdx.x & 31;
+    const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= static_cast<long long>(N) * nt) return;
+    const int r = static_cast<int>(w / nt), t = static_cast<int>(w % nt);
+    const size_t slot = (static_cast<size_t>(r) * nt + t) * T;
+    int c = 0;
+    for (int ch = 0; ch < T; ch += 32) {
+        const int k = ch + lane;
+        const int j = t * T + k;
+        E g{};
+        bool keep = false;
+        if (j < f) {
+            g = G[static_cast<size_t>(r) * f + j];
+            keep = Elem<E>::to_f(g) > 0.0f;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        const int pos = c + __popc(m & ((1u << lane) - 1u));
+        if (keep) {
+            vals[slot + pos] = g;
+            idx[slot + pos] = static_cast<uint8_t>(k);
+        }
+        c += __popc(m);
+    }
+    if (lane == 0) cnt[static_cast<size_t>(r) * nt + t] = static_cast<uint16_t>(c);
+}
+
+template <typename E>
+__global__ void unpack_kernel(const E* __restrict__ vals, const uint8_t* __restrict__ idx,
+                              const uint16_t* __restrict__ cnt, int N, int f, int T, int nt, E* __restrict__ dense,
+                              int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= static_cast<long long>(N) * nt) return;
+    const int r = static_cast<int>(w / nt), t = static_cast<int>(w % nt);
+    E* out = dense + static_cast<size_t>(r) * f;
+    for (int k = lane; k < T; k += 32) {
+        const int j = t * T + k;
+        if (j < f) out[j] = Elem<E>::from_f(0.0f);
+    }
+    __syncwarp();
+    int c = cnt[static_cast<size_t>(r) * nt + t];
+    if (c > T) {
+        if (lane == 0) report(status, TWELL_ERR_DEVICE_CHECK);
+        c = T;
+    }
+    const size_t slot = (static_cast<size_t>(r) * nt + t) * T;
+    for (int k = lane; k < c; k += 32) {
+        const int j = t * T + idx[slot + k];
+        if (j < f) out[j] = vals[slot + k];
+        else report(status, TWELL_ERR_DEVICE_CHECK);
+    }
+}
+
+}  // namespace twell
+
+using namespace twell_host;
+
+static inline unsigned warp_blocks(long long warps, int per_block)
+{
+    return static_cast<unsigned>((warps + per_block - 1) / per_block);
+}
+
+extern "C" twell_status twell_pack_from_gate(const void* G, int32_t N, int32_t f, int32_t T, twell_dtype dtype,
+                                             const twell_packed* out, int32_t* dev_status, void* stream)
+{
+    if (dev_status == nullptr || (G == nullptr && N != 0)) return TWELL_ERR_INVALID;
+    if (N < 0 || f <= 0) return TWELL_ERR_INVALID;
+    if (!dtype_ok(dtype)) return TWELL_ERR_UNSUPPORTED;
+    twell_status st = check_packed(out, N, f, T, dtype);
+    if (st != TWELL_OK) return st;
+    if (N == 0) return TWELL_OK;
+    if (!aligned16(G)) return TWELL_ERR_INVALID;
+    const int nt = (f + T - 1) / T;
+    const long long warps = static_cast<long long>(N) * nt;
+    if (warps / 8 + 1 > 0x7fffffffLL) return TWELL_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == TWELL_BF16)
+        twell::pack_from_gate_kernel<__nv_bfloat16><<<warp_blocks(warps, 8), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(G), N, f, T, nt, static_cast<__nv_bfloat16*>(out->vals), out->idx,
+            out->cnt);
+    else
+        twell::pack_from_gate_kernel<float><<<warp_blocks(warps, 8), 256, 0, s>>>(
+            static_cast<const float*>(G), N, f, T, nt, static_cast<float*>(out->vals), out->idx, out->cnt);
+    return launch_status();
+}
+
+extern "C" twell_status twell_unpack(const twell_packed* a, void* dense_out, int32_t* dev_status, void* stream)
+{
+    if (a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (!dtype_ok(a->dtype)) return TWELL_ERR_UNSUPPORTED;
+    const int N = a->n_rows, f = a->n_cols, T = a->tile;
+    if (N < 0 || f <= 0 || (dense_out == nullptr && N != 0)) return TWELL_ERR_INVALID;
+    twell_status st = check_packed(a, N, f, T, a->dtype);
+    if (st != TWELL_OK) return st;
+    if (N == 0) return TWELL_OK;
+    if (!aligned16(dense_out)) return TWELL_ERR_INVALID;
+    const int nt = (f + T - 1) / T;
+    const long long warps = static_cast<long long>(N) * nt;
+    if (warps / 8 + 1 > 0x7fffffffLL) return TWELL_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a->dtype == TWELL_BF16)
+        twell::unpack_kernel<__nv_bfloat16><<<warp_blocks(warps, 8), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(a->vals), a->idx, a->cnt, N, f, T, nt,
+            static_cast<__nv_bfloat16*>(dense_out), dev_status);
+    else
+        twell::unpack_kernel<float><<<warp_blocks(warps, 8), 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx,
+                                                                          a->cnt, N, f, T, nt,
+                                                                          static_cast<float*>(dense_out), dev_status);
+    return launch_status();
+}

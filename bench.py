@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse inference FFN layer (TwELL) on GB300.
+
+One step = the whole inference hot path over one batch of tokens: twell_gate_pack (tcgen05 gate
+GEMM with the ReLU + TwELL pack epilogue) followed by twell_ffn_fused_fwd (fused up+down walk
+over the packed nonzeros), both through the C ABI. The workload is the 1.5B-like layer:
+N = 8192 tokens, d_model = 2048, d_ff = 5632, T = 128, bf16 with fp32 accumulation, ~29 nonzero
+gate activations per token, 30% dead columns (seed 1). Inputs are resident in HBM; the 129 MB L2
+is flushed (256 MiB write) before every timed step.
+
+Prints ONE JSON line. Beside tokens/s it reports the dominant kernel's roofline fraction, the
+layer roofline of the method's byte model, the speedup over a dense cuBLAS bf16 FFN of the same
+shape, an end-to-end figure with host buffers, and the fp64 CPU oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 is launched with torchrun: every rank runs its own batch (weak scaling, no collective on
+the data path; a barrier and a max over ranks of the timed region only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse FFN tokens/s per layer on 1 GB300; % of roofline; speedup vs dense FFN"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-dense", action="store_true")
+    return p.parse_args()
+
+
+def _peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ oracle (CPU)
+
+def oracle_sparse_rows(L, rows):
+    """The fp64 oracle's sparse path on the given token rows: gate -> TwELL pack -> walk."""
+    import numpy as np
+
+    import oracle
+    G = oracle.gate(L.x, L.Wg_s, rows=rows)
+    vals, idx, cnt = oracle.twell_pack(G, L.T)
+    return oracle.twell_walk(vals, idx, cnt, L.T, L.x[rows].astype(np.float64), L.Wu_s, L.Wd_s)
+
+
+def cpu_oracle_rate(L, target_s=4.0, max_rows=4096):
+    """Tokens/s of the oracle's sparse path on a bounded row sample sized to take ~target_s."""
+    import numpy as np
+    rng = np.random.default_rng(123)
+    n = 8
+    while True:
+        rows = rng.choice(L.N, n, replace=False)
+        t0 = time.perf_counter()
+        oracle_sparse_rows(L, rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= max_rows:
+            return n / dt, n, dt
+        n = min(max_rows, max(n * 2, int(n * target_s / max(dt, 1e-3))))
+
+
+# ------------------------------------------------------------------------------------ reference arm
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+
+    from activation_sparse_ffn_gate_gb300 import synthetic
+    L = synthetic.layer_1p5b()
+    rng = np.random.default_rng(7)
+    # calibrate one row, then size each step's sample so the whole run ends within a few minutes
+    t0 = time.perf_counter()
+    oracle_sparse_rows(L, rng.choice(L.N, 4, replace=False))
+    per_row = (time.perf_counter() - t0) / 4
+    budget = 120.0
+    S = int(max(1, min(512, budget / max(1, a.steps + a.warmup) / per_row)))
+    for _ in range(a.warmup):
+        oracle_sparse_rows(L, rng.choice(L.N, S, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle_sparse_rows(L, rng.choice(L.N, S, replace=False))
+    dt = time.perf_counter() - t0
+    value = a.steps * S / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": L.name, "N": L.N, "d_model": L.d, "d_ff": L.f, "T": L.T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                         "sample": f"{S} random token rows of the {L.N}-token batch per step (fp64 gate, TwELL pack, "
+                                   f"fused walk)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+def _source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "gate": ["activation_sparse_ffn_gate_gb300/csrc/twell_gemm.cuh", "activation_sparse_ffn_gate_gb300/csrc/twell_gate.cu",
+             "activation_sparse_ffn_gate_gb300/csrc/twell_common.cuh"],
+    "fused": ["activation_sparse_ffn_gate_gb300/csrc/twell_ffn.cu", "activation_sparse_ffn_gate_gb300/csrc/twell_common.cuh"],
+}
+
+
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != _source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def run_ours(a, rank, world):
+    import numpy as np
+    import torch
+
+    from activation_sparse_ffn_gate_gb300 import binding, build, synthetic
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    L = synthetic.layer_1p5b(seed=1 + rank)  # every rank its own batch (weak scaling)
+    t = L.torch_inputs(dev)
+    x, Wg, Wu, Wd = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"]
+    N, d, f, T = L.N, L.d, L.f, L.T
+    status = binding.status_buffer(dev)
+    status.zero_()
+    packed = binding.TwELL.empty(N, f, T, torch.float32, dev)  # fp32 packed gate values
+    y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+
+    for _ in range(a.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    binding.check_device_status("warmup", status)
+
+    clk = ClockSampler(dev.index)
+    clk.start()
+    time.sleep(0.6)  # let nvidia-smi start sampling
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(a.steps):
+        flush.fill_(1)
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        e1.record(stream)
+        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk.stop()
+    binding.check_device_status("timed region", status)
+    t_gate = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    t_fused = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    t_step = sum(t_gate) + sum(t_fused)  # ms over K steps, L2 flushes excluded
+    if dist:
+        tt = torch.tensor([t_step], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = tt.item()
+    ms_step = t_step / a.steps
+    value = world * N / (ms_step * 1e-3)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    # ---- realised sparsity and the union of active weight rows per 128-token tile (byte model)
+    dense_a = binding.twell_unpack(packed)
+    active = dense_a != 0
+    nnz = active.sum().item()
+    tiles = (N + 127) // 128
+    union = sum(int(active[i * 128:(i + 1) * 128].any(0).sum().item()) for i in range(tiles))
+    del dense_a, active
+    twell_bytes = N * (f // T) * 2 + nnz * 5  # counts + packed (fp32 value, u8 index) entries
+    peaks, peak_kind = _peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    gate_flops = 2.0 * N * d * f
+    bytes_layer = (N * d * 2) + (f * d * 2) + union * 2 * d * 2 + (N * d * 2)
+    t_roof = max(gate_flops / tc, bytes_layer / hbm)
+    # per-kernel algorithmic work
+    fused_bytes = (N * d * 2) + union * 2 * d * 2 + (N * d * 2) + twell_bytes
+    mg, mf = sum(t_gate) / a.steps, sum(t_fused) / a.steps
+    if mf >= mg:
+        ach = fused_bytes / (mf * 1e-3) / 1e9
+        roof = {"kernel": "twell_ffn_fused_fwd", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": _traffic("fused"),
+                "algorithmic_bytes": fused_bytes, "ms_per_launch": mf, "peak_kind": peak_kind + " hbm_gbs"}
+    else:
+        ach = gate_flops / (mg * 1e-3) / 1e12
+        roof = {"kernel": "twell_gate_pack", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": _traffic("gate"),
+                "algorithmic_flops": gate_flops, "ms_per_launch": mg, "peak_kind": peak_kind + " bf16_tflops (burst)"}
+
+    # ---- dense cuBLAS bf16 FFN of the same shape (best of two formulations)
+    dense = None
+    if not a.no_dense:
+        Wgu = torch.cat([Wg, Wu], 0)
+
+        def dense_a_():
+            g = x @ Wg.T
+            u = x @ Wu.T
+            return (torch.relu(g) * u) @ Wd
+
+        def dense_b_():
+            gu = x @ Wgu.T
+            g, u = gu[:, :f], gu[:, f:]
+            return (torch.relu(g) * u) @ Wd
+
+        best = {}
+        for name, fn in (("three_gemms", dense_a_), ("fused_gate_up_gemm", dense_b_)):
+            for _ in range(5):
+                flush.fill_(1)
+                fn()
+            ts = []
+            for _ in range(30):
+                flush.fill_(1)
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record()
+                fn()
+                s1.record()
+                torch.cuda.synchronize()
+                ts.append(s0.elapsed_time(s1))
+            best[name] = statistics.median(ts)
+        bname = min(best, key=best.get)
+        dense = {"ms": best[bname], "formulation": bname, "all_ms": best, "speedup": best[bname] / ms_step}
+
+    # ---- end to end through the C ABI with host buffers (pinned H2D of x, D2H of y, every step)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty((N, d), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    e2e_steps = max(10, min(a.steps, 200))
+    for _ in range(3):
+        xd.copy_(xh, non_blocking=True)
+        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream)
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream)
+        yh.copy_(y, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    binding.check_device_status("e2e", status)
+
+    cpu = None
+    if not a.no_cpu_baseline:
+        rate, n_rows, secs = cpu_oracle_rate(L)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+               "sample": f"{n_rows} random token rows of the {N}-token batch (fp64 gate GEMV, TwELL pack, fused "
+                         f"walk), {secs:.1f} s wall"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": L.name, "N": N, "d_model": d, "d_ff": f, "T": T, "tokens_per_gpu": N,
+                   "nnz_per_token": nnz / N, "density": nnz / (N * f), "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "roofline": roof,
+        "layer_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step, "bytes": bytes_layer,
+                           "gate_flops": gate_flops, "union_cols_per_128_tokens": union / tiles,
+                           "definition": "max(gate FLOPs / bf16 peak, (x + Wg + union of active Wu/Wd rows per "
+                                         "128-token tile + y) / HBM peak)"},
+        "kernels_ms": {"twell_gate_pack": mg, "twell_ffn_fused_fwd": mf},
+        "vs_dense_cublas": dense,
+        "cpu_baseline": cpu,
+        "e2e": {"value": N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": N * d * 2,
+                "d2h_bytes_per_step": N * d * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * a.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    a = _args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", a.gpus if a.gpus == 1 else 1))
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+    else:
+        run_ours(a, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+/*
+ * twell.h -- C ABI of the GB300 (sm_103a) activation-sparse gated FFN library (libtwell_gb300.so).
+ *
+ * The layer is  y = (ReLU(x Wg) * (x Wu)) Wd  with the gate activation kept in the tile-wise
+ * ELL (TwELL) format. Passages that define each operation are cited by page title and section:
+ *   [AIM] aimodeling.com news item "TwELL：Sakana AI与NVIDIA联合提出稀疏LLM推理加速20%，解决GPU批处理落地难题",
+ *         summary paragraph n (¶n).
+ *   [TG]  Telegram post "Sakana AI и NVIDIA представили TwELL ..." (ai_machinelearning_big_data),
+ *         sections "Вот тут и решает TwELL", "Инференс", "Обучение".
+ *   [PUL] pulsen.vercel.app "Sakana AI og NVIDIA introduserer TwELL ...", paragraph n.
+ *   [TC]  Tencent Cloud "一文读懂 NVIDIA 与 Sakana AI 联手打造的稀疏 LLM 黑科技", sections 1-6.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Shapes: N tokens, d = d_model, f = d_ff, T = TwELL tile width, nt = ceil(f / T),
+ *   K = hybrid per-row capacity.
+ * - Weights are stored one row per hidden unit ("rows of Wu and Wd", [TG] "Инференс"):
+ *   Wg_s = Wg^T, Wu_s = Wu^T and Wd_s = Wd are all [f, d] row-major. x, y, dy, dx are [N, d]
+ *   row-major. So G = x Wg_s^T, U = x Wu_s^T, y = (ReLU(G) * U) Wd_s.
+ * - Every pointer argument named as device memory must be device memory allocated by the
+ *   caller; the library never allocates, never frees and keeps no pointer after a call returns.
+ *   Struct arguments (twell_packed, twell_hybrid) are host structs that hold device pointers.
+ * - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *   default stream). Outputs are valid once the stream reaches the call.
+ * - Alignment: every device pointer must be 16-byte aligned; d must be a multiple of 8.
+ * - Element type: TWELL_BF16 (bf16 storage, fp32 accumulation, tcgen05 tensor cores for the
+ *   gate) or TWELL_F32 (fp32 storage and arithmetic on CUDA cores; small layers and tests).
+ * - Errors: argument errors are detected on the host and returned before anything is launched
+ *   (nothing is written). Conditions found on the device (a bounded wait that ran out, a
+ *   failed device-side check, a full backup buffer) are written to *dev_status (one int32 in
+ *   device memory, first error wins, never cleared by the library) as a twell_status code; read
+ *   it with twell_read_status(). Launch failures return TWELL_ERR_CUDA.
+ */
+#ifndef TWELL_GB300_H
+#define TWELL_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TWELL_API __attribute__((visibility("default")))
+#else
+#define TWELL_API
+#endif
+
+typedef enum {
+    TWELL_OK = 0,
+    TWELL_ERR_INVALID = 1,     /* bad argument (null pointer, size, alignment, mismatch) */
+    TWELL_ERR_UNSUPPORTED = 2, /* valid but not supported here (dtype, tile width, device) */
+    TWELL_ERR_BACKUP_FULL = 3, /* hybrid: more overflow rows than backup_cap (device-reported) */
+    TWELL_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (device-reported) */
+    TWELL_ERR_DEVICE_CHECK = 5,/* a device-side consistency check failed (device-reported) */
+    TWELL_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+    TWELL_ERR_WORKSPACE = 7    /* workspace missing or smaller than twell_workspace_bytes() */
+} twell_status;
+
+typedef enum { TWELL_BF16 = 0, TWELL_F32 = 1 } twell_dtype;
+
+typedef enum {
+    TWELL_OP_GATE_PACK = 0,
+    TWELL_OP_FFN_FUSED_FWD = 1,
+    TWELL_OP_HYBRID_FWD = 2,
+    TWELL_OP_HYBRID_BWD = 3,
+    TWELL_OP_HYBRID_ROUTE = 4
+} twell_op;
+
+/* A TwELL matrix of gate activations a = ReLU(G), [n_rows, n_cols] ([TG] "Вот тут и решает TwELL";
+ * [TC] §2). The columns are cut into nt = ceil(n_cols / tile) tiles of `tile` columns (the last
+ * one partial when tile does not divide n_cols). For row r and tile t:
+ *   cnt[r*nt + t]                 number of kept entries (g > 0) of that row in that tile;
+ *   vals[(r*nt + t)*cap + k]      value of the k-th kept entry, k < cnt (element type `dtype`);
+ *   idx [(r*nt + t)*cap + k]      its column inside the tile (0..tile-1), strictly ascending in k.
+ * Slots k >= cnt are never written or read. cap must equal tile (lossless: a tile can never
+ * overflow). tile is 64, 128 or 256. All three arrays are caller-owned device memory. */
+typedef struct {
+    int32_t n_rows;
+    int32_t n_cols;
+    int32_t tile;
+    int32_t cap;
+    twell_dtype dtype;
+    void* vals;
+    uint8_t* idx;
+    uint16_t* cnt;
+} twell_packed;
+
+/* The hybrid training format ([TG] "Обучение"; [TC] §3): each row either fits in one
+ * globally aligned sparse block of fixed capacity K or, when it has more than K nonzeros,
+ * goes to a dense backup buffer. All pointers are caller-owned device memory.
+ *   cnt[n_rows]          nonzeros of a light row (<= K), or 0xFFFF for a backup row;
+ *   col[n_rows*K]        light rows: kept columns in ascending order, slots >= cnt hold 0;
+ *   a  [n_rows*K]        light rows: a = ReLU(g) at those columns, slots >= cnt hold +0;
+ *   u  [n_rows*K]        light rows: u = x Wu_s^T at those columns (filled by hybrid_fwd);
+ *   backup_rows[backup_cap]  backup row indices in ascending order;
+ *   n_backup[1]          number of overflow rows (may exceed backup_cap: then the call
+ *                        reports TWELL_ERR_BACKUP_FULL and only backup_cap rows are stored);
+ *   A_b[backup_cap*n_cols]   dense a rows of the backup rows (dtype);
+ *   U_b[backup_cap*n_cols]   dense u rows of the backup rows (filled by hybrid_fwd);
+ *   l1[1]                L1 term lambda * mean|h| (fp32, filled by hybrid_fwd);
+ *   dev_status[1]        device status word (see the conventions above).
+ * Entries a/u/A_b/U_b use the context's dtype (TWELL_BF16 only for the hybrid calls). */
+typedef struct {
+    int32_t n_rows;
+    int32_t n_cols;
+    int32_t K;
+    int32_t backup_cap;
+    twell_dtype dtype;
+    void* a;
+    void* u;
+    uint16_t* col;
+    uint16_t* cnt;
+    int32_t* backup_rows;
+    int32_t* n_backup;
+    void* A_b;
+    void* U_b;
+    float* l1;
+    int32_t* dev_status;
+} twell_hybrid;
+
+/* ------------------------------------------------------------------------------------------
+ * Sizes. Bytes of the three TwELL arrays for [n_rows, n_cols] with tile width `tile`
+ * (cap = tile), and workspace bytes an operation needs (0 = none; then ws may be NULL).
+ * Return 0 on invalid arguments.
+ */
+TWELL_API size_t twell_packed_vals_bytes(int32_t n_rows, int32_t n_cols, int32_t tile, twell_dtype dtype);
+TWELL_API size_t twell_packed_idx_bytes(int32_t n_rows, int32_t n_cols, int32_t tile);
+TWELL_API size_t twell_packed_cnt_bytes(int32_t n_rows, int32_t n_cols, int32_t tile);
+TWELL_API size_t twell_workspace_bytes(twell_op op, int32_t N, int32_t d, int32_t f, int32_t tile, int32_t K,
+                             int32_t backup_cap);
+
+/* ------------------------------------------------------------------------------------------
+ * Gate projection with the TwELL pack in its epilogue ([AIM] ¶3; [TG] "Вот тут и решает TwELL";
+ * [PUL] ¶3; [TC] §2): G = x Wg_s^T accumulated in fp32, and in the same kernel, per token row
+ * and column tile, a = ReLU(G) is packed as values + in-tile indices + count. A gate entry is
+ * kept iff its fp32 accumulator is > 0. No dense G is written. x [N, d], Wg_s [f, d] (device,
+ * element type `dtype`). `out` must describe an [N, f] TwELL matrix with out->tile = T; its
+ * values are stored in out->dtype: TWELL_F32 keeps the fp32 accumulator exactly (allowed for
+ * both input types), TWELL_BF16 rounds it to nearest even (bf16 inputs only).
+ * ws/ws_bytes: workspace (twell_workspace_bytes(TWELL_OP_GATE_PACK, ...), currently 0).
+ */
+TWELL_API twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t N, int32_t d, int32_t f,
+                             int32_t T, twell_dtype dtype, const twell_packed* out, void* ws,
+                             size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Fused up+down projection over a TwELL matrix ([AIM] ¶3; [TG] "Инференс"; [PUL] ¶3; [TC] §2):
+ * for every token row, walk only its packed nonzeros (column j, value a), gather row j of Wu_s
+ * and of Wd_s, and accumulate y_r += a * (x_r . Wu_s[j]) * Wd_s[j] in fp32; y is stored in the
+ * TwELL's dtype. The hidden activation h is never written to memory. Rows with no nonzeros get
+ * y = 0. x [N, d], Wu_s / Wd_s [f, d], y [N, d] (device, element type `dtype`; the TwELL
+ * values may be bf16 or fp32 independently, except that fp32 inputs need fp32 values).
+ */
+TWELL_API twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, const void* Wd_s,
+                                 const twell_packed* a, int32_t N, int32_t d, int32_t f,
+                                 twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream);
+
+/* Hybrid-format training forward ([TG] "Обучение"; [TC] §3), bf16 only: gate GEMM + TwELL pack,
+ * routing of each row to the sparse block (nnz <= K) or to the dense backup (nnz > K, in
+ * ascending row order), the up/down products (gathered rows of Wu_s / Wd_s for light rows,
+ * dense tensor-core GEMMs for backup rows), y [N, d], and the L1 term
+ * l1_coef * mean|h| over all N*f entries of h ([AIM] ¶4; [PUL] ¶4) into *ctx->l1.
+ * ctx describes caller-owned buffers for N = ctx->n_rows, f = ctx->n_cols.
+ */
+TWELL_API twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const void* Wu_s, const void* Wd_s,
+                              int32_t N, int32_t d, int32_t f, int32_t K, float l1_coef,
+                              twell_dtype dtype, const twell_hybrid* ctx, void* y, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Hybrid-format training backward ([TG] "Обучение": no product of two dense matrices for the
+ * sparse rows), bf16 storage: given the context filled by twell_hybrid_fwd and dy [N, d],
+ * computes the gradients of  <y, dy> + l1_coef * mean|h| :
+ *   dh = dy_r . Wd_s[j] + l1_coef * sgn(h) / (N f),  du = dh * a,  dg = dh * u  (at kept entries)
+ *   dx [N, d] (bf16)          = sum_j du * Wu_s[j] + dg * Wg_s[j]
+ *   dWg_s, dWu_s, dWd_s [f, d] (fp32, overwritten) = sum_r dg x_r, du x_r, h dy_r.
+ * Backup rows use dense tensor-core GEMMs for the same terms.
+ */
+TWELL_API twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const void* Wu_s, const void* Wd_s,
+                              const twell_hybrid* ctx, const void* dy, int32_t N, int32_t d,
+                              int32_t f, float l1_coef, void* dx, float* dWg_s, float* dWu_s,
+                              float* dWd_s, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Test exports. They run the same device code as the calls above on a gate matrix the caller
+ * provides, so packing and routing can be compared bit for bit with an independent reference.
+ */
+
+/* Dense [N, f] copy of a TwELL matrix (zeros outside the packed entries), in a->dtype. */
+TWELL_API twell_status twell_unpack(const twell_packed* a, void* dense_out, int32_t* dev_status, void* stream);
+
+/* TwELL pack of a given gate matrix G [N, f] (device, dtype): keep g > 0, values copied
+ * unchanged. Uses the warp-ballot compaction of the gate epilogue. */
+TWELL_API twell_status twell_pack_from_gate(const void* G, int32_t N, int32_t f, int32_t T, twell_dtype dtype,
+                                  const twell_packed* out, int32_t* dev_status, void* stream);
+
+/* Hybrid routing of a given gate matrix G [N, f] (device, bf16): the routing kernels of
+ * twell_hybrid_fwd applied to pack(G) with tile width 128. Fills ctx->cnt, col, a,
+ * backup_rows, n_backup, A_b (not u, U_b, l1). ws: twell_workspace_bytes(TWELL_OP_HYBRID_ROUTE). */
+TWELL_API twell_status twell_hybrid_route_from_gate(const void* G, int32_t N, int32_t f, int32_t K,
+                                          twell_dtype dtype, const twell_hybrid* ctx, void* ws,
+                                          size_t ws_bytes, void* stream);
+
+/* Dense fp32 G = x Wg_s^T [N, f] (row-major, ld = f) from the same tcgen05 mainloop as
+ * twell_gate_pack, with a plain store epilogue (bf16 inputs only). */
+TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t N, int32_t d, int32_t f,
+                             float* G_out, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Status.
+ */
+
+/* Synchronises `stream`, then returns the code held in *dev_status (TWELL_OK if 0). */
+TWELL_API twell_status twell_read_status(const int32_t* dev_status, void* stream);
+
+/* Static text for a status code. */
+TWELL_API const char* twell_status_string(twell_status s);
+
+/* Number of SMs and the compute capability of the current device (for callers sizing work);
+ * returns TWELL_ERR_CUDA without a device. */
+TWELL_API twell_status twell_device_info(int32_t* sm_count, int32_t* cc_major, int32_t* cc_minor);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_GB300_H */

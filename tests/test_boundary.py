@@ -1,0 +1,120 @@
+"""Host-side tests of the C ABI (no GPU): the library builds for sm_103a, loads, exports every
+function include/twell.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from activation_sparse_ffn_gate_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "twell.h")).read()
+    return sorted(set(re.findall(r"TWELL_API\s+[\w\s\*]+?\b(twell_\w+)\s*\(", src)))
+
+
+def test_header_declarations_are_exported(lib):
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_built_for_sm103a_only():
+    out = os.popen(f"cuobjdump --list-elf {binding.LIB_PATH} 2>/dev/null").read()
+    if not out:
+        pytest.skip("cuobjdump not available")
+    archs = set(re.findall(r"sm_(\d+a?)", out))
+    assert archs == {"103a"}, archs
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.twell_status_string(code)
+    assert lib.twell_status_string(99) == b"unknown status"
+
+
+def test_sizes(lib):
+    assert lib.twell_packed_vals_bytes(8192, 5632, 128, binding.TWELL_BF16) == 8192 * 44 * 128 * 2
+    assert lib.twell_packed_vals_bytes(10, 300, 256, binding.TWELL_F32) == 10 * 2 * 256 * 4
+    assert lib.twell_packed_idx_bytes(10, 300, 64) == 10 * 5 * 64
+    assert lib.twell_packed_cnt_bytes(10, 300, 64) == 10 * 5 * 2
+    assert lib.twell_packed_vals_bytes(10, 0, 64, 0) == 0
+    assert lib.twell_packed_vals_bytes(-1, 10, 64, 0) == 0
+
+
+def _packed(N=4, f=256, T=128, dtype=0, ptr=4096):
+    return binding._Packed(N, f, T, T, dtype, ptr, ptr, ptr)
+
+
+ALIGNED = ctypes.c_void_p(1 << 20)
+STATUS = ctypes.c_void_p(1 << 21)
+
+
+def test_gate_pack_rejects_bad_arguments(lib):
+    p = _packed()
+    call = lambda **kw: lib.twell_gate_pack(  # noqa: E731
+        kw.get("x", ALIGNED), kw.get("w", ALIGNED), kw.get("N", 4), kw.get("d", 64), kw.get("f", 256),
+        kw.get("T", 128), kw.get("dt", 0), ctypes.byref(kw.get("p", p)), None, 0, kw.get("st", STATUS), None)
+    assert call(x=None) == 1
+    assert call(w=None) == 1
+    assert call(st=None) == 1
+    assert call(d=60) == 1  # d not a multiple of 8
+    assert call(N=-1) == 1
+    assert call(f=0) == 1
+    assert call(x=ctypes.c_void_p((1 << 20) + 2)) == 1  # misaligned
+    assert call(T=100, p=_packed(T=100)) == 2  # unsupported tile width
+    assert call(p=_packed(f=255)) == 1  # descriptor shape mismatch
+    assert call(dt=7) == 2
+    assert call(dt=1) == 1  # fp32 inputs with bf16 packed values
+    bad = _packed()
+    bad.cap = 64
+    assert call(p=bad) == 1
+    null_vals = _packed()
+    null_vals.vals = None
+    assert call(p=null_vals) == 1
+
+
+def test_fused_rejects_bad_arguments(lib):
+    p = _packed()
+    call = lambda **kw: lib.twell_ffn_fused_fwd(  # noqa: E731
+        ALIGNED, ALIGNED, ALIGNED, ctypes.byref(kw.get("p", p)), kw.get("N", 4), kw.get("d", 64),
+        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), None, 0, STATUS, None)
+    assert call(y=None) == 1
+    assert call(N=5) == 1
+    assert call(d=12) == 1
+    assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
+    assert call(dt=1) == 1  # fp32 inputs need fp32 packed values
+    assert call(dt=5) == 2
+
+
+def test_pack_unpack_reject_bad_arguments(lib):
+    p = _packed()
+    assert lib.twell_pack_from_gate(None, 4, 256, 128, 0, ctypes.byref(p), STATUS, None) == 1
+    assert lib.twell_pack_from_gate(ALIGNED, 4, 256, 64, 0, ctypes.byref(p), STATUS, None) == 1
+    assert lib.twell_unpack(ctypes.byref(p), None, STATUS, None) == 1
+    assert lib.twell_gate_gemm(ALIGNED, ALIGNED, 4, 64, 250, ALIGNED, STATUS, None) == 1  # f % 4
+
+
+def test_read_status_rejects_null(lib):
+    assert lib.twell_read_status(None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        binding._lib_backup = binding._lib
+        try:
+            binding._lib = None
+            binding.load(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = binding._lib_backup

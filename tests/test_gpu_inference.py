@@ -1,0 +1,255 @@
+"""GPU parity of the inference path against the fp64 oracle, through the C ABI.
+
+- twell_gate_gemm (tcgen05 main loop, plain epilogue) vs exact integer products and fp64 matmul;
+- twell_pack_from_gate / twell_unpack: bit-exact against the oracle's TwELL pack;
+- twell_gate_pack (tcgen05 + ReLU/TwELL epilogue): bit-exact on integer-valued inputs, where
+  the fp32 accumulator is exact in any order;
+- twell_ffn_fused_fwd on an oracle-packed TwELL, and the whole path (gate_pack + fused), within
+  rel-Frobenius <= 5e-3 and max-abs <= 2e-2 * RMS(ref) of the fp64 oracle;
+- the full-size 1.5B-like and 2B-like layers in the launch configuration the bench times,
+  checked on sampled rows;
+- edge cases: empty batch, zero density, full density, rows longer than one list window.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_sparse_ffn_gate_gb300 import binding, build, synthetic
+from parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_dev):
+    build.build()
+    binding.load()
+    binding.status_buffer(cuda_dev).zero_()
+    yield
+    assert binding.twell_read_status() == 0, "device status was raised"
+
+
+def _int_layer(N, d, f, seed, bias_lo=-6, bias_hi=2):
+    """Integer-valued x and Wg_s: every product and partial sum is exact in fp32 and bf16 holds
+    every input exactly."""
+    rng = np.random.default_rng(seed)
+    x = rng.integers(-1, 2, (N, d)).astype(np.float32)
+    x[:, 0] = 1.0
+    W = rng.integers(-1, 2, (f, d)).astype(np.float32)
+    W[:, 0] = rng.integers(bias_lo, bias_hi, f)
+    return x, W
+
+
+def _to(dev, a, dt=torch.bfloat16):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=dt)
+
+
+def _compare_packed(tw, vals, idx, cnt, exact_vals=None):
+    """Compare a device TwELL with an oracle pack: counts, indices and values of slots < cnt."""
+    g_cnt = tw.counts().cpu().numpy()
+    np.testing.assert_array_equal(g_cnt, cnt.astype(np.int64))
+    g_idx = tw.idx.cpu().numpy()
+    g_val = tw.vals.double().cpu().numpy()
+    ref_vals = vals if exact_vals is None else exact_vals
+    N, nt, T = vals.shape
+    mask = np.arange(T)[None, None, :] < cnt[:, :, None]
+    np.testing.assert_array_equal(g_idx[mask], idx[mask])
+    np.testing.assert_array_equal(g_val[mask], ref_vals[mask])
+
+
+# ------------------------------------------------------------------------------------------ GEMM
+
+@pytest.mark.parametrize("N,d,f", [(128, 64, 256), (300, 136, 700), (1000, 520, 1284), (64, 2048, 256)])
+def test_gate_gemm_integer_exact(cuda_dev, N, d, f):
+    x, W = _int_layer(N, d, f, seed=N + d)
+    G = binding.twell_gate_gemm(_to(cuda_dev, x), _to(cuda_dev, W))
+    ref = x.astype(np.float64) @ W.astype(np.float64).T
+    np.testing.assert_array_equal(G.double().cpu().numpy(), ref)
+
+
+def test_gate_gemm_random_vs_fp64(cuda_dev):
+    L = synthetic.uniform_layer(384, 1024, 1536, 128, 0.01, seed=5)
+    G = binding.twell_gate_gemm(_to(cuda_dev, L.x), _to(cuda_dev, L.Wg_s)).double().cpu().numpy()
+    ref = oracle.gate(L.x, L.Wg_s)
+    assert np.abs(G - ref).max() <= 1e-4 * np.abs(ref).max()
+
+
+# ------------------------------------------------------------------------------------------ pack
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("T,N,f", [(64, 77, 300), (128, 130, 1024), (256, 33, 700), (128, 5, 5632)])
+def test_pack_from_gate_bit_exact(cuda_dev, dtype, T, N, f):
+    rng = np.random.default_rng(T * N + f)
+    G = (rng.standard_normal((N, f)) - 1.5).astype(np.float32)
+    G[0] = -1.0
+    G[1 % N] = 1.0
+    G[2 % N, ::4] = -0.0
+    if dtype == torch.bfloat16:
+        G = synthetic.round_bf16_np(G)
+    tw = binding.twell_pack_from_gate(_to(cuda_dev, G, dtype), T)
+    vals, idx, cnt = oracle.twell_pack(G.astype(np.float64), T)
+    _compare_packed(tw, vals, idx, cnt)
+    dense = binding.twell_unpack(tw).double().cpu().numpy()
+    assert np.array_equal(dense, np.where(G > 0, G, 0).astype(np.float64))
+
+
+def test_pack_empty_batch(cuda_dev):
+    G = torch.zeros((0, 256), dtype=torch.bfloat16, device=cuda_dev)
+    tw = binding.twell_pack_from_gate(G, 128)
+    assert tw.cnt.shape == (0, 2)
+
+
+# ------------------------------------------------------------------------------------------ gate + pack
+
+@pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [64, 128, 256])
+@pytest.mark.parametrize("N,d,f", [(300, 136, 700), (257, 256, 1024), (64, 2048, 5632)])
+def test_gate_pack_integer_bit_exact(cuda_dev, T, N, d, f, vals_dtype):
+    x, W = _int_layer(N, d, f, seed=T + N)
+    tw = binding.twell_gate_pack(_to(cuda_dev, x), _to(cuda_dev, W), T, vals_dtype=vals_dtype)
+    G = oracle.gate(x, W)  # exact integers
+    vals, idx, cnt = oracle.twell_pack(G, T)
+    exact = vals if vals_dtype == torch.float32 else oracle.round_bf16(vals)
+    _compare_packed(tw, vals, idx, cnt, exact_vals=exact)
+    assert cnt.sum() > 0
+
+
+@pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
+def test_gate_pack_random_matches_oracle_away_from_zero(cuda_dev, vals_dtype):
+    """On random bf16 layers the kept set can differ from fp64 only where |g| is at the fp32
+    accumulation-error level."""
+    L = synthetic.uniform_layer(512, 1024, 2048, 128, 0.02, seed=9)
+    tw = binding.twell_gate_pack(_to(cuda_dev, L.x), _to(cuda_dev, L.Wg_s), L.T, vals_dtype=vals_dtype)
+    dense = binding.twell_unpack(tw).double().cpu().numpy()
+    G = oracle.gate(L.x, L.Wg_s)
+    ref = np.where(G > 0, G, 0.0)
+    big = np.abs(G) > 1e-3
+    assert np.array_equal(dense[big] > 0, ref[big] > 0)
+    if vals_dtype == torch.float32:
+        np.testing.assert_allclose(dense[big], ref[big], rtol=1e-5, atol=2e-5)
+    else:
+        # fp32 and fp64 accumulators may round to neighbouring bf16 values: one bf16 ulp (2^-7 relative)
+        np.testing.assert_allclose(dense[big], oracle.round_bf16(ref[big]), rtol=2 ** -7, atol=2e-5)
+
+
+def test_gate_pack_f32_path(cuda_dev):
+    L = synthetic.tiny_fp32()
+    tw = binding.twell_gate_pack(_to(cuda_dev, L.x, torch.float32), _to(cuda_dev, L.Wg_s, torch.float32), L.T)
+    dense = binding.twell_unpack(tw).double().cpu().numpy()
+    G = oracle.gate(L.x, L.Wg_s)
+    big = np.abs(G) > 1e-4
+    assert np.array_equal(dense[big] > 0, G[big] > 0)
+    # fp32 accumulation of terms of size ~1 (with cancellation against the bias): ~1e-6 absolute
+    np.testing.assert_allclose(dense[big], np.maximum(G[big], 0), rtol=1e-5, atol=2e-5)
+
+
+# ------------------------------------------------------------------------------------------ fused up+down
+
+def _fused_from_oracle_pack(dev, L, dt, vals_dt=None):
+    """Run the fused kernel on the oracle's own gate activations, packed on the device."""
+    vals_dt = vals_dt or dt
+    G = oracle.gate(L.x, L.Wg_s)
+    Ga = np.where(G > 0, G, 0.0)
+    Gs = synthetic.round_bf16_np(Ga.astype(np.float32)) if vals_dt == torch.bfloat16 else Ga.astype(np.float32)
+    tw = binding.twell_pack_from_gate(_to(dev, Gs, vals_dt), L.T)
+    t = L.torch_inputs(dev, dt)
+    y = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    vals, idx, cnt = oracle.twell_pack(Gs.astype(np.float64), L.T)
+    y_ref = oracle.twell_walk(vals, idx, cnt, L.T, L.x, L.Wu_s, L.Wd_s)
+    return y.double().cpu().numpy(), y_ref
+
+
+def test_fused_tiny_fp32(cuda_dev):
+    L = synthetic.tiny_fp32()
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.float32)
+    rel, mx = assert_close(y, y_ref, "fused fp32")
+    assert rel < 1e-5
+
+
+@pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_fused_bf16_small(cuda_dev, T, vals_dtype):
+    L = synthetic.uniform_layer(200, 512, 1000, T, 0.03, seed=T)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16, vals_dtype)
+    assert_close(y, y_ref, f"fused bf16 T={T}")
+
+
+def test_fused_wide_model_two_chunks_per_thread(cuda_dev):
+    """d_model = 5120: more 16-byte chunks than consumer threads (two chunks per thread)."""
+    L = synthetic.uniform_layer(64, 5120, 768, 128, 0.03, seed=6)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16, torch.float32)
+    assert_close(y, y_ref, "fused d=5120")
+
+
+def test_fused_long_rows_cross_list_windows(cuda_dev):
+    """Rows with more nonzeros than one list window (256) and than the slot ring."""
+    L = synthetic.uniform_layer(24, 256, 2048, 128, 0.5, seed=4)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16)
+    assert_close(y, y_ref, "fused long rows")
+
+
+def test_fused_zero_density_is_exact_zero(cuda_dev):
+    L = synthetic.uniform_layer(130, 256, 512, 128, 0.02, seed=1)
+    L.Wg_s[:, 0] = -1e4
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128)
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_fused_empty_batch(cuda_dev):
+    L = synthetic.uniform_layer(4, 256, 512, 128, 0.02, seed=1)
+    t = L.torch_inputs(cuda_dev)
+    x = t["x"][:0]
+    y = binding.ffn_forward(x, t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128)
+    assert y.shape == (0, 256)
+
+
+# ------------------------------------------------------------------------------------------ end to end
+
+def test_end_to_end_tiny_fp32(cuda_dev):
+    L = synthetic.tiny_fp32()
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=L.T).double().cpu().numpy()
+    assert_close(y, oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), "tiny fp32 end to end")
+
+
+def test_end_to_end_bf16_values(cuda_dev):
+    """bf16-rounded packed values: one more rounding, still inside the bounds."""
+    L = synthetic.uniform_layer(333, 512, 1280, 128, 0.01, seed=3)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128, vals_dtype=torch.bfloat16)
+    assert_close(y.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), "end to end, bf16 values")
+
+
+@pytest.mark.parametrize("p", [0.005, 0.05, 1.0])
+def test_end_to_end_bf16_density(cuda_dev, p):
+    L = synthetic.uniform_layer(333, 512, 1280, 128, min(p, 0.999), seed=int(p * 1000))
+    if p == 1.0:
+        L.Wg_s[:, 0] = 1e4  # every gate on: the plain ReLU FFN with a = g
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128).double().cpu().numpy()
+    assert_close(y, oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"end to end p={p}")
+
+
+def _sampled_rows(N, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, 1, 2, 3, N - 1], rng.choice(N, n, replace=False)]))
+
+
+@pytest.mark.parametrize("which", ["1.5b", "2b"])
+def test_full_size_layers_sampled(cuda_dev, which):
+    """The bench's workloads at full size, in the bench's launch configuration, on sampled rows."""
+    L = synthetic.layer_1p5b() if which == "1.5b" else synthetic.layer_2b()
+    t = L.torch_inputs(cuda_dev)
+    tw = binding.twell_gate_pack(t["x"], t["Wg_s"], L.T)
+    y = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    torch.cuda.synchronize()
+    rows = _sampled_rows(L.N, 24, seed=1)
+    y_ref, G, _ = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows, return_gu=True)
+    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, which)
+    # the row counts agree with the oracle's except where |g| is at the accumulation-error level
+    cnt = tw.counts()[torch.from_numpy(rows).to(cuda_dev)].sum(1).cpu().numpy()
+    lo = (G > 1e-2).sum(1)
+    hi = (G > -1e-2).sum(1)
+    assert np.all(cnt >= lo) and np.all(cnt <= hi)
