@@ -125,6 +125,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of phase completion (for phases known or likely to be complete).
+__device__ __forceinline__ bool mbar_test_now(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase of `bar` with parity `parity` has completed. Every wait is bounded: it
 // gives up when the CTA-wide abort flag is raised by another thread, or after `limit_ns`, in
 // which case it raises the flag and records TWELL_ERR_TIMEOUT in *status. Returns false when
@@ -133,7 +147,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
                                              int32_t* status, uint64_t limit_ns)
 {
     const uint32_t a = smem_u32(bar);
-    if (mbar_test(a, parity)) return true;
+    if (mbar_test_now(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_test(a, parity)) return true;
