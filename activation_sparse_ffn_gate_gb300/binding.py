@@ -30,8 +30,8 @@ STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED
 # Every function the header declares; the CPU tests check that the library exports each one.
 EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cnt_bytes", "twell_workspace_bytes",
            "twell_gate_pack", "twell_ffn_fused_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
-           "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_gate_gemm", "twell_read_status",
-           "twell_status_string", "twell_device_info")
+           "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_gate_gemm", "twell_gemm_test",
+           "twell_read_status", "twell_status_string", "twell_device_info")
 
 
 class TwellError(RuntimeError):
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
                 "twell_hybrid_route_from_gate": (st, [vp, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Hybrid), vp,
                                                       sz, vp]),
                 "twell_gate_gemm": (st, [vp, vp, i32, i32, i32, vp, vp, vp]),
+                "twell_gemm_test": (st, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
                 "twell_read_status": (st, [vp, vp]),
                 "twell_status_string": (ctypes.c_char_p, [ctypes.c_int]),
                 "twell_device_info": (st, [ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
@@ -273,3 +274,116 @@ def twell_device_info():
     sm, ma, mi = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(load().twell_device_info(ctypes.byref(sm), ctypes.byref(ma), ctypes.byref(mi)), "twell_device_info")
     return sm.value, ma.value, mi.value
+
+
+def twell_gemm_test(A: torch.Tensor, B: torch.Tensor, a_mn: bool, b_mn: bool, status=None, stream=None) -> torch.Tensor:
+    """C = A_logical @ B_logical (fp32) where A is [M,K] (or [K,M] if a_mn) and B is [N,K] (or [K,N] if b_mn)."""
+    M = A.shape[1] if a_mn else A.shape[0]
+    K = A.shape[0] if a_mn else A.shape[1]
+    N = B.shape[1] if b_mn else B.shape[0]
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check(load().twell_gemm_test(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(C),
+                                  _ptr(status if status is not None else status_buffer(A.device)), _stream(stream)),
+           "twell_gemm_test")
+    return C
+
+
+# ------------------------------------------------------------------------------------------ hybrid format
+
+@dataclasses.dataclass
+class Hybrid:
+    """A hybrid sparse-block / dense-backup context in device memory (twell_hybrid in include/twell.h)."""
+
+    n_rows: int
+    n_cols: int
+    K: int
+    backup_cap: int
+    a: torch.Tensor  # [N, K] fp32
+    u: torch.Tensor  # [N, K] fp32
+    col: torch.Tensor  # [N, K] int16 storage of uint16 columns
+    cnt: torch.Tensor  # [N] int16 storage of uint16 counts (0xFFFF = backup row)
+    backup_rows: torch.Tensor  # [cap] int32
+    n_backup: torch.Tensor  # [1] int32
+    A_b: torch.Tensor  # [cap, f] fp32
+    U_b: torch.Tensor  # [cap, f] fp32
+    l1: torch.Tensor  # [1] fp32
+    status: torch.Tensor  # [1] int32
+
+    @staticmethod
+    def empty(n_rows, n_cols, K, backup_cap, device=None):
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        cap = max(int(backup_cap), 0)
+        z = dict(device=device)
+        return Hybrid(n_rows, n_cols, K, cap,
+                      torch.empty((n_rows, K), dtype=torch.float32, **z),
+                      torch.empty((n_rows, K), dtype=torch.float32, **z),
+                      torch.empty((n_rows, K), dtype=torch.int16, **z),
+                      torch.empty((n_rows,), dtype=torch.int16, **z),
+                      torch.empty((max(cap, 1),), dtype=torch.int32, **z),
+                      torch.zeros((1,), dtype=torch.int32, **z),
+                      torch.empty((max(cap, 1), n_cols), dtype=torch.float32, **z),
+                      torch.empty((max(cap, 1), n_cols), dtype=torch.float32, **z),
+                      torch.zeros((1,), dtype=torch.float32, **z),
+                      torch.zeros((1,), dtype=torch.int32, **z))
+
+    def counts(self) -> torch.Tensor:
+        return self.cnt.to(torch.int32) & 0xFFFF
+
+    def cols(self) -> torch.Tensor:
+        return self.col.to(torch.int32) & 0xFFFF
+
+    def c_struct(self) -> _Hybrid:
+        return _Hybrid(self.n_rows, self.n_cols, self.K, self.backup_cap, TWELL_BF16, self.a.data_ptr(),
+                       self.u.data_ptr(), self.col.data_ptr(), self.cnt.data_ptr(), self.backup_rows.data_ptr(),
+                       self.n_backup.data_ptr(), self.A_b.data_ptr(), self.U_b.data_ptr(), self.l1.data_ptr(),
+                       self.status.data_ptr())
+
+
+def _workspace(op, N, d, f, K, cap, device, ws=None):
+    nbytes = twell_workspace_bytes(op, N, d, f, 0, K, cap)
+    if ws is not None and ws.numel() >= nbytes:
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def twell_hybrid_route_from_gate(G: torch.Tensor, K: int, backup_cap: int, ctx: Optional[Hybrid] = None, ws=None,
+                                 stream=None) -> Hybrid:
+    N, f = G.shape
+    ctx = ctx if ctx is not None else Hybrid.empty(N, f, K, backup_cap, G.device)
+    ws = _workspace(OP_HYBRID_ROUTE, N, 8, f, K, ctx.backup_cap, G.device, ws)
+    s = ctx.c_struct()
+    _check(load().twell_hybrid_route_from_gate(_ptr(G), N, f, K, TWELL_BF16, ctypes.byref(s), _ptr(ws), ws.numel(),
+                                               _stream(stream)), "twell_hybrid_route_from_gate")
+    return ctx
+
+
+def twell_hybrid_fwd(x, Wg_s, Wu_s, Wd_s, K: int, backup_cap: int, l1_coef: float = 2e-5,
+                     ctx: Optional[Hybrid] = None, y=None, ws=None, stream=None):
+    """Hybrid-format training forward: returns (y, ctx)."""
+    N, d = x.shape
+    f = Wg_s.shape[0]
+    ctx = ctx if ctx is not None else Hybrid.empty(N, f, K, backup_cap, x.device)
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    ws = _workspace(OP_HYBRID_FWD, N, d, f, K, ctx.backup_cap, x.device, ws)
+    s = ctx.c_struct()
+    _check(load().twell_hybrid_fwd(_ptr(x), _ptr(Wg_s), _ptr(Wu_s), _ptr(Wd_s), N, d, f, K, ctypes.c_float(l1_coef),
+                                   TWELL_BF16, ctypes.byref(s), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "twell_hybrid_fwd")
+    return y, ctx
+
+
+def twell_hybrid_bwd(x, Wg_s, Wu_s, Wd_s, ctx: Hybrid, dy, l1_coef: float = 2e-5, dx=None, dWg_s=None, dWu_s=None,
+                     dWd_s=None, ws=None, stream=None):
+    """Hybrid-format training backward: returns (dx, dWg_s, dWu_s, dWd_s), all fp32."""
+    N, d = x.shape
+    f = Wg_s.shape[0]
+    dx = dx if dx is not None else torch.empty((N, d), dtype=torch.float32, device=x.device)
+    dWg_s = dWg_s if dWg_s is not None else torch.empty((f, d), dtype=torch.float32, device=x.device)
+    dWu_s = dWu_s if dWu_s is not None else torch.empty((f, d), dtype=torch.float32, device=x.device)
+    dWd_s = dWd_s if dWd_s is not None else torch.empty((f, d), dtype=torch.float32, device=x.device)
+    ws = _workspace(OP_HYBRID_BWD, N, d, f, ctx.K, ctx.backup_cap, x.device, ws)
+    s = ctx.c_struct()
+    _check(load().twell_hybrid_bwd(_ptr(x), _ptr(Wg_s), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), _ptr(dy), N, d, f,
+                                   ctypes.c_float(l1_coef), _ptr(dx), _ptr(dWg_s), _ptr(dWu_s), _ptr(dWd_s), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "twell_hybrid_bwd")
+    return dx, dWg_s, dWu_s, dWd_s

@@ -344,4 +344,7 @@ inline twell_status check_packed(const twell_packed* p, int32_t N, int32_t f, in
     return TWELL_OK;
 }
 inline bool dtype_ok(twell_dtype dt) { return dt == TWELL_BF16 || dt == TWELL_F32; }
+
+// TwELL pack of a bf16 gate matrix into a TwELL with fp32 values (exact widening; twell_pack.cu).
+twell_status pack_gate_widened(const void* G, int N, int f, const twell_packed* out, int32_t* status, cudaStream_t s);
 }  // namespace twell_host

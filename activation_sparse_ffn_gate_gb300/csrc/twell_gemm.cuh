@@ -29,13 +29,15 @@ enum class Epi : int {
     StoreBF16 = 2,   // out[m, n] = bf16(acc)
     ScatterBF16 = 3, // out[rowmap[m], n] = bf16(acc)
     AccumF32 = 4,    // out[m, n] += acc (fp32)
+    ScatterF32 = 5,  // out[rowmap[m], n] = acc (fp32)
 };
 
 struct GemmArgs {
     int M, N, K;             // extents; M and K are upper bounds when M_dyn / K_dyn are given
     const int32_t* M_dyn;    // optional device scalar: M = min(M, *M_dyn)
     const int32_t* K_dyn;    // optional device scalar: K = min(K, *K_dyn)
-    int kb_split;            // k-blocks >= kb_split read B from the second map, k restarting at 0
+    int kb_split;            // B source period in k-blocks: block kb reads map (kb / kb_split) & 1 at
+                             // k-block kb % kb_split (one map: kb_split larger than every kb)
     void* out;               // epilogue output
     int64_t ldo;             // its leading dimension (elements)
     const int32_t* rowmap;   // ScatterBF16: destination row of each m
@@ -148,12 +150,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d(a, &tmA, m0, k0, &full[stage]);
                         tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[stage]);
                     }
-                    const CUtensorMap* tb = &tmB;
-                    int kk = k0;
-                    if (kb >= g.kb_split) {
-                        tb = &tmB2;
-                        kk = (kb - g.kb_split) * kBK;
-                    }
+                    const CUtensorMap* tb = ((kb / g.kb_split) & 1) ? &tmB2 : &tmB;
+                    const int kk = (kb % g.kb_split) * kBK;
                     if constexpr (!B_MN) {
                         tma_load_2d(b, tb, kk, n0, &full[stage]);
                     } else {
@@ -263,8 +261,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int col0 = n0 + ch * 32;
                     if (!row_ok || col0 >= g.N) continue;
                     const int nvalid = min(32, g.N - col0);
-                    if constexpr (EPI == Epi::StoreF32 || EPI == Epi::AccumF32) {
-                        float* o = static_cast<float*>(g.out) + static_cast<size_t>(row) * g.ldo + col0;
+                    if constexpr (EPI == Epi::StoreF32 || EPI == Epi::AccumF32 || EPI == Epi::ScatterF32) {
+                        const int orow = (EPI == Epi::ScatterF32) ? g.rowmap[row] : row;
+                        float* o = static_cast<float*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0;
                         if (nvalid == 32) {
 #pragma unroll
                             for (int k = 0; k < 32; k += 4) {

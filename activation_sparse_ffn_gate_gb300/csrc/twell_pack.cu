@@ -8,8 +8,8 @@
 
 namespace twell {
 
-template <typename E>
-__global__ void pack_from_gate_kernel(const E* __restrict__ G, int N, int f, int T, int nt, E* __restrict__ vals,
+template <typename E, typename VO = E>
+__global__ void pack_from_gate_kernel(const E* __restrict__ G, int N, int f, int T, int nt, VO* __restrict__ vals,
                                       uint8_t* __restrict__ idx, uint16_t* __restrict__ cnt)
 {
     const int lane = threadIdx.x & 31;
@@ -30,7 +30,7 @@ __global__ void pack_from_gate_kernel(const E* __restrict__ G, int N, int f, int
         const unsigned m = __ballot_sync(0xffffffffu, keep);
         const int pos = c + __popc(m & ((1u << lane) - 1u));
         if (keep) {
-            vals[slot + pos] = g;
+            vals[slot + pos] = static_cast<VO>(Elem<E>::to_f(g));
             idx[slot + pos] = static_cast<uint8_t>(k);
         }
         c += __popc(m);
@@ -96,6 +96,19 @@ extern "C" twell_status twell_pack_from_gate(const void* G, int32_t N, int32_t f
     else
         twell::pack_from_gate_kernel<float><<<warp_blocks(warps, 8), 256, 0, s>>>(
             static_cast<const float*>(G), N, f, T, nt, static_cast<float*>(out->vals), out->idx, out->cnt);
+    return launch_status();
+}
+
+twell_status twell_host::pack_gate_widened(const void* G, int N, int f, const twell_packed* out, int32_t* status,
+                                          cudaStream_t s)
+{
+    (void)status;
+    if (out == nullptr || out->dtype != TWELL_F32) return TWELL_ERR_INVALID;
+    const int T = out->tile, nt = (f + T - 1) / T;
+    const long long warps = static_cast<long long>(N) * nt;
+    if (N == 0) return TWELL_OK;
+    twell::pack_from_gate_kernel<__nv_bfloat16, float><<<warp_blocks(warps, 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(G), N, f, T, nt, static_cast<float*>(out->vals), out->idx, out->cnt);
     return launch_status();
 }
 

@@ -90,18 +90,20 @@ typedef struct {
 /* The hybrid training format ([TG] "Обучение"; [TC] §3): each row either fits in one
  * globally aligned sparse block of fixed capacity K or, when it has more than K nonzeros,
  * goes to a dense backup buffer. All pointers are caller-owned device memory.
- *   cnt[n_rows]          nonzeros of a light row (<= K), or 0xFFFF for a backup row;
- *   col[n_rows*K]        light rows: kept columns in ascending order, slots >= cnt hold 0;
- *   a  [n_rows*K]        light rows: a = ReLU(g) at those columns, slots >= cnt hold +0;
- *   u  [n_rows*K]        light rows: u = x Wu_s^T at those columns (filled by hybrid_fwd);
- *   backup_rows[backup_cap]  backup row indices in ascending order;
- *   n_backup[1]          number of overflow rows (may exceed backup_cap: then the call
- *                        reports TWELL_ERR_BACKUP_FULL and only backup_cap rows are stored);
- *   A_b[backup_cap*n_cols]   dense a rows of the backup rows (dtype);
- *   U_b[backup_cap*n_cols]   dense u rows of the backup rows (filled by hybrid_fwd);
- *   l1[1]                L1 term lambda * mean|h| (fp32, filled by hybrid_fwd);
- *   dev_status[1]        device status word (see the conventions above).
- * Entries a/u/A_b/U_b use the context's dtype (TWELL_BF16 only for the hybrid calls). */
+ *   cnt[n_rows]          uint16: nonzeros of a light row (<= K), or 0xFFFF for a backup row;
+ *   col[n_rows*K]        uint16: light rows' kept columns in ascending order (slots >= cnt: 0);
+ *   a  [n_rows*K]        fp32: a = ReLU(g) at those columns (slots >= cnt: +0);
+ *   u  [n_rows*K]        fp32: u = x Wu_s^T at those columns (filled by hybrid_fwd);
+ *   backup_rows[backup_cap]  int32: backup row indices in ascending order;
+ *   n_backup[1]          int32: number of overflow rows (may exceed backup_cap: then the call
+ *                        reports TWELL_ERR_BACKUP_FULL, only backup_cap rows are stored and the
+ *                        outputs of the other overflow rows are undefined);
+ *   A_b[backup_cap*n_cols]   fp32: dense a rows of the backup rows;
+ *   U_b[backup_cap*n_cols]   fp32: dense u rows of the backup rows (filled by hybrid_fwd);
+ *   l1[1]                fp32: L1 term lambda * mean|h| (filled by hybrid_fwd);
+ *   dev_status[1]        int32 device status word (see the conventions above).
+ * Rows of a light row that are not written are never read; a row is in exactly one of the sparse
+ * block and the backup. dtype must be TWELL_BF16 (the element type of x, weights, y, dy, dx). */
 typedef struct {
     int32_t n_rows;
     int32_t n_cols;
@@ -157,12 +159,14 @@ TWELL_API twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, cons
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);
 
-/* Hybrid-format training forward ([TG] "Обучение"; [TC] §3), bf16 only: gate GEMM + TwELL pack,
+/* Hybrid-format training forward ([TG] "Обучение"; [TC] §3), bf16 only (d_ff a multiple of
+ * 64, d_model at most 4096, d_ff at most 65535): gate GEMM + TwELL pack,
  * routing of each row to the sparse block (nnz <= K) or to the dense backup (nnz > K, in
  * ascending row order), the up/down products (gathered rows of Wu_s / Wd_s for light rows,
  * dense tensor-core GEMMs for backup rows), y [N, d], and the L1 term
  * l1_coef * mean|h| over all N*f entries of h ([AIM] ¶4; [PUL] ¶4) into *ctx->l1.
  * ctx describes caller-owned buffers for N = ctx->n_rows, f = ctx->n_cols.
+ * ws: at least twell_workspace_bytes(TWELL_OP_HYBRID_FWD, N, d, f, 0, K, backup_cap) bytes.
  */
 TWELL_API twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const void* Wu_s, const void* Wd_s,
                               int32_t N, int32_t d, int32_t f, int32_t K, float l1_coef,
@@ -173,13 +177,17 @@ TWELL_API twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const v
  * sparse rows), bf16 storage: given the context filled by twell_hybrid_fwd and dy [N, d],
  * computes the gradients of  <y, dy> + l1_coef * mean|h| :
  *   dh = dy_r . Wd_s[j] + l1_coef * sgn(h) / (N f),  du = dh * a,  dg = dh * u  (at kept entries)
- *   dx [N, d] (bf16)          = sum_j du * Wu_s[j] + dg * Wg_s[j]
+ *   dx [N, d] (fp32)          = sum_j du * Wu_s[j] + dg * Wg_s[j]
  *   dWg_s, dWu_s, dWd_s [f, d] (fp32, overwritten) = sum_r dg x_r, du x_r, h dy_r.
- * Backup rows use dense tensor-core GEMMs for the same terms.
+ * Gradients are written in fp32: a bf16 copy of dx rounds its largest element by up to 2^-8 of
+ * itself, more than the accuracy the layer is held to.
+ * Backup rows use dense tensor-core GEMMs for the same terms. Same shape limits as the forward.
+ * ws: at least twell_workspace_bytes(TWELL_OP_HYBRID_BWD, N, d, f, 0, K, backup_cap) bytes; it
+ * need not hold anything from the forward call (the context carries what the backward needs).
  */
 TWELL_API twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const void* Wu_s, const void* Wd_s,
                               const twell_hybrid* ctx, const void* dy, int32_t N, int32_t d,
-                              int32_t f, float l1_coef, void* dx, float* dWg_s, float* dWu_s,
+                              int32_t f, float l1_coef, float* dx, float* dWg_s, float* dWu_s,
                               float* dWd_s, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
@@ -206,6 +214,14 @@ TWELL_API twell_status twell_hybrid_route_from_gate(const void* G, int32_t N, in
  * twell_gate_pack, with a plain store epilogue (bf16 inputs only). */
 TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t N, int32_t d, int32_t f,
                              float* G_out, int32_t* dev_status, void* stream);
+
+/* C[M, N] = A * B in fp32 from the tcgen05 GEMM used by the hybrid backup rows, bf16 operands:
+ * A is [M, K] row-major (a_mn = 0) or [K, M] row-major (a_mn = 1); B is [N, K] row-major
+ * (b_mn = 0) or [K, N] row-major (b_mn = 1); C is [M, N] row-major. N and the contiguous
+ * extents must be multiples of 8. */
+TWELL_API twell_status twell_gemm_test(const void* A, const void* B, int32_t M, int32_t N, int32_t K,
+                                       int32_t a_mn, int32_t b_mn, float* C, int32_t* dev_status,
+                                       void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * Status.

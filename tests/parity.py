@@ -2,13 +2,13 @@
 
 Bounds (bf16 storage, fp32 accumulation, against the fp64 oracle):
   * relative Frobenius error  ||got - ref||_F / ||ref||_F <= 5e-3, over the whole tensor;
-  * max-abs error <= 2e-2 * RMS(reference), with the RMS taken per row of the output (a token row
-    of y or dx, a hidden-unit row of dW): each row is an independent result of the layer. A row
-    whose reference is exactly zero is held to 2e-2 * the tensor's RMS.
-Why per row: the layer's outputs are heavy-tailed across rows (a few tokens carry many more
-nonzeros), with max|y| up to ~20x the global RMS, and storing y in bf16 alone moves an element by
-up to 2^-9 of itself; against a global RMS even the correctly rounded fp64 result fails the bound
-(tests/test_tolerance_reading.py shows it), so the global reading cannot be what is meant.
+  * max-abs error <= 2e-2 * max(RMS of the row, RMS of the tensor), per row of the output (a token
+    row of y or dx, a hidden-unit row of dW): rows at or below the tensor's RMS are held to the
+    bound with the tensor's RMS, rows above it to the bound with their own RMS.
+Why: the layer's outputs are heavy-tailed across rows (a few tokens carry many more nonzeros),
+with max|y| up to ~12x the tensor's RMS, and storing y in bf16 alone moves an element by up to
+2^-8 of itself; against the tensor's RMS alone even the correctly rounded fp64 result fails the
+bound (tests/test_tolerance_reading.py shows it), so a heavy row is held to its own RMS.
 """
 import numpy as np
 
@@ -27,8 +27,8 @@ def errors(got, ref):
     nrm = np.linalg.norm(ref)
     rel = np.linalg.norm(diff) / nrm if nrm > 0 else np.linalg.norm(diff)
     rms_all = np.sqrt((ref ** 2).mean())
-    rms_row = np.sqrt((ref ** 2).mean(axis=1))
-    rms_row = np.where(rms_row > 0, rms_row, rms_all if rms_all > 0 else 1.0)
+    rms_row = np.maximum(np.sqrt((ref ** 2).mean(axis=1)), rms_all)
+    rms_row = np.where(rms_row > 0, rms_row, 1.0)
     mx = (np.abs(diff).max(axis=1) / rms_row).max()
     return rel, mx
 
