@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED
 # Every function the header declares; the CPU tests check that the library exports each one.
 EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cnt_bytes", "twell_workspace_bytes",
            "twell_gate_pack", "twell_ffn_fused_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
-           "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_gate_gemm", "twell_gemm_test",
+           "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
+           "twell_gate_gemm", "twell_gemm_test",
            "twell_read_status", "twell_status_string", "twell_device_info")
 
 
@@ -85,6 +86,7 @@ def load(path: str = LIB_PATH):
                 "twell_pack_from_gate": (st, [vp, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Packed), vp, vp]),
                 "twell_hybrid_route_from_gate": (st, [vp, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Hybrid), vp,
                                                       sz, vp]),
+                "twell_hybrid_route_noalloc": (st, [ctypes.POINTER(_Packed), i32, ctypes.POINTER(_Hybrid), vp]),
                 "twell_gate_gemm": (st, [vp, vp, i32, i32, i32, vp, vp, vp]),
                 "twell_gemm_test": (st, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
                 "twell_read_status": (st, [vp, vp]),
@@ -387,3 +389,12 @@ def twell_hybrid_bwd(x, Wg_s, Wu_s, Wd_s, ctx: Hybrid, dy, l1_coef: float = 2e-5
                                    ctypes.c_float(l1_coef), _ptr(dx), _ptr(dWg_s), _ptr(dWu_s), _ptr(dWd_s), _ptr(ws),
                                    ws.numel(), _stream(stream)), "twell_hybrid_bwd")
     return dx, dWg_s, dWu_s, dWd_s
+
+
+def twell_hybrid_route_noalloc(a: TwELL, K: int, ctx: Hybrid, stream=None) -> Hybrid:
+    """Route a packed TwELL (fp32 values, tile 128) into `ctx` with no workspace and no allocation
+    in the library (see twell_hybrid_route_noalloc in include/twell.h for who needs this)."""
+    sa, sc = a.c_struct(), ctx.c_struct()
+    _check(load().twell_hybrid_route_noalloc(ctypes.byref(sa), K, ctypes.byref(sc), _stream(stream)),
+           "twell_hybrid_route_noalloc")
+    return ctx

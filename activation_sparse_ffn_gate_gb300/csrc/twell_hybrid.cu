@@ -11,6 +11,8 @@
 //
 // Loss whose gradients are computed: L = <y, dy> + lambda * mean|h| over all N*f entries of h
 // ([AIM] ¶4; [PUL] ¶4: L1 coefficient 2e-5 on the hidden activations).
+#include <mutex>
+
 #include "twell_gemm.cuh"
 
 namespace twell {
@@ -964,4 +966,70 @@ extern "C" twell_status twell_gemm_test(const void* A, const void* B, int32_t M,
     if (a_mn && !b_mn) return launch_gemm<256, true, false, twell::Epi::StoreF32>(Ao, Bo, nullptr, g, s);
     if (!a_mn && b_mn) return launch_gemm<256, false, true, twell::Epi::StoreF32>(Ao, Bo, nullptr, g, s);
     return launch_gemm<256, true, true, twell::Epi::StoreF32>(Ao, Bo, nullptr, g, s);
+}
+
+// ------------------------------------------------------------------------------------------
+// Routing without any allocation or workspace.
+//
+// Some callers cannot hand the library a workspace or let anything allocate device memory: code
+// that runs while a CUDA graph is being captured (cudaMalloc is not allowed during capture), code
+// living inside a framework whose allocator owns all device memory, and latency-critical loops
+// where a cudaMalloc / cudaFree would synchronise the device. For them the routing of an already
+// packed TwELL matrix keeps its only scratch -- the number of overflow rows of each 128-row block
+// -- in the fixed array below. The array lives in every GPU that loads the library until the
+// process exits, and holds the previous call's counts (every call rewrites the entries it uses).
+
+namespace {
+
+constexpr int kNoAllocBlocks = 8192;  // 128-row blocks: at most 1,048,576 token rows per call
+static __device__ __align__(256) int32_t g_noalloc_blk_counts[kNoAllocBlocks];
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[64] = {};
+
+// Device address of the array on the current device, looked up once per device.
+twell_status noalloc_scratch(int32_t** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TWELL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_blk_counts) != cudaSuccess || p == nullptr) return TWELL_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return TWELL_OK;
+}
+
+}  // namespace
+
+extern "C" twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_t K, const twell_hybrid* ctx,
+                                                   void* stream)
+{
+    if (a == nullptr || ctx == nullptr) return TWELL_ERR_INVALID;
+    const int N = a->n_rows, f = a->n_cols;
+    if (N < 0 || f <= 0 || f > 65535 || K < 0 || K > twell::kMaxK) return TWELL_ERR_INVALID;
+    if (a->dtype != TWELL_F32 || a->tile != twell::kHybTile) return TWELL_ERR_UNSUPPORTED;
+    twell_status st = check_packed(a, N, f, twell::kHybTile, TWELL_F32);
+    if (st != TWELL_OK) return st;
+    st = check_hybrid(ctx, N, f, K);
+    if (st != TWELL_OK) return st;
+    const int nblk = (N + twell::kRouteRows - 1) / twell::kRouteRows;
+    if (nblk > kNoAllocBlocks) return TWELL_ERR_UNSUPPORTED;  // more rows than the fixed scratch covers
+    if (N == 0) return TWELL_OK;
+    int32_t* blk = nullptr;
+    st = noalloc_scratch(&blk);
+    if (st != TWELL_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int nt = (f + twell::kHybTile - 1) / twell::kHybTile;
+    twell::route_rows_kernel<<<nblk, 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx, a->cnt, N, f, nt, K,
+                                                  static_cast<float*>(ctx->a), ctx->col, ctx->cnt, blk, nullptr,
+                                                  ctx->dev_status);
+    if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
+    twell::route_backup_kernel<<<nblk, 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx, a->cnt, ctx->cnt, blk,
+                                                    nblk, N, f, nt, ctx->backup_cap, nullptr, 8, ctx->backup_rows,
+                                                    ctx->n_backup, static_cast<float*>(ctx->A_b), nullptr,
+                                                    ctx->dev_status);
+    return launch_status();
 }

@@ -215,6 +215,24 @@ TWELL_API twell_status twell_hybrid_route_from_gate(const void* G, int32_t N, in
 TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t N, int32_t d, int32_t f,
                              float* G_out, int32_t* dev_status, void* stream);
 
+/* Hybrid routing of an already packed TwELL matrix `a` (fp32 values, tile 128, as written by
+ * twell_gate_pack or twell_pack_from_gate) into ctx -- the same kernels and the same results as
+ * the routing inside twell_hybrid_fwd / twell_hybrid_route_from_gate (ctx->cnt, col, a,
+ * backup_rows, n_backup, A_b; not u, U_b, l1) -- without any workspace and without allocating.
+ * The pages have no counterpart: this call exists for callers that cannot allocate device memory
+ * or pass a workspace (code recorded into a CUDA graph, where cudaMalloc is not allowed during
+ * capture; code inside a framework whose allocator owns all device memory; latency-critical
+ * loops where an allocation would synchronise the device).
+ * Its only scratch, the overflow-row count of each 128-row block, is a fixed array of 8192 int32
+ * inside the library: every GPU that loads the library keeps it (32 KB) until the process exits.
+ * Limit: a->n_rows <= 1,048,576; larger inputs return TWELL_ERR_UNSUPPORTED before any launch.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress), so make
+ * that first call before any stream capture. All calls share the one array: two calls that
+ * overlap on the GPU (different streams, no ordering between them) race and give wrong routes;
+ * order them on one stream or with events. */
+TWELL_API twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_t K,
+                                                  const twell_hybrid* ctx, void* stream);
+
 /* C[M, N] = A * B in fp32 from the tcgen05 GEMM used by the hybrid backup rows, bf16 operands:
  * A is [M, K] row-major (a_mn = 0) or [K, M] row-major (a_mn = 1); B is [N, K] row-major
  * (b_mn = 0) or [K, N] row-major (b_mn = 1); C is [M, N] row-major. N and the contiguous
