@@ -42,6 +42,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--no-train", action="store_true", help="skip the hybrid training-step measurement")
+    p.add_argument("--train-steps", type=int, default=20)
     return p.parse_args()
 
 
@@ -359,6 +361,10 @@ def run_ours(a, rank, world):
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
     binding.check_device_status("e2e", status)
 
+    train = None
+    if not a.no_train:
+        train = train_step_measure(a, dev, flush, peaks)
+
     cpu = None
     if not a.no_cpu_baseline:
         rate, n_rows, secs = cpu_oracle_rate(L)
@@ -380,6 +386,7 @@ def run_ours(a, rank, world):
                                          "128-token tile + y) / HBM peak)"},
         "kernels_ms": {"twell_gate_pack": mg, "twell_ffn_fused_fwd": mf},
         "vs_dense_cublas": dense,
+        "train_step": train,
         "cpu_baseline": cpu,
         "e2e": {"value": N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": N * d * 2,
                 "d2h_bytes_per_step": N * d * 2, "ms_per_step": e2e_ms},
@@ -390,6 +397,70 @@ def run_ours(a, rank, world):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def train_step_measure(a, dev, flush, peaks):
+    """The hybrid training step on the 2B-like layer (N=16384, d=2560, f=6912, K=64, L1 2e-5):
+    twell_hybrid_fwd + twell_hybrid_bwd, against a dense cuBLAS bf16 step of the same layer."""
+    import torch
+
+    from activation_sparse_ffn_gate_gb300 import binding, synthetic
+    L = synthetic.train_2b()
+    t = L.torch_inputs(dev)
+    x, Wg, Wu, Wd, dy = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], t["dy"]
+    N, d, f, K = L.N, L.d, L.f, L.K
+    cap = N // 8
+    ctx = binding.Hybrid.empty(N, f, K, cap, dev)
+    ws_f = torch.empty(binding.twell_workspace_bytes(binding.OP_HYBRID_FWD, N, d, f, 0, K, cap), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(binding.twell_workspace_bytes(binding.OP_HYBRID_BWD, N, d, f, 0, K, cap), dtype=torch.uint8,
+                       device=dev)
+    y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((N, d), dtype=torch.float32, device=dev)
+    dW = [torch.empty((f, d), dtype=torch.float32, device=dev) for _ in range(3)]
+
+    def step():
+        binding.twell_hybrid_fwd(x, Wg, Wu, Wd, K, cap, L.l1_coef, ctx=ctx, y=y, ws=ws_f)
+        binding.twell_hybrid_bwd(x, Wg, Wu, Wd, ctx, dy, L.l1_coef, dx=dx, dWg_s=dW[0], dWu_s=dW[1], dWd_s=dW[2],
+                                 ws=ws_b)
+
+    def dense():
+        g = x @ Wg.T
+        u = x @ Wu.T
+        a_ = torch.relu(g)
+        h = a_ * u
+        yd = h @ Wd
+        dh = dy @ Wd.T + L.l1_coef / (N * f) * torch.sign(h)
+        du = dh * a_
+        dg = dh * u * (g > 0)
+        dxd = du @ Wu + dg @ Wg
+        return yd, dxd, h.T @ dy, du.T @ x, dg.T @ x
+
+    def timed(fn, n):
+        for _ in range(3):
+            flush.fill_(1)
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    ms = timed(step, a.train_steps)
+    code = binding.twell_read_status(ctx.status)
+    if code != 0:
+        raise RuntimeError(f"hybrid training step reported status {code}")
+    ms_dense = timed(dense, max(5, a.train_steps // 2))
+    nb = int(ctx.n_backup.item())
+    return {"workload": f"train2b_N{N}_d{d}_f{f}_K{K} (hybrid fwd + bwd, L1 {L.l1_coef})", "ms": ms,
+            "tokens_per_s": N / (ms * 1e-3), "backup_rows": nb, "backup_frac": nb / N,
+            "dense_cublas_ms": ms_dense, "speedup_vs_dense": ms_dense / ms,
+            "launches_per_step": 23, "l2": "flushed before every step"}
 
 
 def main():
