@@ -145,6 +145,24 @@ def status_buffer(device=None) -> torch.Tensor:
     return buf
 
 
+_fused_ws = {}
+
+
+def fused_workspace(device=None, stream=None) -> torch.Tensor:
+    """The workspace twell_ffn_fused_fwd needs (its row-ticket counter), one per device and stream:
+    calls on one stream run one after the other, so they can share it."""
+    dev = torch.device(device if device is not None else torch.cuda.current_device())
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    key = (dev.index, _stream(stream).value or 0)
+    buf = _fused_ws.get(key)
+    if buf is None:
+        n = load().twell_workspace_bytes(OP_FFN_FUSED_FWD, 1, 8, 8, 8, 0, 0)
+        buf = torch.zeros(n, dtype=torch.uint8, device=dev)
+        _fused_ws[key] = buf
+    return buf
+
+
 def twell_read_status(status: Optional[torch.Tensor] = None, stream=None, reset: bool = True) -> int:
     """Synchronise the stream and return the device status code (optionally clearing it)."""
     status = status if status is not None else status_buffer()
@@ -215,14 +233,15 @@ def twell_gate_pack(x: torch.Tensor, Wg_s: torch.Tensor, T: int = 128, out: Opti
 
 def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, a: TwELL,
                         y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                        stream=None) -> torch.Tensor:
+                        stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Fused up+down projection over the packed nonzeros: y = (a * (x Wu_s^T)) Wd_s."""
     N, d = x.shape
     f = Wu_s.shape[0]
     y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    ws = ws if ws is not None else fused_workspace(x.device, stream)
     s = a.c_struct()
     _check(load().twell_ffn_fused_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), N, d, f,
-                                      _dtype_code(x.dtype), _ptr(y), None, 0,
+                                      _dtype_code(x.dtype), _ptr(y), _ptr(ws), ws.numel(),
                                       _ptr(status if status is not None else status_buffer(x.device)),
                                       _stream(stream)),
            "twell_ffn_fused_fwd")

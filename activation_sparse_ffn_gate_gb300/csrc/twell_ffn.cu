@@ -5,545 +5,763 @@
 // accumulates y_r += h * Wd_s[j] in fp32 registers; the hidden activation never leaves the SM
 // ([AIM] ¶3; [TG] "Инференс"; [PUL] ¶3; [TC] §2).
 //
-// GB300 layout: one persistent CTA per SM, rows assigned round-robin. The CTA is split into
-//   - a metadata warp that reads the TwELL counts, indices and values of its rows and writes
-//     them as an item stream (row record, then the row's nonzeros) into a shared-memory ring,
-//     running ahead of use;
-//   - an issuer warp that walks the items and streams the needed weight rows (Wu_s[j] and
-//     Wd_s[j], d*2 bytes each) and each row's x into shared-memory rings with cp.async.bulk
-//     copies completing on mbarriers (weights with an L2 evict-last hint so they stay resident,
-//     x with evict-first). It runs up to S nonzeros ahead, across row boundaries, so about
-//     S*4*d bytes of gathers are in flight;
-//   - consumer warps (one thread per 16-byte chunk of d_model) that take the staged nonzeros in
-//     batches of one nonzero per warp: each warp forms the whole dot x_r . Wu_s[j] of its nonzero
-//     (warp shuffles only), one named barrier publishes the batch's h = a*u (and agrees on
-//     abort), and every thread applies the batch's rank-1 updates h * Wd_s[j] to its fp32 slice
-//     of y_r, then frees the slots.
-// Every wait is bounded; on a timeout the CTA records TWELL_ERR_TIMEOUT, all roles leave their
-// loops together, and the producer waits (bounded) for its copies in flight before exit.
+// GB300 layout. The work is a gather of 2 * d_model * sizeof(E) bytes per nonzero out of weight
+// rows that stay resident in the 129 MB L2, plus ~2 * d_model multiply-adds per nonzero. Plain
+// loads into registers reach 10-20 TB/s on random 4 KB rows (whole-row cp.async.bulk copies
+// stayed near 2.8 TB/s on the same pattern), so weight rows go straight into registers; what is
+// left to engineer is keeping enough bytes in flight per SM while spending few instructions.
+//
+// Both kernels share the row stream (RowStream below): one token row is owned by a group of G
+// warps; x_r is staged in shared memory by cp.async one segment ahead (three buffers per warp);
+// the TwELL metadata runs one 32-nonzero segment ahead: counts of the next row are loaded a row
+// ahead, scanned into per-tile offsets in shared memory, and one lane per nonzero finds its tile
+// by binary search and loads its index and value into registers. With G = 1 warps take rows from
+// a ticket counter (the caller's workspace, cleared on the launch stream), so per-token nonzero
+// counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
+//
+// ffn_mma_kernel (bf16, d_model a multiple of 256 up to 2048): nonzeros are taken in batches of
+// up to 8 of one row. The 8 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
+// mma.sync m16n8k16 with the batch's weight rows as the 8 columns of B and x_r in every row of
+// A (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
+// permuted the same way on both sides, so that each lane reads 32 contiguous bytes). The
+// rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's 64 columns. Weight
+// rows move in 4 KB steps (32 bytes per lane per load, so four lanes cover a 128-byte line)
+// through a three-step register ring, two steps ahead of use across batch and row boundaries.
+//
+// ffn_rows_kernel (every other shape, fp32): one nonzero at a time, the dot product as a warp
+// reduction (plus a named-barrier exchange between the G warps of a row), weight rows of the
+// next nonzero loaded while the current one is used.
+//
+// Neither kernel has a spin-wait. The TwELL is checked on the way in (a count above the tile
+// width, an in-tile index at or beyond T, a column at or beyond d_ff): a bad entry is recorded
+// in the status word as TWELL_ERR_DEVICE_CHECK and contributes nothing, and every access stays
+// inside the TwELL's own arrays.
 #include "twell_common.cuh"
 
 namespace twell {
 
-constexpr int kItemCap = 256;   // items per buffer of the metadata -> issuer ring
-constexpr int kItemBufs = 4;
-constexpr int kItemEager = 64;  // a buffer holding this many items is handed over at the next row end
+constexpr int kSeg = 32;        // nonzeros per metadata segment (one per lane)
+constexpr int kXBufs = 3;       // x_r buffers per warp
 constexpr int kCntRegs = 4;     // rows with nt <= 128 tiles get their counts prefetched in registers
-constexpr int kEndItem = -2147483647 - 1;
 constexpr int kMaxTiles = 1024;
-constexpr int kRowSlots = 4;
-constexpr int kMaxSlots = 32;
-constexpr int kMaxConsumers = 512;
+constexpr int kCtaWarps = 4;
+constexpr int kCtaThreads = 32 * kCtaWarps;
+constexpr int kFirst = 1, kLast = 2;
 
-template <typename E, typename VT>
-struct FusedArgs {
+template <typename E>
+struct RowArgs {
     const E* x;
     const E* Wu;
     const E* Wd;
-    const VT* vals;
+    const void* vals;  // fp32 or bf16 (vals_bf16)
     const uint8_t* idx;
     const uint16_t* cnt;
     E* y;
-    int N, d, f, T, nt;
-    int S;          // weight-row slots in the ring
-    int consumers;  // consumer threads (multiple of 32)
+    int* tickets;  // G == 1: row counter, zero at launch
     int32_t* status;
-    uint64_t wait_limit_ns;
+    int N, d, f, T, nt, nchunks, vals_bf16;
 };
 
-// Shared-memory layout of the fused kernel. Every region starts on a 16-byte boundary (bulk-copy
-// destinations need 16 bytes, the item ring holds 8-byte int2, mbarriers need 8).
-struct FusedLayout {
-    size_t wu, wd, x, a, nnz, pref, items, nitems, red, bars, abort_flag, total;
-    __host__ __device__ static size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
-    __host__ __device__ FusedLayout(int S, int row_bytes)
+__host__ __device__ inline size_t pref_bytes(int nt) { return (static_cast<size_t>(nt + 1) * 4 + 15) & ~size_t(15); }
+
+// ---- packed fp32 pairs (fma.rn.f32x2)
+
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// Two bf16 in one 32-bit word -> the fp32 pair (low element first). Exact.
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+
+// A 16-byte chunk as P fp32 pairs, in element order.
+template <typename E>
+struct Chunk;
+template <>
+struct Chunk<__nv_bfloat16> {
+    static constexpr int P = 4;
+    __device__ __forceinline__ static void pairs(const uint4& v, uint64_t (&o)[4])
     {
-        size_t o = 0;
-        wu = o;
-        o = up16(o + static_cast<size_t>(S) * row_bytes);
-        wd = o;
-        o = up16(o + static_cast<size_t>(S) * row_bytes);
-        x = o;
-        o = up16(o + static_cast<size_t>(kRowSlots) * row_bytes);
-        a = o;
-        o = up16(o + kMaxSlots * 4);
-        nnz = o;
-        o = up16(o + kRowSlots * 4);
-        pref = o;
-        o = up16(o + (kMaxTiles + 1) * 4);
-        items = o;
-        o = up16(o + kItemBufs * kItemCap * 8);
-        nitems = o;
-        o = up16(o + kItemBufs * 4);
-        red = o;
-        o = up16(o + 2 * (kMaxConsumers / 32) * 4);
-        bars = o;
-        o = up16(o + (2 * kMaxSlots + 2 * kRowSlots + 2 * kItemBufs) * 8);
-        abort_flag = o;
-        o = up16(o + 16);
-        total = o;
+        o[0] = bf2_to_f2(v.x);
+        o[1] = bf2_to_f2(v.y);
+        o[2] = bf2_to_f2(v.z);
+        o[3] = bf2_to_f2(v.w);
     }
-    __host__ bool aligned() const
+};
+template <>
+struct Chunk<float> {
+    static constexpr int P = 2;
+    __device__ __forceinline__ static void pairs(const uint4& v, uint64_t (&o)[2])
     {
-        const size_t all[] = {wu, wd, x, a, nnz, pref, items, nitems, red, bars, abort_flag, total};
-        for (size_t v : all)
-            if (v % 16 != 0) return false;
+        o[0] = (static_cast<uint64_t>(v.y) << 32) | v.x;
+        o[1] = (static_cast<uint64_t>(v.w) << 32) | v.z;
+    }
+};
+
+// Weight loads: read-only, not kept in L1 (a row is used once per visit), kept in L2.
+__device__ __forceinline__ uint4 ldg_keep16(const void* p, uint64_t policy)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(policy));
+    return v;
+}
+// 32 bytes (32-byte aligned) into eight registers.
+__device__ __forceinline__ void ldg_keep32(uint32_t (&r)[8], const void* p, uint64_t policy)
+{
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "l"(p), "l"(policy));
+}
+
+// cp.async: 16-byte global -> shared copies, tracked per thread in commit groups.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------------------------------
+// The row stream of one group of G warps: row tickets, TwELL metadata one segment ahead, x_r
+// staged by cp.async (CPLX 16-byte chunks per lane: chunk q = q0 + m*32*G sits at
+// s_x[(xs*CPLX + m)*32 + lane], so with G = 1 a buffer holds x_r contiguously).
+template <typename E, int CPLX, int G>
+struct RowStream {
+    static constexpr int V = Elem<E>::kPer16B;
+    uint4* s_x;
+    int* s_pref;
+    int lane, q0, stride;
+    bool pre;
+    int tk, srow;
+    int creg[kCntRegs];
+    int i_row, n_row, i_nnz, i_base, xs_next;              // metadata side
+    int nx_row, nx_n, nx_flags, nx_xs, nx_toff;            // next segment (warp-uniform)
+    uint32_t nx_idx, nx_val;                               // next segment (one nonzero per lane)
+    int c_row, c_n, c_flags, c_xs, c_j, pos;               // current segment
+    float c_a;
+
+    __device__ void next_ticket(const RowArgs<E>& a)
+    {
+        if constexpr (G == 1) {
+            tk = 0;
+            if (lane == 0) tk = atomicAdd(a.tickets, 1);
+        } else {
+            tk = srow;
+            srow += stride;
+        }
+    }
+    __device__ int ticket_row() const
+    {
+        if constexpr (G == 1) return __shfl_sync(0xffffffffu, tk, 0);
+        else return tk;
+    }
+    __device__ void load_counts(const RowArgs<E>& a, int r)
+    {
+#pragma unroll
+        for (int m = 0; m < kCntRegs; ++m) {
+            const int t = lane + 32 * m;
+            creg[m] = (pre && r < a.N && t < a.nt) ? static_cast<int>(a.cnt[static_cast<size_t>(r) * a.nt + t]) : 0;
+        }
+    }
+    // exclusive offsets of row r's tiles into s_pref[0..nt]; returns the row's nonzeros
+    __device__ int scan_row(const RowArgs<E>& a, int r)
+    {
+        __syncwarp();  // every lane is done reading the previous row's offsets
+        int run = 0;
+        const int iters = (a.nt + 31) / 32;
+        for (int m = 0; m < iters; ++m) {
+            const int t = lane + 32 * m;
+            int v = 0;
+            if (pre) {
+#pragma unroll
+                for (int mm = 0; mm < kCntRegs; ++mm)
+                    if (mm == m) v = creg[mm];
+            } else if (t < a.nt) {
+                v = a.cnt[static_cast<size_t>(r) * a.nt + t];
+            }
+            if (v > a.T) {
+                report(a.status, TWELL_ERR_DEVICE_CHECK);
+                v = 0;
+            }
+            int inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            if (t < a.nt) s_pref[t] = run + inc - v;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_pref[a.nt] = run;
+        __syncwarp();
+        return run;
+    }
+    __device__ void advance_issue_row(const RowArgs<E>& a)
+    {
+        i_row = n_row;
+        i_nnz = i_row < a.N ? scan_row(a, i_row) : 0;
+        i_base = 0;
+        n_row = ticket_row();
+        load_counts(a, n_row);
+        next_ticket(a);
+    }
+    // Describe the next segment (loads of its indices and values stay in flight) and, at a row
+    // start, copy x of that row into the next x buffer. Commits exactly one cp.async group.
+    __device__ void issue_segment(const RowArgs<E>& a)
+    {
+        if (i_row >= a.N) {
+            nx_n = -1;  // end of this group's rows
+            cp_async_commit();
+            return;
+        }
+        const int n = min(kSeg, i_nnz - i_base);
+        nx_row = i_row;
+        nx_n = n;
+        nx_flags = (i_base == 0 ? kFirst : 0) | (i_base + n >= i_nnz ? kLast : 0);
+        if (i_base == 0 && n > 0) {
+            nx_xs = xs_next;
+            xs_next = xs_next + 1 == kXBufs ? 0 : xs_next + 1;
+            const E* xr = a.x + static_cast<size_t>(i_row) * a.d;
+#pragma unroll
+            for (int m = 0; m < CPLX; ++m) {
+                const int q = q0 + m * 32 * G;
+                if (q < a.nchunks) cp_async16(&s_x[(nx_xs * CPLX + m) * 32 + lane], xr + q * V);
+            }
+        }
+        if (lane < n) {
+            const int gp = i_base + lane;
+            int lo = 0, hi = a.nt;  // s_pref[lo] <= gp < s_pref[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_pref[mid] <= gp) lo = mid;
+                else hi = mid;
+            }
+            const size_t e = (static_cast<size_t>(i_row) * a.nt + lo) * a.T + (gp - s_pref[lo]);
+            nx_toff = lo * a.T;
+            nx_idx = a.idx[e];
+            nx_val = a.vals_bf16 ? static_cast<uint32_t>(static_cast<const uint16_t*>(a.vals)[e]) << 16
+                                 : static_cast<const uint32_t*>(a.vals)[e];
+        }
+        cp_async_commit();
+        i_base += n;
+        if (nx_flags & kLast) advance_issue_row(a);
+    }
+    __device__ void take_segment(const RowArgs<E>& a)
+    {
+        c_row = nx_row;
+        c_n = nx_n;
+        c_flags = nx_flags;
+        c_xs = nx_xs;
+        if (lane < c_n) {
+            int j = nx_toff + static_cast<int>(nx_idx);
+            float v = __uint_as_float(nx_val);
+            if (static_cast<int>(nx_idx) >= a.T || j >= a.f) {  // corrupt entry: record it, contribute nothing
+                report(a.status, TWELL_ERR_DEVICE_CHECK);
+                j = 0;
+                v = 0.0f;
+            }
+            c_j = j;
+            c_a = v;
+        }
+    }
+    __device__ void zero_row(const RowArgs<E>& a, int row)
+    {
+        E* yr = a.y + static_cast<size_t>(row) * a.d;
+        for (int q = q0; q < a.nchunks; q += 32 * G) st_stream16(yr + q * V, make_uint4(0, 0, 0, 0));
+    }
+    __device__ void init(const RowArgs<E>& a, uint4* sx, int* spref, int lane_, int wg, int group, int groups)
+    {
+        s_x = sx;
+        s_pref = spref;
+        lane = lane_;
+        q0 = wg * 32 + lane;
+        stride = groups;
+        pre = a.nt <= 32 * kCntRegs;
+        srow = group;
+        tk = 0;
+        i_row = n_row = a.N;
+        i_nnz = i_base = xs_next = 0;
+        nx_row = nx_flags = nx_xs = nx_toff = 0;
+        nx_n = -1;
+        nx_idx = nx_val = 0;
+        c_row = c_n = c_flags = c_xs = c_j = pos = 0;
+        c_a = 0.0f;
+        // pipeline fill: first row's counts and offsets, the next row's counts, the first segment
+        next_ticket(a);
+        n_row = ticket_row();
+        load_counts(a, n_row);
+        next_ticket(a);
+        advance_issue_row(a);
+        issue_segment(a);
+    }
+    // Make the current segment one with nonzeros left to take (pos < c_n); false at the end.
+    // Rows without nonzeros met on the way get y_r = 0.
+    __device__ bool ready(const RowArgs<E>& a)
+    {
+        while (pos >= c_n) {
+            if (c_n < 0) return false;
+            take_segment(a);
+            issue_segment(a);
+            pos = 0;
+            if (c_n < 0) return false;
+            if (c_n == 0) {
+                zero_row(a, c_row);
+                continue;
+            }
+            if (c_flags & kFirst) {
+                cp_async_wait<1>();  // x of this row: the group before the one just committed
+                __syncwarp();        // lanes read chunks other lanes copied
+            }
+        }
         return true;
     }
 };
 
-// Threads per CTA: consumer warps (<= XC of them when x is held in registers) + 2 producer warps.
-template <int XC>
-struct FusedThreads {
-    static constexpr int kMax = (XC > 0 ? 32 * XC : kMaxConsumers) + 64;
+// ------------------------------------------------------------------------------------------
+// General kernel: one nonzero at a time.
+
+struct Entry {
+    int j;      // hidden unit
+    float a;    // gate activation
+    int row;    // token row
+    int xs;     // x buffer holding x_row
+    int flags;  // kFirst: first nonzero of the row; kLast: last one
 };
 
-template <typename E, typename VT, int XC>
-__global__ void __launch_bounds__(FusedThreads<XC>::kMax, 1) ffn_fused_kernel(const FusedArgs<E, VT> a)
+template <int CPL>
+struct RowSmem {
+    __host__ __device__ static size_t x_bytes() { return static_cast<size_t>(kXBufs) * CPL * 32 * 16; }
+    __host__ __device__ static size_t warp_bytes(int nt) { return x_bytes() + pref_bytes(nt); }
+    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * warp_bytes(nt) + 2 * kCtaWarps * 4; }
+};
+
+template <typename E, int CPL, int G>
+__global__ void __launch_bounds__(kCtaThreads, (CPL >= 5 ? 2 : CPL == 4 ? 3 : 4)) ffn_rows_kernel(const RowArgs<E> a)
 {
     constexpr int V = Elem<E>::kPer16B;
+    constexpr int P = Chunk<E>::P;
+    constexpr int kGroups = kCtaWarps / G;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int row_bytes = a.d * static_cast<int>(sizeof(E));
-    const FusedLayout L(a.S, row_bytes);
-    E* s_wu = reinterpret_cast<E*>(smem + L.wu);
-    E* s_wd = reinterpret_cast<E*>(smem + L.wd);
-    E* s_x = reinterpret_cast<E*>(smem + L.x);
-    float* s_a = reinterpret_cast<float*>(smem + L.a);
-    int* s_nnz = reinterpret_cast<int*>(smem + L.nnz);
-    int* s_pref = reinterpret_cast<int*>(smem + L.pref);
-    int2* s_items = reinterpret_cast<int2*>(smem + L.items);
-    int* s_nitems = reinterpret_cast<int*>(smem + L.nitems);
-    float* s_red = reinterpret_cast<float*>(smem + L.red);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* empty = full + kMaxSlots;
-    uint64_t* rfull = empty + kMaxSlots;
-    uint64_t* rempty = rfull + kRowSlots;
-    uint64_t* lfull = rempty + kRowSlots;
-    uint64_t* lempty = lfull + kItemBufs;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wg = warp % G, grp = warp / G;
+    const size_t wbytes = RowSmem<CPL>::warp_bytes(a.nt);
+    uint4* s_x = reinterpret_cast<uint4*>(smem + warp * wbytes);
+    int* s_pref = reinterpret_cast<int*>(smem + warp * wbytes + RowSmem<CPL>::x_bytes());
+    float* s_part = reinterpret_cast<float*>(smem + kCtaWarps * wbytes) + grp * 2 * G;
 
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int C = a.consumers;
-    const int cwarps = C >> 5;
-    const int S = a.S;
-    const int batch = min(cwarps, S);  // nonzeros per consumer batch (one per warp)
-    const int nchunks = a.d / V;
+    const uint64_t pol = policy_evict_last();
+    const int nchunks = a.nchunks;
+    const int q0 = wg * 32 + lane;  // chunk of m = 0; chunk m is q0 + m * 32 * G
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], cwarps);
+    RowStream<E, CPL, G> rs;
+    rs.init(a, s_x, s_pref, lane, wg, blockIdx.x * kGroups + grp, gridDim.x * kGroups);
+    auto next_entry = [&](Entry& en) -> bool {
+        if (!rs.ready(a)) return false;
+        en.j = __shfl_sync(0xffffffffu, rs.c_j, rs.pos);
+        en.a = __shfl_sync(0xffffffffu, rs.c_a, rs.pos);
+        en.row = rs.c_row;
+        en.xs = rs.c_xs;
+        en.flags = (rs.pos == 0 ? (rs.c_flags & kFirst) : 0) | (rs.pos == rs.c_n - 1 ? (rs.c_flags & kLast) : 0);
+        ++rs.pos;
+        return true;
+    };
+
+    uint64_t acc[CPL][P];
+#pragma unroll
+    for (int m = 0; m < CPL; ++m)
+#pragma unroll
+        for (int p = 0; p < P; ++p) acc[m][p] = 0;
+    auto store_row = [&](int row) {
+        E* yr = a.y + static_cast<size_t>(row) * a.d;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            const int q = q0 + m * 32 * G;
+            if (q >= nchunks) continue;
+            float fv[V];
+#pragma unroll
+            for (int p = 0; p < P; ++p) f2unpack(acc[m][p], fv[2 * p], fv[2 * p + 1]);
+            st_stream16(yr + q * V, pack16(fv, static_cast<E*>(nullptr)));
         }
-        for (int s = 0; s < kRowSlots; ++s) {
-            mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], cwarps);
+    };
+
+    int par = 0;
+    auto load_w = [&](uint4 (&wu)[CPL], uint4 (&wd)[CPL], int j) {
+        const E* pu = a.Wu + static_cast<size_t>(j) * a.d;
+        const E* pd = a.Wd + static_cast<size_t>(j) * a.d;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            const int q = q0 + m * 32 * G;
+            if (q < nchunks) {
+                wu[m] = ldg_keep16(pu + q * V, pol);
+                wd[m] = ldg_keep16(pd + q * V, pol);
+            }
         }
-        for (int s = 0; s < kItemBufs; ++s) {
-            mbar_init(&lfull[s], 1);
-            mbar_init(&lempty[s], 1);
+    };
+    auto compute = [&](const uint4 (&wu)[CPL], const uint4 (&wd)[CPL], const Entry& en) {
+        if (en.flags & kFirst) {
+#pragma unroll
+            for (int m = 0; m < CPL; ++m)
+#pragma unroll
+                for (int p = 0; p < P; ++p) acc[m][p] = 0;
         }
-        *abort_flag = 0;
-        fence_mbar_init();
+        uint64_t s[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) s[p] = 0;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            const int q = q0 + m * 32 * G;
+            if (q < nchunks) {
+                uint64_t xp[P], wp[P];
+                Chunk<E>::pairs(s_x[(en.xs * CPL + m) * 32 + lane], xp);
+                Chunk<E>::pairs(wu[m], wp);
+#pragma unroll
+                for (int p = 0; p < P; ++p) fma2(s[p], xp[p], wp[p]);
+            }
+        }
+        float part = 0.0f;
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            float lo, hi;
+            f2unpack(s[p], lo, hi);
+            part += lo + hi;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        float u = part;
+        if constexpr (G > 1) {
+            if (lane == 0) s_part[par * G + wg] = part;
+            bar_sync_named(1 + grp, 32 * G);
+            u = 0.0f;
+#pragma unroll
+            for (int g = 0; g < G; ++g) u += s_part[par * G + g];
+            par ^= 1;
+        }
+        const float h = en.a * u;
+        const uint64_t h2 = f2pack(h, h);
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            const int q = q0 + m * 32 * G;
+            if (q < nchunks) {
+                uint64_t wp[P];
+                Chunk<E>::pairs(wd[m], wp);
+#pragma unroll
+                for (int p = 0; p < P; ++p) fma2(acc[m][p], h2, wp[p]);
+            }
+        }
+        if (en.flags & kLast) store_row(en.row);
+    };
+
+    uint4 ua[CPL], da[CPL], ub[CPL], db[CPL];
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) ua[m] = da[m] = ub[m] = db[m] = make_uint4(0, 0, 0, 0);
+    Entry ea, eb;
+    bool ha = next_entry(ea);
+    if (ha) load_w(ua, da, ea.j);
+    while (ha) {
+        const bool hb = next_entry(eb);
+        if (hb) load_w(ub, db, eb.j);
+        compute(ua, da, ea);
+        if (!hb) break;
+        ha = next_entry(ea);
+        if (ha) load_w(ua, da, ea.j);
+        compute(ub, db, eb);
     }
-    __syncthreads();
-
-    if (tid >= C + 32) {
-        // ---------------------------------------------------------------- metadata warp
-        // Turns the TwELL of this CTA's rows into a stream of items for the issuer: a row record
-        // {~r, nnz} followed by the row's nonzeros {j, a} in TwELL order, written into a ring of
-        // kItemBufs buffers. The counts of the next row are loaded while the current row's
-        // indices and values are gathered, so one L2 round trip is paid per row, ahead of use.
-        int buf = 0, fill = 0;
-        uint32_t bph = 0;
-        bool ok = true;
-        auto publish = [&]() {  // hand the current buffer to the issuer and open the next one
-            __syncwarp();
-            if (lane == 0) {
-                s_nitems[buf] = fill;
-                mbar_arrive(&lfull[buf]);
-            }
-            if (++buf == kItemBufs) {
-                buf = 0;
-                bph ^= 1u;
-            }
-            fill = 0;
-            int w = 1;
-            if (lane == 0) w = wait_bounded(&lempty[buf], bph ^ 1u, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        };
-        {
-            int w = 1;
-            if (lane == 0) w = wait_bounded(&lempty[0], 1u, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        }
-        const bool pre = a.nt <= 32 * kCntRegs;
-        int creg[kCntRegs];
-        auto load_counts = [&](int row, int (&c)[kCntRegs]) {
-#pragma unroll
-            for (int m = 0; m < kCntRegs; ++m) {
-                const int t = lane + 32 * m;
-                c[m] = (row < a.N && t < a.nt) ? static_cast<int>(a.cnt[static_cast<size_t>(row) * a.nt + t]) : 0;
-            }
-        };
-        if (pre) load_counts(blockIdx.x, creg);
-        for (int r = blockIdx.x; ok && r < a.N; r += gridDim.x) {
-            // per-tile exclusive offsets of row r in shared memory
-            int run = 0;
-            if (pre) {
-                int c[kCntRegs];
-#pragma unroll
-                for (int m = 0; m < kCntRegs; ++m) c[m] = creg[m];
-                load_counts(r + gridDim.x, creg);  // next row's counts, in flight during this row
-#pragma unroll
-                for (int m = 0; m < kCntRegs; ++m) {
-                    const int t = lane + 32 * m;
-                    int v = c[m];
-                    if (v > a.T) {
-                        report(a.status, TWELL_ERR_DEVICE_CHECK);
-                        v = 0;
-                    }
-                    int inc = v;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int u = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += u;
-                    }
-                    if (t < a.nt) s_pref[t] = run + inc - v;
-                    run += __shfl_sync(0xffffffffu, inc, 31);
-                }
-            } else {
-                for (int t0 = 0; t0 < a.nt; t0 += 32) {
-                    const int t = t0 + lane;
-                    int v = t < a.nt ? static_cast<int>(a.cnt[static_cast<size_t>(r) * a.nt + t]) : 0;
-                    if (v > a.T) {
-                        report(a.status, TWELL_ERR_DEVICE_CHECK);
-                        v = 0;
-                    }
-                    int inc = v;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int u = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += u;
-                    }
-                    if (t < a.nt) s_pref[t] = run + inc - v;
-                    run += __shfl_sync(0xffffffffu, inc, 31);
-                }
-            }
-            if (lane == 0) s_pref[a.nt] = run;
-            __syncwarp();
-            const int nnz = run;
-            if (fill == kItemCap) publish();
-            if (!ok) break;
-            if (lane == 0) s_items[buf * kItemCap + fill] = make_int2(~r, nnz);
-            ++fill;
-            for (int pos = 0; ok && pos < nnz;) {
-                if (fill == kItemCap) {
-                    publish();
-                    if (!ok) break;
-                }
-                const int take = min(kItemCap - fill, nnz - pos);
-                // one entry per lane: its tile is the last t with s_pref[t] <= position (binary
-                // search), so all the row's index/value loads are in flight together
-                for (int i = lane; i < take; i += 32) {
-                    const int gp = pos + i;
-                    int lo = 0, hi = a.nt;  // invariant: s_pref[lo] <= gp < s_pref[hi]
-                    while (hi - lo > 1) {
-                        const int mid = (lo + hi) >> 1;
-                        if (s_pref[mid] <= gp) lo = mid;
-                        else hi = mid;
-                    }
-                    const size_t e = (static_cast<size_t>(r) * a.nt + lo) * a.T + (gp - s_pref[lo]);
-                    int j = lo * a.T + a.idx[e];
-                    float v = Elem<VT>::to_f(a.vals[e]);
-                    if (j >= a.f) {  // corrupt index: record it and contribute nothing
-                        report(a.status, TWELL_ERR_DEVICE_CHECK);
-                        j = 0;
-                        v = 0.0f;
-                    }
-                    s_items[buf * kItemCap + fill + i] = make_int2(j, __float_as_int(v));
-                }
-                fill += take;
-                pos += take;
-            }
-            __syncwarp();
-            if (fill >= kItemEager) publish();  // keep the issuer fed from the first rows on
-        }
-        // end marker, then hand over the last buffer
-        if (ok) {
-            if (fill == kItemCap) publish();
-            if (ok) {
-                if (lane == 0) s_items[buf * kItemCap + fill] = make_int2(kEndItem, 0);
-                ++fill;
-                __syncwarp();
-                if (lane == 0) {
-                    s_nitems[buf] = fill;
-                    mbar_arrive(&lfull[buf]);
-                }
-            }
-        }
-    } else if (tid >= C) {
-        // ---------------------------------------------------------------- issuer warp (lane 0)
-        // Walks the item stream: a row record stages x_r (bulk copy) and its nonzero count into
-        // the row ring; a nonzero stages rows j of Wu_s and Wd_s into the slot ring.
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_last();
-            const uint64_t pol_x = policy_evict_first();
-            int slot = 0, rs = 0, buf = 0;
-            uint32_t ph = 0, rph = 0, bph = 0;
-            uint32_t issued = 0, issued_ph = 0, xissued = 0, xissued_ph = 0;
-            bool ok = true, done = false;
-            while (ok && !done) {
-                if (!wait_bounded(&lfull[buf], bph, abort_flag, a.status, a.wait_limit_ns)) break;
-                const int n = s_nitems[buf];
-                for (int i = 0; ok && i < n; ++i) {
-                    const int2 it = s_items[buf * kItemCap + i];
-                    if (it.x == kEndItem) {
-                        done = true;
-                        break;
-                    }
-                    if (it.x < 0) {
-                        const int r = ~it.x, nnz = it.y;
-                        if (!wait_bounded(&rempty[rs], rph ^ 1u, abort_flag, a.status, a.wait_limit_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        s_nnz[rs] = nnz;
-                        if (nnz > 0) {
-                            mbar_arrive_expect_tx(&rfull[rs], row_bytes);
-                            bulk_load(s_x + static_cast<size_t>(rs) * a.d, a.x + static_cast<size_t>(r) * a.d, row_bytes,
-                                      &rfull[rs], pol_x);
-                            xissued |= 1u << rs;
-                            xissued_ph = (xissued_ph & ~(1u << rs)) | (rph << rs);
-                        } else {
-                            mbar_arrive(&rfull[rs]);
-                        }
-                        if (++rs == kRowSlots) {
-                            rs = 0;
-                            rph ^= 1u;
-                        }
-                    } else {
-                        if (!wait_bounded(&empty[slot], ph ^ 1u, abort_flag, a.status, a.wait_limit_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        const size_t j = static_cast<size_t>(it.x);
-                        s_a[slot] = __int_as_float(it.y);
-                        mbar_arrive_expect_tx(&full[slot], 2 * row_bytes);
-                        bulk_load(s_wu + static_cast<size_t>(slot) * a.d, a.Wu + j * a.d, row_bytes, &full[slot], pol_w);
-                        bulk_load(s_wd + static_cast<size_t>(slot) * a.d, a.Wd + j * a.d, row_bytes, &full[slot], pol_w);
-                        issued |= 1u << slot;
-                        issued_ph = (issued_ph & ~(1u << slot)) | (ph << slot);
-                        if (++slot == S) {
-                            slot = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                }
-                mbar_arrive(&lempty[buf]);
-                if (++buf == kItemBufs) {
-                    buf = 0;
-                    bph ^= 1u;
-                }
-            }
-            // no bulk copy may still be writing shared memory when the CTA exits
-            for (int s = 0; s < S; ++s)
-                if (issued & (1u << s)) wait_bounded(&full[s], (issued_ph >> s) & 1u, nullptr, a.status, a.wait_limit_ns);
-            for (int s = 0; s < kRowSlots; ++s)
-                if (xissued & (1u << s))
-                    wait_bounded(&rfull[s], (xissued_ph >> s) & 1u, nullptr, a.status, a.wait_limit_ns);
-        }
-    } else {
-        // ---------------------------------------------------------------- consumer warps
-        // Batch = one nonzero per consumer warp. Warp w forms the whole dot x_r . Wu_s[j] of the
-        // batch's w-th nonzero (x_r held in fp32 registers, lane l covering 16-byte chunks
-        // l, l+32, ...), reduces it with 5 shuffles and publishes h = a * u; after one named
-        // barrier every warp applies all of the batch's rank-1 updates h * Wd_s[j] to its own
-        // slice of y_r (lane l of warp w owns chunk 32w + l).
-        const int warp = tid >> 5;
-        constexpr int YC = XC > 0 ? 1 : 2;  // chunks of y per thread: tid, tid + C
-        int slot = 0, rs = 0, buf = 0;
-        uint32_t ph = 0, rph = 0;
-        for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
-            // one lane per warp observes the row record; the named barrier that follows orders the
-            // staged x row before every consumer thread's reads
-            int rok = 1;
-            if (lane == 0) rok = wait_bounded(&rfull[rs], rph, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
-            if (bar_or(1, C, rok == 0)) break;
-            const int nnz = s_nnz[rs];
-            float acc[YC][V];
-#pragma unroll
-            for (int i = 0; i < YC; ++i)
-#pragma unroll
-                for (int e = 0; e < V; ++e) acc[i][e] = 0.0f;
-            float xf[XC > 0 ? XC : 1][V];
-            const E* xrow = s_x + static_cast<size_t>(rs) * a.d;
-            if (XC > 0 && nnz > 0) {
-#pragma unroll
-                for (int m = 0; m < (XC > 0 ? XC : 1); ++m) {
-                    const int c = lane + 32 * m;
-                    if (c < nchunks) unpack16(*reinterpret_cast<const uint4*>(xrow + c * V), xf[m], static_cast<E*>(nullptr));
-                    else
-#pragma unroll
-                        for (int e = 0; e < V; ++e) xf[m][e] = 0.0f;
-                }
-            }
-            bool failed = false;
-            for (int b = 0; b < nnz; b += batch) {
-                const int nb = min(batch, nnz - b);
-                // slot of this warp's nonzero
-                int s = slot + warp;
-                uint32_t p = ph;
-                if (s >= S) {
-                    s -= S;
-                    p ^= 1u;
-                }
-                bool okb = true;
-                float h = 0.0f;
-                if (warp < nb) {
-                    int w = 1;
-                    if (lane == 0) w = wait_bounded(&full[s], p, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
-                    okb = __shfl_sync(0xffffffffu, w, 0) != 0;
-                    const E* wrow = s_wu + static_cast<size_t>(s) * a.d;
-                    float dp[V];
-#pragma unroll
-                    for (int e = 0; e < V; ++e) dp[e] = 0.0f;
-                    if (XC > 0) {
-                        uint4 wraw[XC > 0 ? XC : 1];
-#pragma unroll
-                        for (int m = 0; m < (XC > 0 ? XC : 1); ++m) {
-                            const int c = lane + 32 * m;
-                            wraw[m] = c < nchunks ? *reinterpret_cast<const uint4*>(wrow + c * V) : make_uint4(0, 0, 0, 0);
-                        }
-#pragma unroll
-                        for (int m = 0; m < (XC > 0 ? XC : 1); ++m) {
-                            float wv[V];
-                            unpack16(wraw[m], wv, static_cast<E*>(nullptr));
-#pragma unroll
-                            for (int e = 0; e < V; ++e) dp[e] = fmaf(xf[m][e], wv[e], dp[e]);
-                        }
-                    } else {
-                        for (int c = lane; c < nchunks; c += 32) {
-                            float xv[V], wv[V];
-                            unpack16(*reinterpret_cast<const uint4*>(xrow + c * V), xv, static_cast<E*>(nullptr));
-                            unpack16(*reinterpret_cast<const uint4*>(wrow + c * V), wv, static_cast<E*>(nullptr));
-#pragma unroll
-                            for (int e = 0; e < V; ++e) dp[e] = fmaf(xv[e], wv[e], dp[e]);
-                        }
-                    }
-                    float dsum = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < V; ++e) dsum += dp[e];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-                    h = s_a[s] * dsum;
-                    if (lane == 0) s_red[buf * (kMaxConsumers / 32) + warp] = h;
-                }
-                if (bar_or(1, C, !okb)) {
-                    failed = true;
-                    break;
-                }
-                // rank-1 updates of this thread's chunk of y_r. Every slot of the batch was observed
-                // complete by its dot warp before the named barrier above, which orders the
-                // bulk-copied bytes before these reads; the batch's Wd chunks are loaded in groups
-                // of four so the shared-memory latencies overlap.
-                {
-                    const float* hb = s_red + buf * (kMaxConsumers / 32);
-#pragma unroll
-                    for (int i = 0; i < YC; ++i) {
-                        const int q = tid + i * C;
-                        if (q >= nchunks) continue;
-                        for (int k0 = 0; k0 < nb; k0 += 4) {
-                            uint4 w4[4];
-                            float h4[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                int sk = slot + k0 + u;
-                                if (sk >= S) sk -= S;
-                                const bool live = k0 + u < nb;
-                                h4[u] = live ? hb[k0 + u] : 0.0f;
-                                w4[u] = live ? *reinterpret_cast<const uint4*>(s_wd + static_cast<size_t>(sk) * a.d + q * V)
-                                             : make_uint4(0, 0, 0, 0);
-                            }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                float wv[V];
-                                unpack16(w4[u], wv, static_cast<E*>(nullptr));
-#pragma unroll
-                                for (int e = 0; e < V; ++e) acc[i][e] = fmaf(h4[u], wv[e], acc[i][e]);
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    int sk = slot;
-                    for (int k = 0; k < nb; ++k) {
-                        mbar_arrive(&empty[sk]);
-                        if (++sk == S) sk = 0;
-                    }
-                }
-                slot += nb;
-                if (slot >= S) {
-                    slot -= S;
-                    ph ^= 1u;
-                }
-                buf ^= 1;
-            }
-            if (failed) break;
-#pragma unroll
-            for (int i = 0; i < YC; ++i) {
-                const int q = tid + i * C;
-                if (q < nchunks) st_stream16(a.y + static_cast<size_t>(r) * a.d + q * V, pack16(acc[i], static_cast<E*>(nullptr)));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&rempty[rs]);
-            if (++rs == kRowSlots) {
-                rs = 0;
-                rph ^= 1u;
-            }
-        }
-    }
-    __syncthreads();
+    cp_async_wait<0>();
 }
 
-template <typename E, typename VT, int XC>
-static twell_status launch_fused(FusedArgs<E, VT> a, cudaStream_t s)
+// ------------------------------------------------------------------------------------------
+// Tensor-core kernel (bf16, d_model % 256 == 0, 512 <= d_model <= 2048, one warp per row).
+
+constexpr int kBatch = 8;  // nonzeros per batch: the n dimension of m16n8k16
+constexpr int kBatchSlots = 4;
+
+struct __align__(16) BatchDesc {
+    int row, k, xs, flags;  // flags: kFirst = the row's first batch, kLast = its last
+    int j[kBatch];
+    float a[kBatch];
+    float h[kBatch];        // h = a * u, filled when the batch's dot products are done
+};
+
+template <int CPL>  // 32-byte chunks per lane of a weight row in the down projection
+struct MmaSmem {
+    static constexpr int CPLX = 2 * CPL;  // 16-byte x chunks per lane
+    __host__ __device__ static size_t x_bytes() { return static_cast<size_t>(kXBufs) * CPLX * 32 * 16; }
+    __host__ __device__ static size_t warp_bytes(int nt)
+    {
+        return x_bytes() + pref_bytes(nt) + kBatchSlots * sizeof(BatchDesc);
+    }
+    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * warp_bytes(nt); }
+};
+
+template <int CPL>
+__global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<__nv_bfloat16> a)
+{
+    using E = __nv_bfloat16;
+    constexpr int CPLX = MmaSmem<CPL>::CPLX;
+    constexpr int kU = 1, kD = 2, kEnd = 3;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const size_t wbytes = MmaSmem<CPL>::warp_bytes(a.nt);
+    uint8_t* wsm = smem + warp * wbytes;
+    uint4* s_x = reinterpret_cast<uint4*>(wsm);
+    int* s_pref = reinterpret_cast<int*>(wsm + MmaSmem<CPL>::x_bytes());
+    BatchDesc* s_bd = reinterpret_cast<BatchDesc*>(wsm + MmaSmem<CPL>::x_bytes() + pref_bytes(a.nt));
+
+    const uint64_t pol = policy_evict_last();
+    const int nU = a.d / 256;  // up-projection steps per batch (256 columns of d_model each)
+    const int n32 = a.d / 16;  // 32-byte chunks of a row
+
+    RowStream<E, CPLX, 1> rs;
+    rs.init(a, s_x, s_pref, lane, 0, blockIdx.x * kCtaWarps + warp, gridDim.x * kCtaWarps);
+
+    // -------------------------------------------------------------- issue side: 4 KB steps
+    // A batch of k nonzeros is nU up-projection steps (lane (g, t) loads 32 bytes of Wu_s[j_g]
+    // at column 64c + 16t, four c per step) followed by k down-projection steps (lane loads its
+    // CPL 32-byte chunks of Wd_s[j_e]). The tag of a step: kind | batch slot << 2 | step << 4.
+    int is_slot = 0, is_step = 0, is_nsteps = 0, is_k = 0, nslot = 0;
+    bool ended = false;
+    auto form_batch = [&](BatchDesc* D) -> bool {
+        if (!rs.ready(a)) return false;
+        const int k = min(kBatch, rs.c_n - rs.pos);
+        if (lane >= rs.pos && lane < rs.pos + k) {
+            D->j[lane - rs.pos] = rs.c_j;
+            D->a[lane - rs.pos] = rs.c_a;
+        }
+        if (lane == 0) {
+            D->row = rs.c_row;
+            D->k = k;
+            D->xs = rs.c_xs;
+            D->flags = (rs.pos == 0 ? (rs.c_flags & kFirst) : 0) | (rs.pos + k == rs.c_n ? (rs.c_flags & kLast) : 0);
+        }
+        __syncwarp();
+        rs.pos += k;
+        return true;
+    };
+    auto issue = [&](uint32_t (&B)[4][8], int& tag) {
+        if (ended) {
+            tag = kEnd;
+            return;
+        }
+        if (is_step == is_nsteps) {
+            if (!form_batch(&s_bd[nslot])) {
+                ended = true;
+                tag = kEnd;
+                return;
+            }
+            is_slot = nslot;
+            nslot = (nslot + 1) & (kBatchSlots - 1);
+            is_k = s_bd[is_slot].k;
+            is_nsteps = nU + is_k;
+            is_step = 0;
+        }
+        const BatchDesc* D = &s_bd[is_slot];
+        if (is_step < nU) {
+            if (g < is_k) {
+                const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + 256 * is_step + 16 * t;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) ldg_keep32(B[cc], w + 64 * cc, pol);
+            }
+            tag = kU;
+        } else {
+            const E* w = a.Wd + static_cast<size_t>(D->j[is_step - nU]) * a.d;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                const int q = lane + 32 * m;
+                if (q < n32) ldg_keep32(B[m], w + 16 * q, pol);
+            }
+            tag = kD;
+        }
+        tag |= (is_slot << 2) | (is_step << 4);
+        ++is_step;
+    };
+
+    // -------------------------------------------------------------- process side
+    float macc[2][4];  // two accumulator sets: independent mma chains
+#pragma unroll
+    for (int i = 0; i < 2; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
+    uint64_t acc[CPL][8];
+#pragma unroll
+    for (int m = 0; m < CPL; ++m)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) acc[m][w] = 0;
+    auto process = [&](const uint32_t (&B)[4][8], int tag) {
+        BatchDesc* D = &s_bd[(tag >> 2) & (kBatchSlots - 1)];
+        const int step = tag >> 4;
+        if ((tag & 3) == kU) {
+            if (step == 0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
+            }
+            // x_r in every row of A; B column n is the batch's nonzero n. Inside each 16-wide k
+            // block, k slots (2t, 2t+1, 2t+8, 2t+9) hold columns o+4b .. o+4b+3 of d_model with
+            // o = 64c + 16t, on both sides.
+            const uint4* xr = s_x + D->xs * (CPLX * 32);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * step + cc;
+                const uint4 X0 = xr[8 * c + 2 * t], X1 = xr[8 * c + 2 * t + 1];
+                mma_bf16(macc[0], X0.x, X0.x, X0.y, X0.y, B[cc][0], B[cc][1]);
+                mma_bf16(macc[1], X0.z, X0.z, X0.w, X0.w, B[cc][2], B[cc][3]);
+                mma_bf16(macc[0], X1.x, X1.x, X1.y, X1.y, B[cc][4], B[cc][5]);
+                mma_bf16(macc[1], X1.z, X1.z, X1.w, X1.w, B[cc][6], B[cc][7]);
+            }
+            if (step == nU - 1) {
+                // lane (g, t) holds u of nonzeros 2t and 2t+1 (every row of D is the same)
+                const float u0 = macc[0][0] + macc[1][0];
+                const float u1 = macc[0][1] + macc[1][1];
+                if (lane < 4) {
+                    D->h[2 * lane] = D->a[2 * lane] * u0;
+                    D->h[2 * lane + 1] = D->a[2 * lane + 1] * u1;
+                }
+                __syncwarp();
+            }
+        } else {
+            const int e = step - nU;
+            const float h = D->h[e];
+            const uint64_t h2 = f2pack(h, h);
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                const int q = lane + 32 * m;
+                if (q < n32) {
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) fma2(acc[m][w], h2, bf2_to_f2(B[m][w]));
+                }
+            }
+            if (e == D->k - 1 && (D->flags & kLast)) {
+                E* yr = a.y + static_cast<size_t>(D->row) * a.d;
+#pragma unroll
+                for (int m = 0; m < CPL; ++m) {
+                    const int q = lane + 32 * m;
+                    if (q < n32) {
+                        float lo8[8], hi8[8];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            f2unpack(acc[m][w], lo8[2 * w], lo8[2 * w + 1]);
+                            f2unpack(acc[m][w + 4], hi8[2 * w], hi8[2 * w + 1]);
+                        }
+                        st_stream16(yr + 16 * q, pack16(lo8, static_cast<E*>(nullptr)));
+                        st_stream16(yr + 16 * q + 8, pack16(hi8, static_cast<E*>(nullptr)));
+                    }
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) acc[m][w] = 0;
+                }
+            }
+        }
+    };
+
+    uint32_t B0[4][8], B1[4][8], B2[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) B0[i][w] = B1[i][w] = B2[i][w] = 0;
+    int t0, t1, t2;
+    issue(B0, t0);
+    issue(B1, t1);
+    for (;;) {
+        issue(B2, t2);
+        if (t0 == kEnd) break;
+        process(B0, t0);
+        issue(B0, t0);
+        if (t1 == kEnd) break;
+        process(B1, t1);
+        issue(B1, t1);
+        if (t2 == kEnd) break;
+        process(B2, t2);
+    }
+    cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------------------------------
+// Launch
+
+template <typename E, typename K>
+static twell_status launch_persistent(K kern, const RowArgs<E>& a, size_t smem, int groups_per_cta, bool tickets,
+                                      cudaStream_t s)
 {
     twell_host::DevInfo di;
     if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
-    constexpr int V = Elem<E>::kPer16B;
-    const int nchunks = a.d / V;
-    a.consumers = XC > 0 ? (nchunks + 31) / 32 * 32 : ((nchunks + 1) / 2 + 31) / 32 * 32;
-    const int row_bytes = a.d * static_cast<int>(sizeof(E));
-    const size_t fixed = FusedLayout(0, row_bytes).total;
-    const size_t budget = di.max_smem_optin;
-    if (budget <= fixed) return TWELL_ERR_UNSUPPORTED;
-    int S = static_cast<int>((budget - fixed) / (2 * static_cast<size_t>(row_bytes)));
-    if (S > kMaxSlots) S = kMaxSlots;
-    if (S < 4) return TWELL_ERR_UNSUPPORTED;
-    a.S = S;
-    a.wait_limit_ns = twell_host::wait_limit_ns();
-    const FusedLayout layout(S, row_bytes);
-    if (row_bytes % 16 != 0 || !layout.aligned()) return TWELL_ERR_UNSUPPORTED;
-    const size_t smem = layout.total;
-    auto kern = ffn_fused_kernel<E, VT, XC>;
+    if (smem > di.max_smem_optin) return TWELL_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return TWELL_ERR_CUDA;
-    const int grid = a.N < di.sm_count ? a.N : di.sm_count;
-    kern<<<grid, a.consumers + 64, smem, s>>>(a);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCtaThreads, smem) != cudaSuccess || per_sm < 1)
+        return TWELL_ERR_CUDA;
+    if (tickets && cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    const int need = (a.N + groups_per_cta - 1) / groups_per_cta;  // CTAs until every group has a row
+    int grid = di.sm_count * per_sm;
+    if (grid > need) grid = need;
+    kern<<<grid, kCtaThreads, smem, s>>>(a);
     return twell_host::launch_status();
 }
 
-template <typename E, typename VT>
-static twell_status run_fused(const FusedArgs<E, VT>& a, cudaStream_t s)
+template <typename E, int CPL, int G>
+static twell_status launch_rows(const RowArgs<E>& a, cudaStream_t s)
 {
-    constexpr int V = Elem<E>::kPer16B;
-    const int nchunks = a.d / V;
-    if (nchunks <= 32 * 4) return launch_fused<E, VT, 4>(a, s);
-    if (nchunks <= 32 * 8) return launch_fused<E, VT, 8>(a, s);
-    if (nchunks <= 32 * 10) return launch_fused<E, VT, 10>(a, s);
-    if (nchunks <= 2 * kMaxConsumers) return launch_fused<E, VT, 0>(a, s);
+    return launch_persistent(ffn_rows_kernel<E, CPL, G>, a, RowSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, G == 1, s);
+}
+
+template <int CPL>
+static twell_status launch_mma(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
+{
+    return launch_persistent(ffn_mma_kernel<CPL>, a, MmaSmem<CPL>::cta_bytes(a.nt), kCtaWarps, true, s);
+}
+
+// Kernel and layout for d_model = nchunks 16-byte chunks: the tensor-core kernel where it applies,
+// else chunks per lane (CPL) and warps per row (G) of the general kernel.
+template <typename E>
+static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
+{
+    if constexpr (std::is_same<E, __nv_bfloat16>::value) {
+        const bool a32 = (reinterpret_cast<uintptr_t>(a.Wu) % 32 == 0) && (reinterpret_cast<uintptr_t>(a.Wd) % 32 == 0);
+        if (a32 && a.d % 256 == 0 && a.d >= 512 && a.d <= 2048) {
+            if (a.d <= 512) return launch_mma<1>(a, s);
+            if (a.d <= 1024) return launch_mma<2>(a, s);
+            return launch_mma<4>(a, s);
+        }
+    }
+    const int n = a.nchunks;
+    if (n <= 32 * 2) return launch_rows<E, 2, 1>(a, s);
+    if (n <= 32 * 4) return launch_rows<E, 4, 1>(a, s);
+    if (n <= 32 * 8) return launch_rows<E, 8, 1>(a, s);
+    if (n <= 64 * 5) return launch_rows<E, 5, 2>(a, s);
+    if (n <= 64 * 8) return launch_rows<E, 8, 2>(a, s);
+    if (n <= 128 * 8) return launch_rows<E, 8, 4>(a, s);
     return TWELL_ERR_UNSUPPORTED;
 }
 
@@ -555,8 +773,6 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
                                             int32_t N, int32_t d, int32_t f, twell_dtype dtype, void* y, void* ws,
                                             size_t ws_bytes, int32_t* dev_status, void* stream)
 {
-    (void)ws;
-    (void)ws_bytes;
     if (Wu_s == nullptr || Wd_s == nullptr || a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
     if ((x == nullptr || y == nullptr) && N != 0) return TWELL_ERR_INVALID;
     if (N < 0 || d <= 0 || f <= 0 || d % 8 != 0) return TWELL_ERR_INVALID;
@@ -567,25 +783,21 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
     const int nt = (f + a->tile - 1) / a->tile;
     if (nt > twell::kMaxTiles) return TWELL_ERR_UNSUPPORTED;
     if (N == 0) return TWELL_OK;
-    if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd_s) || !aligned16(y)) return TWELL_ERR_INVALID;
+    if (ws == nullptr || ws_bytes < twell_workspace_bytes(TWELL_OP_FFN_FUSED_FWD, N, d, f, a->tile, 0, 0))
+        return TWELL_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd_s) || !aligned16(y) || !aligned16(ws))
+        return TWELL_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    using bf = __nv_bfloat16;
+    const int vals_bf16 = a->dtype == TWELL_BF16 ? 1 : 0;
     if (dtype == TWELL_BF16) {
-        const bf* xb = static_cast<const bf*>(x);
-        const bf* wu = static_cast<const bf*>(Wu_s);
-        const bf* wd = static_cast<const bf*>(Wd_s);
-        bf* yb = static_cast<bf*>(y);
-        if (a->dtype == TWELL_F32) {
-            twell::FusedArgs<bf, float> p{xb, wu, wd, static_cast<const float*>(a->vals), a->idx, a->cnt, yb,
-                                          N, d, f, a->tile, nt, 0, 0, dev_status, 0};
-            return twell::run_fused(p, s);
-        }
-        twell::FusedArgs<bf, bf> p{xb, wu, wd, static_cast<const bf*>(a->vals), a->idx, a->cnt, yb,
-                                   N, d, f, a->tile, nt, 0, 0, dev_status, 0};
+        using bf = __nv_bfloat16;
+        twell::RowArgs<bf> p{static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd_s),
+                             a->vals, a->idx, a->cnt, static_cast<bf*>(y), static_cast<int*>(ws), dev_status,
+                             N, d, f, a->tile, nt, d / twell::Elem<bf>::kPer16B, vals_bf16};
         return twell::run_fused(p, s);
     }
-    twell::FusedArgs<float, float> p{static_cast<const float*>(x), static_cast<const float*>(Wu_s),
-                                     static_cast<const float*>(Wd_s), static_cast<const float*>(a->vals), a->idx,
-                                     a->cnt, static_cast<float*>(y), N, d, f, a->tile, nt, 0, 0, dev_status, 0};
+    twell::RowArgs<float> p{static_cast<const float*>(x), static_cast<const float*>(Wu_s),
+                            static_cast<const float*>(Wd_s), a->vals, a->idx, a->cnt, static_cast<float*>(y),
+                            static_cast<int*>(ws), dev_status, N, d, f, a->tile, nt, d / twell::Elem<float>::kPer16B, 0};
     return twell::run_fused(p, s);
 }

@@ -153,6 +153,13 @@ TWELL_API twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t 
  * TwELL's dtype. The hidden activation h is never written to memory. Rows with no nonzeros get
  * y = 0. x [N, d], Wu_s / Wd_s [f, d], y [N, d] (device, element type `dtype`; the TwELL
  * values may be bf16 or fp32 independently, except that fp32 inputs need fp32 values).
+ * d <= 8192 (bf16) / 4096 (fp32); f / tile <= 1024 tiles.
+ * ws/ws_bytes: device workspace of at least twell_workspace_bytes(TWELL_OP_FFN_FUSED_FWD, ...)
+ * bytes (256), 16-byte aligned, required when N > 0 (else TWELL_ERR_WORKSPACE). The call clears
+ * its first word on `stream` and the kernel hands out token rows from it, so two calls in flight
+ * at the same time must not share one workspace. Its contents need not be initialised.
+ * A corrupt TwELL (count above the tile width, in-tile index >= tile, column >= f) is reported
+ * as TWELL_ERR_DEVICE_CHECK in *dev_status; such entries contribute nothing.
  */
 TWELL_API twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, const void* Wd_s,
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,

@@ -89,8 +89,12 @@ def test_fused_rejects_bad_arguments(lib):
     p = _packed()
     call = lambda **kw: lib.twell_ffn_fused_fwd(  # noqa: E731
         ALIGNED, ALIGNED, ALIGNED, ctypes.byref(kw.get("p", p)), kw.get("N", 4), kw.get("d", 64),
-        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), None, 0, STATUS, None)
+        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), kw.get("ws", ALIGNED), kw.get("ws_bytes", 256),
+        STATUS, None)
     assert call(y=None) == 1
+    assert call(ws=None) == 7  # TWELL_ERR_WORKSPACE: the row-ticket counter is required
+    assert call(ws_bytes=16) == 7
+    assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0  # an empty batch needs no workspace
     assert call(N=5) == 1
     assert call(d=12) == 1
     assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1

@@ -182,6 +182,53 @@ def test_fused_wide_model_two_chunks_per_thread(cuda_dev):
     assert_close(y, y_ref, "fused d=5120")
 
 
+@pytest.mark.parametrize("d,dt", [(64, torch.bfloat16), (1024, torch.bfloat16), (2048, torch.bfloat16),
+                                  (2560, torch.bfloat16), (4096, torch.bfloat16), (1024, torch.float32),
+                                  (2048, torch.float32)])
+def test_fused_every_row_layout(cuda_dev, d, dt):
+    """Every (chunks per lane, warps per row) layout the fused kernel dispatches to, with a ragged
+    last tile (f = 1000) and more rows than resident warps."""
+    L = synthetic.uniform_layer(1500 if d <= 2048 else 600, d, 1000, 128, 0.02, seed=d, bf16=dt == torch.bfloat16)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, dt, torch.float32)
+    assert_close(y, y_ref, f"fused d={d} {dt}")
+
+
+def test_fused_mostly_empty_rows(cuda_dev):
+    """About one nonzero per row: most metadata segments are empty rows (y = 0) or hold one entry."""
+    L = synthetic.uniform_layer(2000, 512, 1000, 128, 0.0008, seed=8)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16)
+    assert (np.abs(y_ref).sum(1) == 0).sum() > 500
+    assert_close(y, y_ref, "fused mostly empty rows")
+    assert np.array_equal(np.abs(y).sum(1) == 0, np.abs(y_ref).sum(1) == 0)
+
+
+def test_fused_reports_corrupt_entries(cuda_dev):
+    """A count above the tile width, an in-tile index >= T and a column >= d_ff are reported as
+    TWELL_ERR_DEVICE_CHECK and contribute nothing; the other rows are unaffected."""
+    L = synthetic.uniform_layer(64, 256, 1000, 128, 0.05, seed=9, bf16=False)
+    G = oracle.gate(L.x, L.Wg_s)
+    vals, idx, cnt = oracle.twell_pack(np.where(G > 0, G, 0.0), L.T)
+    assert cnt[0, 0] > 0 and cnt[1, 0] > 0 and cnt[2, 7] > 0
+    bad_vals, bad_idx, bad_cnt = vals.copy(), idx.copy(), cnt.copy()
+    bad_cnt[0, 0] = L.T + 5  # count above the tile width: the tile is dropped
+    bad_idx[1, 0, 0] = L.T + 3  # in-tile index past the tile
+    bad_idx[2, 7, 0] = 110  # column 7*128 + 110 = 1006 >= d_ff = 1000
+    clean_vals, clean_cnt = vals.copy(), cnt.copy()
+    clean_cnt[0, 0] = 0
+    clean_vals[1, 0, 0] = 0.0
+    clean_vals[2, 7, 0] = 0.0
+    y_ref = oracle.twell_walk(clean_vals, idx, clean_cnt, L.T, L.x, L.Wu_s, L.Wd_s)
+    nt = cnt.shape[1]
+    tw = binding.TwELL(L.N, L.f, L.T, _to(cuda_dev, np.nan_to_num(bad_vals), torch.float32),
+                       torch.from_numpy(bad_idx).to(cuda_dev),
+                       torch.from_numpy(bad_cnt.astype(np.int16)).to(cuda_dev).reshape(L.N, nt))
+    t = L.torch_inputs(cuda_dev, torch.float32)
+    y = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    assert binding.twell_read_status(reset=True) == 5  # TWELL_ERR_DEVICE_CHECK
+    rel, mx = assert_close(y.double().cpu().numpy(), y_ref, "fused with corrupt entries")
+    assert rel < 1e-5
+
+
 def test_fused_long_rows_cross_list_windows(cuda_dev):
     """Rows with more nonzeros than one list window (256) and than the slot ring."""
     L = synthetic.uniform_layer(24, 256, 2048, 128, 0.5, seed=4)
