@@ -19,14 +19,19 @@
 // a ticket counter (the caller's workspace, cleared on the launch stream), so per-token nonzero
 // counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
 //
-// ffn_mma_kernel (bf16, d_model a multiple of 256 up to 2048): nonzeros are taken in batches of
+// ffn_mma_kernel (bf16, d_model 512, 1024, 2048 or 4096): nonzeros are taken in batches of
 // up to 8 of one row. The 8 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
 // mma.sync m16n8k16 with the batch's weight rows as the 8 columns of B and x_r in every row of
 // A (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
 // permuted the same way on both sides, so that each lane reads 32 contiguous bytes). The
-// rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's 64 columns. Weight
+// rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's columns. Weight
 // rows move in 4 KB steps (32 bytes per lane per load, so four lanes cover a 128-byte line)
-// through a three-step register ring, two steps ahead of use across batch and row boundaries.
+// through a register ring, two or three steps ahead of use across batch and row boundaries.
+// For d_model = 4096 two warps share a row, each with half the columns and half the k range
+// (the two partial dot products meet once per batch in shared memory). On the 2048-wide layer
+// one warp per row with a three-step ring measured faster (0.276 ms) than two warps per row
+// with three to five steps (0.31-0.47 ms): the kernel is bound by instruction issue, not by
+// bytes in flight.
 //
 // ffn_rows_kernel (every other shape, fp32): one nonzero at a time, the dot product as a warp
 // reduction (plus a named-barrier exchange between the G warps of a row), weight rows of the
@@ -156,18 +161,24 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Shared memory of one group of G warps: two ticket mailboxes, then 2 x G x 8 partial sums.
+constexpr int kGroupBytes = 16 + 2 * 4 * 8 * 4;
+
 // ------------------------------------------------------------------------------------------
 // The row stream of one group of G warps: row tickets, TwELL metadata one segment ahead, x_r
 // staged by cp.async (CPLX 16-byte chunks per lane: chunk q = q0 + m*32*G sits at
-// s_x[(xs*CPLX + m)*32 + lane], so with G = 1 a buffer holds x_r contiguously).
+// s_x[(xs*CPLX + m)*32 + lane], so with G = 1 a buffer holds x_r contiguously). Every warp of a
+// group runs its own copy of the stream over the same rows; the group's first warp takes the row
+// tickets and hands them to the others through a mailbox behind the group's named barrier.
 template <typename E, int CPLX, int G>
 struct RowStream {
     static constexpr int V = Elem<E>::kPer16B;
     uint4* s_x;
     int* s_pref;
-    int lane, q0, stride;
+    int* s_tk;
+    int lane, wg, q0, bar_id, tpar;
     bool pre;
-    int tk, srow;
+    int tk;
     int creg[kCntRegs];
     int i_row, n_row, i_nnz, i_base, xs_next;              // metadata side
     int nx_row, nx_n, nx_flags, nx_xs, nx_toff;            // next segment (warp-uniform)
@@ -177,18 +188,25 @@ struct RowStream {
 
     __device__ void next_ticket(const RowArgs<E>& a)
     {
-        if constexpr (G == 1) {
-            tk = 0;
-            if (lane == 0) tk = atomicAdd(a.tickets, 1);
-        } else {
-            tk = srow;
-            srow += stride;
-        }
+        tk = 0;
+        if (wg == 0 && lane == 0) tk = atomicAdd(a.tickets, 1);
     }
-    __device__ int ticket_row() const
+    // The ticket taken one call of next_ticket earlier (its atomic has had a row's time to land).
+    __device__ int ticket_row()
     {
-        if constexpr (G == 1) return __shfl_sync(0xffffffffu, tk, 0);
-        else return tk;
+        if constexpr (G == 1) {
+            return __shfl_sync(0xffffffffu, tk, 0);
+        } else {
+            int v = 0;
+            if (wg == 0) {
+                v = __shfl_sync(0xffffffffu, tk, 0);
+                if (lane == 0) s_tk[tpar] = v;
+            }
+            bar_sync_named(bar_id, 32 * G);
+            if (wg != 0) v = s_tk[tpar];
+            tpar ^= 1;  // the next write goes to the other box: a reader may still be on this one
+            return v;
+        }
     }
     __device__ void load_counts(const RowArgs<E>& a, int r)
     {
@@ -304,15 +322,17 @@ struct RowStream {
         E* yr = a.y + static_cast<size_t>(row) * a.d;
         for (int q = q0; q < a.nchunks; q += 32 * G) st_stream16(yr + q * V, make_uint4(0, 0, 0, 0));
     }
-    __device__ void init(const RowArgs<E>& a, uint4* sx, int* spref, int lane_, int wg, int group, int groups)
+    __device__ void init(const RowArgs<E>& a, uint4* sx, int* spref, int* stk, int lane_, int wg_, int bar)
     {
         s_x = sx;
         s_pref = spref;
+        s_tk = stk;
         lane = lane_;
+        wg = wg_;
         q0 = wg * 32 + lane;
-        stride = groups;
+        bar_id = bar;
+        tpar = 0;
         pre = a.nt <= 32 * kCntRegs;
-        srow = group;
         tk = 0;
         i_row = n_row = a.N;
         i_nnz = i_base = xs_next = 0;
@@ -367,7 +387,7 @@ template <int CPL>
 struct RowSmem {
     __host__ __device__ static size_t x_bytes() { return static_cast<size_t>(kXBufs) * CPL * 32 * 16; }
     __host__ __device__ static size_t warp_bytes(int nt) { return x_bytes() + pref_bytes(nt); }
-    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * warp_bytes(nt) + 2 * kCtaWarps * 4; }
+    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * warp_bytes(nt) + kCtaWarps * kGroupBytes; }
 };
 
 template <typename E, int CPL, int G>
@@ -375,21 +395,22 @@ __global__ void __launch_bounds__(kCtaThreads, (CPL >= 5 ? 2 : CPL == 4 ? 3 : 4)
 {
     constexpr int V = Elem<E>::kPer16B;
     constexpr int P = Chunk<E>::P;
-    constexpr int kGroups = kCtaWarps / G;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wg = warp % G, grp = warp / G;
     const size_t wbytes = RowSmem<CPL>::warp_bytes(a.nt);
     uint4* s_x = reinterpret_cast<uint4*>(smem + warp * wbytes);
     int* s_pref = reinterpret_cast<int*>(smem + warp * wbytes + RowSmem<CPL>::x_bytes());
-    float* s_part = reinterpret_cast<float*>(smem + kCtaWarps * wbytes) + grp * 2 * G;
+    uint8_t* gsm = smem + kCtaWarps * wbytes + grp * kGroupBytes;
+    int* s_tk = reinterpret_cast<int*>(gsm);
+    float* s_part = reinterpret_cast<float*>(gsm + 16);
 
     const uint64_t pol = policy_evict_last();
     const int nchunks = a.nchunks;
     const int q0 = wg * 32 + lane;  // chunk of m = 0; chunk m is q0 + m * 32 * G
 
     RowStream<E, CPL, G> rs;
-    rs.init(a, s_x, s_pref, lane, wg, blockIdx.x * kGroups + grp, gridDim.x * kGroups);
+    rs.init(a, s_x, s_pref, s_tk, lane, wg, 1 + grp);
     auto next_entry = [&](Entry& en) -> bool {
         if (!rs.ready(a)) return false;
         en.j = __shfl_sync(0xffffffffu, rs.c_j, rs.pos);
@@ -505,7 +526,10 @@ __global__ void __launch_bounds__(kCtaThreads, (CPL >= 5 ? 2 : CPL == 4 ? 3 : 4)
 }
 
 // ------------------------------------------------------------------------------------------
-// Tensor-core kernel (bf16, d_model % 256 == 0, 512 <= d_model <= 2048, one warp per row).
+// Tensor-core kernel (bf16, d_model / G = 512 * CPL with CPL in {1, 2, 4}): a group of G warps
+// per row, each warp owning d_model / G columns for the down projection and the same share of
+// the k range of the dot products (256-column blocks wg, wg + G, ...: the blocks of x_r its
+// row stream stages).
 
 constexpr int kBatch = 8;  // nonzeros per batch: the n dimension of m16n8k16
 constexpr int kBatchSlots = 4;
@@ -517,7 +541,7 @@ struct __align__(16) BatchDesc {
     float h[kBatch];        // h = a * u, filled when the batch's dot products are done
 };
 
-template <int CPL>  // 32-byte chunks per lane of a weight row in the down projection
+template <int CPL>  // 32-byte chunks per lane of the warp's columns in the down projection
 struct MmaSmem {
     static constexpr int CPLX = 2 * CPL;  // 16-byte x chunks per lane
     __host__ __device__ static size_t x_bytes() { return static_cast<size_t>(kXBufs) * CPLX * 32 * 16; }
@@ -525,35 +549,42 @@ struct MmaSmem {
     {
         return x_bytes() + pref_bytes(nt) + kBatchSlots * sizeof(BatchDesc);
     }
-    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * warp_bytes(nt); }
+    __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * (warp_bytes(nt) + kGroupBytes); }
 };
 
-template <int CPL>
+// CPL in {1, 2, 4}: a warp's columns are 512 * CPL; R: depth of the register ring of 4 KB steps.
+template <int CPL, int G, int R>
 __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<__nv_bfloat16> a)
 {
     using E = __nv_bfloat16;
     constexpr int CPLX = MmaSmem<CPL>::CPLX;
+    constexpr int EPS = 4 / CPL;  // nonzeros per down-projection step
+    constexpr int nU = CPL * 2;   // up-projection steps per batch (256 columns of d_model each)
     constexpr int kU = 1, kD = 2, kEnd = 3;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wg = warp % G, grp = warp / G;
     const int g = lane >> 2, t = lane & 3;
     const size_t wbytes = MmaSmem<CPL>::warp_bytes(a.nt);
     uint8_t* wsm = smem + warp * wbytes;
     uint4* s_x = reinterpret_cast<uint4*>(wsm);
     int* s_pref = reinterpret_cast<int*>(wsm + MmaSmem<CPL>::x_bytes());
     BatchDesc* s_bd = reinterpret_cast<BatchDesc*>(wsm + MmaSmem<CPL>::x_bytes() + pref_bytes(a.nt));
+    uint8_t* gsm = smem + kCtaWarps * wbytes + grp * kGroupBytes;
+    int* s_tk = reinterpret_cast<int*>(gsm);
+    float* s_part = reinterpret_cast<float*>(gsm + 16);  // [2][G][8]
 
     const uint64_t pol = policy_evict_last();
-    const int nU = a.d / 256;  // up-projection steps per batch (256 columns of d_model each)
-    const int n32 = a.d / 16;  // 32-byte chunks of a row
+    const int dh = a.d / G;  // this warp's columns of the down projection: [wg * dh, (wg + 1) * dh)
 
-    RowStream<E, CPLX, 1> rs;
-    rs.init(a, s_x, s_pref, lane, 0, blockIdx.x * kCtaWarps + warp, gridDim.x * kCtaWarps);
+    RowStream<E, CPLX, G> rs;
+    rs.init(a, s_x, s_pref, s_tk, lane, wg, 1 + grp);
 
     // -------------------------------------------------------------- issue side: 4 KB steps
     // A batch of k nonzeros is nU up-projection steps (lane (g, t) loads 32 bytes of Wu_s[j_g]
-    // at column 64c + 16t, four c per step) followed by k down-projection steps (lane loads its
-    // CPL 32-byte chunks of Wd_s[j_e]). The tag of a step: kind | batch slot << 2 | step << 4.
+    // at column 256 * (i * G + wg) + 64c + 16t, c = 0..3, in step i) followed by ceil(k / EPS)
+    // down-projection steps (lane loads its CPL 32-byte chunks of Wd_s[j_e] for EPS nonzeros).
+    // The tag of a step: kind | batch slot << 2 | step << 4.
     int is_slot = 0, is_step = 0, is_nsteps = 0, is_k = 0, nslot = 0;
     bool ended = false;
     auto form_batch = [&](BatchDesc* D) -> bool {
@@ -587,23 +618,26 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
             is_slot = nslot;
             nslot = (nslot + 1) & (kBatchSlots - 1);
             is_k = s_bd[is_slot].k;
-            is_nsteps = nU + is_k;
+            is_nsteps = nU + (is_k + EPS - 1) / EPS;
             is_step = 0;
         }
         const BatchDesc* D = &s_bd[is_slot];
         if (is_step < nU) {
             if (g < is_k) {
-                const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + 256 * is_step + 16 * t;
+                const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + 256 * (is_step * G + wg) + 16 * t;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) ldg_keep32(B[cc], w + 64 * cc, pol);
             }
             tag = kU;
         } else {
-            const E* w = a.Wd + static_cast<size_t>(D->j[is_step - nU]) * a.d;
+            const int e0 = (is_step - nU) * EPS;
 #pragma unroll
-            for (int m = 0; m < CPL; ++m) {
-                const int q = lane + 32 * m;
-                if (q < n32) ldg_keep32(B[m], w + 16 * q, pol);
+            for (int ee = 0; ee < EPS; ++ee) {
+                if (e0 + ee < is_k) {
+                    const E* w = a.Wd + static_cast<size_t>(D->j[e0 + ee]) * a.d + wg * dh + 16 * lane;
+#pragma unroll
+                    for (int m = 0; m < CPL; ++m) ldg_keep32(B[ee * CPL + m], w + 512 * m, pol);
+                }
             }
             tag = kD;
         }
@@ -612,39 +646,57 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     };
 
     // -------------------------------------------------------------- process side
-    float macc[2][4];  // two accumulator sets: independent mma chains
+    float macc[4][4];  // four accumulator sets: independent mma chains
 #pragma unroll
-    for (int i = 0; i < 2; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
+    for (int i = 0; i < 4; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
     uint64_t acc[CPL][8];
 #pragma unroll
     for (int m = 0; m < CPL; ++m)
 #pragma unroll
         for (int w = 0; w < 8; ++w) acc[m][w] = 0;
+    int par = 0;
     auto process = [&](const uint32_t (&B)[4][8], int tag) {
         BatchDesc* D = &s_bd[(tag >> 2) & (kBatchSlots - 1)];
         const int step = tag >> 4;
         if ((tag & 3) == kU) {
             if (step == 0) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
+                for (int i = 0; i < 4; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
             }
             // x_r in every row of A; B column n is the batch's nonzero n. Inside each 16-wide k
-            // block, k slots (2t, 2t+1, 2t+8, 2t+9) hold columns o+4b .. o+4b+3 of d_model with
-            // o = 64c + 16t, on both sides.
-            const uint4* xr = s_x + D->xs * (CPLX * 32);
+            // block, k slots (2t, 2t+1, 2t+8, 2t+9) hold columns o+4b .. o+4b+3 of the step's 256
+            // columns with o = 64c + 16t, on both sides.
+            const uint4* xr = s_x + (D->xs * CPLX + step) * 32;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                const int c = 4 * step + cc;
-                const uint4 X0 = xr[8 * c + 2 * t], X1 = xr[8 * c + 2 * t + 1];
+                const uint4 X0 = xr[8 * cc + 2 * t], X1 = xr[8 * cc + 2 * t + 1];
                 mma_bf16(macc[0], X0.x, X0.x, X0.y, X0.y, B[cc][0], B[cc][1]);
                 mma_bf16(macc[1], X0.z, X0.z, X0.w, X0.w, B[cc][2], B[cc][3]);
-                mma_bf16(macc[0], X1.x, X1.x, X1.y, X1.y, B[cc][4], B[cc][5]);
-                mma_bf16(macc[1], X1.z, X1.z, X1.w, X1.w, B[cc][6], B[cc][7]);
+                mma_bf16(macc[2], X1.x, X1.x, X1.y, X1.y, B[cc][4], B[cc][5]);
+                mma_bf16(macc[3], X1.z, X1.z, X1.w, X1.w, B[cc][6], B[cc][7]);
             }
             if (step == nU - 1) {
-                // lane (g, t) holds u of nonzeros 2t and 2t+1 (every row of D is the same)
-                const float u0 = macc[0][0] + macc[1][0];
-                const float u1 = macc[0][1] + macc[1][1];
+                // lane (g, t) holds this warp's part of u for nonzeros 2t and 2t+1 (every row of D
+                // is the same); the G parts are added in warp order by every warp of the group
+                float u0 = (macc[0][0] + macc[1][0]) + (macc[2][0] + macc[3][0]);
+                float u1 = (macc[0][1] + macc[1][1]) + (macc[2][1] + macc[3][1]);
+                if constexpr (G > 1) {
+                    float* sp = s_part + par * G * 8;
+                    if (lane < 4) {
+                        sp[wg * 8 + 2 * lane] = u0;
+                        sp[wg * 8 + 2 * lane + 1] = u1;
+                    }
+                    bar_sync_named(1 + grp, 32 * G);
+                    u0 = u1 = 0.0f;
+                    if (lane < 4) {
+#pragma unroll
+                        for (int w = 0; w < G; ++w) {
+                            u0 += sp[w * 8 + 2 * lane];
+                            u1 += sp[w * 8 + 2 * lane + 1];
+                        }
+                    }
+                    par ^= 1;
+                }
                 if (lane < 4) {
                     D->h[2 * lane] = D->a[2 * lane] * u0;
                     D->h[2 * lane + 1] = D->a[2 * lane + 1] * u1;
@@ -652,32 +704,30 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
                 __syncwarp();
             }
         } else {
-            const int e = step - nU;
-            const float h = D->h[e];
-            const uint64_t h2 = f2pack(h, h);
+            const int e0 = (step - nU) * EPS;
 #pragma unroll
-            for (int m = 0; m < CPL; ++m) {
-                const int q = lane + 32 * m;
-                if (q < n32) {
+            for (int ee = 0; ee < EPS; ++ee) {
+                if (e0 + ee < D->k) {
+                    const float h = D->h[e0 + ee];
+                    const uint64_t h2 = f2pack(h, h);
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) fma2(acc[m][w], h2, bf2_to_f2(B[m][w]));
+                    for (int m = 0; m < CPL; ++m)
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) fma2(acc[m][w], h2, bf2_to_f2(B[ee * CPL + m][w]));
                 }
             }
-            if (e == D->k - 1 && (D->flags & kLast)) {
-                E* yr = a.y + static_cast<size_t>(D->row) * a.d;
+            if (e0 + EPS >= D->k && (D->flags & kLast)) {
+                E* yr = a.y + static_cast<size_t>(D->row) * a.d + wg * dh + 16 * lane;
 #pragma unroll
                 for (int m = 0; m < CPL; ++m) {
-                    const int q = lane + 32 * m;
-                    if (q < n32) {
-                        float lo8[8], hi8[8];
+                    float lo8[8], hi8[8];
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            f2unpack(acc[m][w], lo8[2 * w], lo8[2 * w + 1]);
-                            f2unpack(acc[m][w + 4], hi8[2 * w], hi8[2 * w + 1]);
-                        }
-                        st_stream16(yr + 16 * q, pack16(lo8, static_cast<E*>(nullptr)));
-                        st_stream16(yr + 16 * q + 8, pack16(hi8, static_cast<E*>(nullptr)));
+                    for (int w = 0; w < 4; ++w) {
+                        f2unpack(acc[m][w], lo8[2 * w], lo8[2 * w + 1]);
+                        f2unpack(acc[m][w + 4], hi8[2 * w], hi8[2 * w + 1]);
                     }
+                    st_stream16(yr + 512 * m, pack16(lo8, static_cast<E*>(nullptr)));
+                    st_stream16(yr + 512 * m + 8, pack16(hi8, static_cast<E*>(nullptr)));
 #pragma unroll
                     for (int w = 0; w < 8; ++w) acc[m][w] = 0;
                 }
@@ -685,24 +735,26 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
         }
     };
 
-    uint32_t B0[4][8], B1[4][8], B2[4][8];
+    uint32_t B[R][4][8];
+    int tg[R];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int w = 0; w < 8; ++w) B0[i][w] = B1[i][w] = B2[i][w] = 0;
-    int t0, t1, t2;
-    issue(B0, t0);
-    issue(B1, t1);
-    for (;;) {
-        issue(B2, t2);
-        if (t0 == kEnd) break;
-        process(B0, t0);
-        issue(B0, t0);
-        if (t1 == kEnd) break;
-        process(B1, t1);
-        issue(B1, t1);
-        if (t2 == kEnd) break;
-        process(B2, t2);
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int w = 0; w < 8; ++w) B[r][i][w] = 0;
+#pragma unroll
+    for (int r = 0; r < R - 1; ++r) issue(B[r], tg[r]);
+    bool run = true;
+    while (run) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (run) {
+                issue(B[(r + R - 1) % R], tg[(r + R - 1) % R]);
+                if (tg[r] == kEnd) run = false;
+                else process(B[r], tg[r]);
+            }
+        }
     }
     cp_async_wait<0>();
 }
@@ -711,8 +763,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
 // Launch
 
 template <typename E, typename K>
-static twell_status launch_persistent(K kern, const RowArgs<E>& a, size_t smem, int groups_per_cta, bool tickets,
-                                      cudaStream_t s)
+static twell_status launch_persistent(K kern, const RowArgs<E>& a, size_t smem, int groups_per_cta, cudaStream_t s)
 {
     twell_host::DevInfo di;
     if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
@@ -722,7 +773,7 @@ static twell_status launch_persistent(K kern, const RowArgs<E>& a, size_t smem, 
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCtaThreads, smem) != cudaSuccess || per_sm < 1)
         return TWELL_ERR_CUDA;
-    if (tickets && cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    if (cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
     const int need = (a.N + groups_per_cta - 1) / groups_per_cta;  // CTAs until every group has a row
     int grid = di.sm_count * per_sm;
     if (grid > need) grid = need;
@@ -733,13 +784,13 @@ static twell_status launch_persistent(K kern, const RowArgs<E>& a, size_t smem, 
 template <typename E, int CPL, int G>
 static twell_status launch_rows(const RowArgs<E>& a, cudaStream_t s)
 {
-    return launch_persistent(ffn_rows_kernel<E, CPL, G>, a, RowSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, G == 1, s);
+    return launch_persistent(ffn_rows_kernel<E, CPL, G>, a, RowSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, s);
 }
 
-template <int CPL>
+template <int CPL, int G, int R>
 static twell_status launch_mma(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
 {
-    return launch_persistent(ffn_mma_kernel<CPL>, a, MmaSmem<CPL>::cta_bytes(a.nt), kCtaWarps, true, s);
+    return launch_persistent(ffn_mma_kernel<CPL, G, R>, a, MmaSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, s);
 }
 
 // Kernel and layout for d_model = nchunks 16-byte chunks: the tensor-core kernel where it applies,
@@ -749,11 +800,10 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
 {
     if constexpr (std::is_same<E, __nv_bfloat16>::value) {
         const bool a32 = (reinterpret_cast<uintptr_t>(a.Wu) % 32 == 0) && (reinterpret_cast<uintptr_t>(a.Wd) % 32 == 0);
-        if (a32 && a.d % 256 == 0 && a.d >= 512 && a.d <= 2048) {
-            if (a.d <= 512) return launch_mma<1>(a, s);
-            if (a.d <= 1024) return launch_mma<2>(a, s);
-            return launch_mma<4>(a, s);
-        }
+        if (a32 && a.d == 512) return launch_mma<1, 1, 4>(a, s);
+        if (a32 && a.d == 1024) return launch_mma<2, 1, 3>(a, s);
+        if (a32 && a.d == 2048) return launch_mma<4, 1, 3>(a, s);
+        if (a32 && a.d == 4096) return launch_mma<4, 2, 3>(a, s);
     }
     const int n = a.nchunks;
     if (n <= 32 * 2) return launch_rows<E, 2, 1>(a, s);

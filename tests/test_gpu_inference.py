@@ -182,7 +182,7 @@ def test_fused_wide_model_two_chunks_per_thread(cuda_dev):
     assert_close(y, y_ref, "fused d=5120")
 
 
-@pytest.mark.parametrize("d,dt", [(64, torch.bfloat16), (1024, torch.bfloat16), (2048, torch.bfloat16),
+@pytest.mark.parametrize("d,dt", [(64, torch.bfloat16), (512, torch.bfloat16), (1024, torch.bfloat16), (2048, torch.bfloat16),
                                   (2560, torch.bfloat16), (4096, torch.bfloat16), (1024, torch.float32),
                                   (2048, torch.float32)])
 def test_fused_every_row_layout(cuda_dev, d, dt):
