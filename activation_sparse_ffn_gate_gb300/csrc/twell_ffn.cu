@@ -20,9 +20,9 @@
 // counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
 //
 // ffn_mma_kernel (bf16, d_model 512, 1024, 2048 or 4096): nonzeros are taken in batches of
-// up to 8 of one row. The 8 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
-// mma.sync m16n8k16 with the batch's weight rows as the 8 columns of B and x_r in every row of
-// A (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
+// up to 16 of one row. The 16 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
+// mma.sync m16n8k16 with the batch's weight rows as the 16 rows of A and x_r in every column of
+// B (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
 // permuted the same way on both sides, so that each lane reads 32 contiguous bytes). The
 // rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's columns. Weight
 // rows move in 4 KB steps (32 bytes per lane per load, so four lanes cover a 128-byte line)
@@ -161,8 +161,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared memory of one group of G warps: two ticket mailboxes, then 2 x G x 8 partial sums.
-constexpr int kGroupBytes = 16 + 2 * 4 * 8 * 4;
+// Shared memory of one group of G warps: two ticket mailboxes, then the partial dot products
+// (2 x G floats for the general kernel, G <= 4; 2 x G x 16 for the tensor-core kernel, G <= 2).
+constexpr int kGroupBytes = 16 + 2 * 2 * 16 * 4;
 
 // ------------------------------------------------------------------------------------------
 // The row stream of one group of G warps: row tickets, TwELL metadata one segment ahead, x_r
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(kCtaThreads, (CPL >= 5 ? 2 : CPL == 4 ? 3 : 4)
 // the k range of the dot products (256-column blocks wg, wg + G, ...: the blocks of x_r its
 // row stream stages).
 
-constexpr int kBatch = 8;  // nonzeros per batch: the n dimension of m16n8k16
+constexpr int kBatch = 16;  // nonzeros per batch: the m dimension of m16n8k16
 constexpr int kBatchSlots = 4;
 
 struct __align__(16) BatchDesc {
@@ -559,7 +560,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     using E = __nv_bfloat16;
     constexpr int CPLX = MmaSmem<CPL>::CPLX;
     constexpr int EPS = 4 / CPL;  // nonzeros per down-projection step
-    constexpr int nU = CPL * 2;   // up-projection steps per batch (256 columns of d_model each)
+    constexpr int nU = CPL * 4;   // up-projection steps per batch (128 columns of d_model each)
     constexpr int kU = 1, kD = 2, kEnd = 3;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     BatchDesc* s_bd = reinterpret_cast<BatchDesc*>(wsm + MmaSmem<CPL>::x_bytes() + pref_bytes(a.nt));
     uint8_t* gsm = smem + kCtaWarps * wbytes + grp * kGroupBytes;
     int* s_tk = reinterpret_cast<int*>(gsm);
-    float* s_part = reinterpret_cast<float*>(gsm + 16);  // [2][G][8]
+    float* s_part = reinterpret_cast<float*>(gsm + 16);  // [2][G][16]
 
     const uint64_t pol = policy_evict_last();
     const int dh = a.d / G;  // this warp's columns of the down projection: [wg * dh, (wg + 1) * dh)
@@ -581,9 +582,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     rs.init(a, s_x, s_pref, s_tk, lane, wg, 1 + grp);
 
     // -------------------------------------------------------------- issue side: 4 KB steps
-    // A batch of k nonzeros is nU up-projection steps (lane (g, t) loads 32 bytes of Wu_s[j_g]
-    // at column 256 * (i * G + wg) + 64c + 16t, c = 0..3, in step i) followed by ceil(k / EPS)
-    // down-projection steps (lane loads its CPL 32-byte chunks of Wd_s[j_e] for EPS nonzeros).
+    // A batch of k <= 16 nonzeros is nU up-projection steps (step i covers columns
+    // 256 * ((i / 2) * G + wg) + 128 * (i % 2) + [0, 128): lane (g, t) loads 32 bytes of Wu_s[j_g] and
+    // of Wu_s[j_{g+8}] at offset 64c + 16t, c = 0, 1) followed by ceil(k / EPS) down-projection steps
+    // (lane loads its CPL 32-byte chunks of Wd_s[j_e] for EPS nonzeros).
     // The tag of a step: kind | batch slot << 2 | step << 4.
     int is_slot = 0, is_step = 0, is_nsteps = 0, is_k = 0, nslot = 0;
     bool ended = false;
@@ -623,10 +625,16 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
         }
         const BatchDesc* D = &s_bd[is_slot];
         if (is_step < nU) {
+            const int col = 256 * ((is_step >> 1) * G + wg) + 128 * (is_step & 1) + 16 * t;
             if (g < is_k) {
-                const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + 256 * (is_step * G + wg) + 16 * t;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) ldg_keep32(B[cc], w + 64 * cc, pol);
+                const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + col;
+                ldg_keep32(B[0], w, pol);
+                ldg_keep32(B[2], w + 64, pol);
+            }
+            if (g + 8 < is_k) {
+                const E* w = a.Wu + static_cast<size_t>(D->j[g + 8]) * a.d + col;
+                ldg_keep32(B[1], w, pol);
+                ldg_keep32(B[3], w + 64, pol);
             }
             tag = kU;
         } else {
@@ -663,43 +671,43 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
 #pragma unroll
                 for (int i = 0; i < 4; ++i) macc[i][0] = macc[i][1] = macc[i][2] = macc[i][3] = 0.0f;
             }
-            // x_r in every row of A; B column n is the batch's nonzero n. Inside each 16-wide k
-            // block, k slots (2t, 2t+1, 2t+8, 2t+9) hold columns o+4b .. o+4b+3 of the step's 256
-            // columns with o = 64c + 16t, on both sides.
-            const uint4* xr = s_x + (D->xs * CPLX + step) * 32;
+            // A row m is the batch's nonzero m (rows g: B[0], B[2]; rows g+8: B[1], B[3]); x_r in
+            // every column of B. Inside each 16-wide k block, k slots (2t, 2t+1, 2t+8, 2t+9) hold
+            // columns o+4b .. o+4b+3 of the step's 128 columns with o = 64c + 16t, on both sides.
+            const uint4* xr = s_x + (D->xs * CPLX + (step >> 1)) * 32 + 16 * (step & 1);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const uint32_t(&Wg)[8] = B[2 * cc];
+                const uint32_t(&Wg8)[8] = B[2 * cc + 1];
                 const uint4 X0 = xr[8 * cc + 2 * t], X1 = xr[8 * cc + 2 * t + 1];
-                mma_bf16(macc[0], X0.x, X0.x, X0.y, X0.y, B[cc][0], B[cc][1]);
-                mma_bf16(macc[1], X0.z, X0.z, X0.w, X0.w, B[cc][2], B[cc][3]);
-                mma_bf16(macc[2], X1.x, X1.x, X1.y, X1.y, B[cc][4], B[cc][5]);
-                mma_bf16(macc[3], X1.z, X1.z, X1.w, X1.w, B[cc][6], B[cc][7]);
+                mma_bf16(macc[0], Wg[0], Wg8[0], Wg[1], Wg8[1], X0.x, X0.y);
+                mma_bf16(macc[1], Wg[2], Wg8[2], Wg[3], Wg8[3], X0.z, X0.w);
+                mma_bf16(macc[2], Wg[4], Wg8[4], Wg[5], Wg8[5], X1.x, X1.y);
+                mma_bf16(macc[3], Wg[6], Wg8[6], Wg[7], Wg8[7], X1.z, X1.w);
             }
             if (step == nU - 1) {
-                // lane (g, t) holds this warp's part of u for nonzeros 2t and 2t+1 (every row of D
-                // is the same); the G parts are added in warp order by every warp of the group
+                // lane (g, t) holds this warp's part of u for nonzeros g (D row g) and g+8 (row
+                // g+8), the same in every column; the G parts are added in warp order by every warp
                 float u0 = (macc[0][0] + macc[1][0]) + (macc[2][0] + macc[3][0]);
-                float u1 = (macc[0][1] + macc[1][1]) + (macc[2][1] + macc[3][1]);
+                float u1 = (macc[0][2] + macc[1][2]) + (macc[2][2] + macc[3][2]);
                 if constexpr (G > 1) {
-                    float* sp = s_part + par * G * 8;
-                    if (lane < 4) {
-                        sp[wg * 8 + 2 * lane] = u0;
-                        sp[wg * 8 + 2 * lane + 1] = u1;
+                    float* sp = s_part + par * G * 16;
+                    if (t == 0) {
+                        sp[wg * 16 + g] = u0;
+                        sp[wg * 16 + g + 8] = u1;
                     }
                     bar_sync_named(1 + grp, 32 * G);
                     u0 = u1 = 0.0f;
-                    if (lane < 4) {
 #pragma unroll
-                        for (int w = 0; w < G; ++w) {
-                            u0 += sp[w * 8 + 2 * lane];
-                            u1 += sp[w * 8 + 2 * lane + 1];
-                        }
+                    for (int w = 0; w < G; ++w) {
+                        u0 += sp[w * 16 + g];
+                        u1 += sp[w * 16 + g + 8];
                     }
                     par ^= 1;
                 }
-                if (lane < 4) {
-                    D->h[2 * lane] = D->a[2 * lane] * u0;
-                    D->h[2 * lane + 1] = D->a[2 * lane + 1] * u1;
+                if (t == 0) {
+                    D->h[g] = D->a[g] * u0;
+                    D->h[g + 8] = D->a[g + 8] * u1;
                 }
                 __syncwarp();
             }

@@ -13,6 +13,7 @@ layer roofline of the method's byte model, the speedup over a dense cuBLAS bf16 
 shape, an end-to-end figure with host buffers, and the fp64 CPU oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --sweep     # density x tile-width sweep and the 2B-like layer, one line each
 N > 1 is launched with torchrun: every rank runs its own batch (weak scaling, no collective on
 the data path; a barrier and a max over ranks of the timed region only).
 """
@@ -44,7 +45,27 @@ def _args():
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-train", action="store_true", help="skip the hybrid training-step measurement")
     p.add_argument("--train-steps", type=int, default=20)
+    p.add_argument("--sweep", action="store_true",
+                   help="density x tile-width sweep on the 1.5B-like shapes and the 2B-like layer, against dense "
+                        "cuBLAS (one JSON line per point; not the default bench line)")
+    p.add_argument("--sweep-iters", type=int, default=15)
     return p.parse_args()
+
+
+def max_over_ranks(value, dist, device):
+    """Largest value over the ranks of the process group (the timed region ends when the slowest
+    rank ends), or the value itself without a group."""
+    if dist is None:
+        return value
+    import torch
+    tt = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return tt.item()
+
+
+def weak_scaling_rate(tokens_per_rank, ms_per_step, world):
+    """Whole-job tokens/s when every rank processes its own batch of tokens_per_rank per step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
 
 
 def _peaks():
@@ -267,12 +288,20 @@ def run_ours(a, rank, world):
     t_gate = [e0.elapsed_time(e1) for e0, e1, _ in ev]
     t_fused = [e1.elapsed_time(e2) for _, e1, e2 in ev]
     t_step = sum(t_gate) + sum(t_fused)  # ms over K steps, L2 flushes excluded
-    if dist:
-        tt = torch.tensor([t_step], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = tt.item()
+    t_step = max_over_ranks(t_step, dist, dev)
     ms_step = t_step / a.steps
-    value = world * N / (ms_step * 1e-3)
+    value = weak_scaling_rate(N, ms_step, world)
+
+    # the same step without the L2 flush in between (weights and x may stay L2-resident)
+    warm_steps = max(10, min(a.steps, 200))
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step()
+    w0.record(stream)
+    for _ in range(warm_steps):
+        step()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks(w0.elapsed_time(w1) / warm_steps, dist, dev)
 
     if rank != 0:
         if dist:
@@ -367,10 +396,17 @@ def run_ours(a, rank, world):
 
     cpu = None
     if not a.no_cpu_baseline:
+        import oracle
+        oracle.set_threads(_cores())
         rate, n_rows, secs = cpu_oracle_rate(L)
         cpu = {"value": rate, "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                "sample": f"{n_rows} random token rows of the {N}-token batch (fp64 gate GEMV, TwELL pack, fused "
                          f"walk), {secs:.1f} s wall"}
+        oracle.set_threads(1)
+        rate1, n1, secs1 = cpu_oracle_rate(L, target_s=2.0, max_rows=512)
+        oracle.set_threads(_cores())
+        cpu["one_core"] = {"value": rate1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"{n1} random token rows, {secs1:.1f} s wall"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
@@ -385,6 +421,8 @@ def run_ours(a, rank, world):
                            "definition": "max(gate FLOPs / bf16 peak, (x + Wg + union of active Wu/Wd rows per "
                                          "128-token tile + y) / HBM peak)"},
         "kernels_ms": {"twell_gate_pack": mg, "twell_ffn_fused_fwd": mf},
+        "warm": {"ms_per_step": warm_ms, "tokens_per_s": weak_scaling_rate(N, warm_ms, world),
+                 "l2": "not flushed between steps"},
         "vs_dense_cublas": dense,
         "train_step": train,
         "cpu_baseline": cpu,
@@ -463,10 +501,75 @@ def train_step_measure(a, dev, flush, peaks):
             "launches_per_step": 23, "l2": "flushed before every step"}
 
 
+def run_sweep(a):
+    """Density x tile-width sweep on the 1.5B-like shapes (N=8192, d=2048, f=5632, uniform density
+    p, no dead columns) and the 2B-like layer, each against a dense cuBLAS bf16 FFN of the same
+    shape. One JSON line per point; L2 flushed before every timed iteration, median of the rest."""
+    import torch
+
+    from activation_sparse_ffn_gate_gb300 import binding, build, synthetic
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    status = binding.status_buffer(dev)
+    status.zero_()
+
+    def timed(fn, n):
+        for _ in range(3):
+            flush.fill_(1)
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
+    layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
+    layers.append(("layer2b", synthetic.layer_2b))
+    for label, make in layers:
+        L = make()
+        t = L.torch_inputs(dev)
+        x, Wg, Wu, Wd = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"]
+        packed = binding.TwELL.empty(L.N, L.f, L.T, torch.float32, dev)
+        y = torch.empty((L.N, L.d), dtype=torch.bfloat16, device=dev)
+        binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)
+        nnz = int(packed.counts().sum().item())
+        n_it = a.sweep_iters if nnz / L.N < 400 else max(3, a.sweep_iters // 3)
+        ms_gate = timed(lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status), n_it)
+        ms_fused = timed(lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status), n_it)
+
+        def dense_fn():
+            return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
+
+        ms_dense = timed(dense_fn, n_it)
+        binding.check_device_status(label, status)
+        ms = ms_gate + ms_fused
+        print(json.dumps({"sweep": label, "workload": L.name, "N": L.N, "d_model": L.d, "d_ff": L.f, "T": L.T,
+                          "density": nnz / (L.N * L.f), "nnz_per_token": nnz / L.N, "ms_gate_pack": ms_gate,
+                          "ms_fused": ms_fused, "ms_sparse": ms, "tokens_per_s": L.N / (ms * 1e-3),
+                          "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
+                          "l2": "flushed before every iteration"}), flush=True)
+        del t, x, Wg, Wu, Wd, packed, y
+        torch.cuda.empty_cache()
+
+
 def main():
     a = _args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", a.gpus if a.gpus == 1 else 1))
+    if a.sweep:
+        if rank == 0:
+            run_sweep(a)
+        return
     if a.impl == "reference":
         run_reference(a, rank, world)
     else:

@@ -56,6 +56,8 @@ def _load():
             lib.oracle_l1.argtypes = [i64, i64, i64, dbl, vp, vp, vp]
             lib.oracle_ffn_bwd_rows.argtypes = [i64, vp, i64, i64, i64, dbl, vp, vp, vp, vp, vp, vp]
             lib.oracle_ffn_bwd_cols.argtypes = [i64, vp, i64, i64, i64, dbl, vp, vp, vp, vp, vp, vp, vp, vp]
+            lib.oracle_set_threads.argtypes = [i64]
+            lib.oracle_max_threads.restype = i64
             _lib = lib
     return _lib
 
@@ -88,6 +90,16 @@ def round_bf16(a):
 
 
 # ------------------------------------------------------------------------------ dense layer
+
+def set_threads(n: int) -> None:
+    """Threads the oracle's OpenMP loops use from now on (for timing: per-row results do not depend on it;
+    the order in which the L1 sum adds its per-thread parts does)."""
+    _load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
 
 def gate(x, Wg_s, rows=None):
     """G[rows] = x[rows] Wg_s^T in fp64."""

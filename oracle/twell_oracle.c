@@ -24,6 +24,7 @@
  * invariants, closed forms, brute force on tiny inputs and central finite differences.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -329,3 +330,8 @@ EXPORT void oracle_ffn_bwd_cols(i64 n_sel, const i64* cols, i64 N, i64 d, i64 f,
         }
     }
 }
+
+/* Threads used by the parallel loops above (test infrastructure: lets a caller time the oracle on
+ * one core or on every core of its affinity mask). */
+void oracle_set_threads(int64_t n) { omp_set_num_threads(n > 0 ? (int)n : 1); }
+int64_t oracle_max_threads(void) { return (int64_t)omp_get_max_threads(); }

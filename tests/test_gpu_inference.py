@@ -284,6 +284,29 @@ def _sampled_rows(N, n, seed):
     return np.unique(np.concatenate([[0, 1, 2, 3, N - 1], rng.choice(N, n, replace=False)]))
 
 
+@pytest.mark.parametrize("T", [64, 128, 256])
+@pytest.mark.parametrize("p", [0.001, 0.05, 0.5])
+def test_sweep_shapes_end_to_end_sampled(cuda_dev, p, T):
+    """The density x tile-width sweep's shapes (d_model 2048, d_ff 5632, uniform density p) at
+    N = 1024, end to end (gate + pack, fused walk), on sampled rows."""
+    L = synthetic.sweep_point(p, T, N=1024)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=T)
+    rows = _sampled_rows(L.N, 12, seed=T)
+    y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
+    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"sweep p={p} T={T}")
+
+
+def test_sweep_point_full_size_sampled(cuda_dev):
+    """One sweep point at the bench's full size (N = 8192, p = 1%, T = 256), on sampled rows."""
+    L = synthetic.sweep_point(0.01, 256)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=256)
+    rows = _sampled_rows(L.N, 16, seed=5)
+    y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
+    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, "sweep p=1% T=256 full size")
+
+
 @pytest.mark.parametrize("which", ["1.5b", "2b"])
 def test_full_size_layers_sampled(cuda_dev, which):
     """The bench's workloads at full size, in the bench's launch configuration, on sampled rows."""
