@@ -19,7 +19,7 @@
 // a ticket counter (the caller's workspace, cleared on the launch stream), so per-token nonzero
 // counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
 //
-// ffn_mma_kernel (bf16, d_model 512, 1024, 2048 or 4096): nonzeros are taken in batches of
+// ffn_mma_kernel (bf16, d_model 512, 1024, 1280, 1536, 2048, 2560, 3072 or 4096): nonzeros are taken in batches of
 // up to 16 of one row. The 16 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
 // mma.sync m16n8k16 with the batch's weight rows as the 16 rows of A and x_r in every column of
 // B (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
@@ -27,7 +27,7 @@
 // rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's columns. Weight
 // rows move in 4 KB steps (32 bytes per lane per load, so four lanes cover a 128-byte line)
 // through a register ring, two or three steps ahead of use across batch and row boundaries.
-// For d_model = 4096 two warps share a row, each with half the columns and half the k range
+// Above 2048 columns two warps share a row, each with half the columns and half the k range
 // (the two partial dot products meet once per batch in shared memory). On the 2048-wide layer
 // one warp per row with a three-step ring measured faster (0.276 ms) than two warps per row
 // with three to five steps (0.31-0.47 ms): the kernel is bound by instruction issue, not by
@@ -161,9 +161,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Shared memory of one group of G warps: two ticket mailboxes, then the partial dot products
-// (2 x G floats for the general kernel, G <= 4; 2 x G x 16 for the tensor-core kernel, G <= 2).
-constexpr int kGroupBytes = 16 + 2 * 2 * 16 * 4;
+// Shared memory of one group of G warps: two ticket mailboxes, then the 2 x G partial dot
+// products of the general kernel (G <= 4).
+constexpr int kGroupBytes = 16 + 2 * 4 * 4;
 
 // ------------------------------------------------------------------------------------------
 // The row stream of one group of G warps: row tickets, TwELL metadata one segment ahead, x_r
@@ -527,10 +527,7 @@ __global__ void __launch_bounds__(kCtaThreads, (CPL >= 5 ? 2 : CPL == 4 ? 3 : 4)
 }
 
 // ------------------------------------------------------------------------------------------
-// Tensor-core kernel (bf16, d_model / G = 512 * CPL with CPL in {1, 2, 4}): a group of G warps
-// per row, each warp owning d_model / G columns for the down projection and the same share of
-// the k range of the dot products (256-column blocks wg, wg + G, ...: the blocks of x_r its
-// row stream stages).
+// Tensor-core kernel (bf16, d_model = 256 * CPLX <= 2048): one warp per token row.
 
 constexpr int kBatch = 16;  // nonzeros per batch: the m dimension of m16n8k16
 constexpr int kBatchSlots = 4;
@@ -542,9 +539,8 @@ struct __align__(16) BatchDesc {
     float h[kBatch];        // h = a * u, filled when the batch's dot products are done
 };
 
-template <int CPL>  // 32-byte chunks per lane of the warp's columns in the down projection
+template <int CPLX>  // 256-column blocks per warp (16-byte x chunks per lane)
 struct MmaSmem {
-    static constexpr int CPLX = 2 * CPL;  // 16-byte x chunks per lane
     __host__ __device__ static size_t x_bytes() { return static_cast<size_t>(kXBufs) * CPLX * 32 * 16; }
     __host__ __device__ static size_t warp_bytes(int nt)
     {
@@ -553,39 +549,37 @@ struct MmaSmem {
     __host__ __device__ static size_t cta_bytes(int nt) { return kCtaWarps * (warp_bytes(nt) + kGroupBytes); }
 };
 
-// CPL in {1, 2, 4}: a warp's columns are 512 * CPL; R: depth of the register ring of 4 KB steps.
-template <int CPL, int G, int R>
+// CPLX: 256-column blocks of d_model; R: depth of the register ring of 4 KB steps.
+template <int CPLX, int R>
 __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<__nv_bfloat16> a)
 {
+    constexpr int G = 1;
     using E = __nv_bfloat16;
-    constexpr int CPLX = MmaSmem<CPL>::CPLX;
-    constexpr int EPS = 4 / CPL;  // nonzeros per down-projection step
-    constexpr int nU = CPL * 4;   // up-projection steps per batch (128 columns of d_model each)
+    constexpr int CPL = (CPLX + 1) / 2;  // 32-byte chunks per lane of y_r in the down projection
+    constexpr int N32 = 16 * CPLX;       // 32-byte chunks of a row (lane l owns l, l + 32, ...)
+    constexpr int EPS = 4 / CPL;         // nonzeros per down-projection step
+    constexpr int nU = 2 * CPLX;         // up-projection steps per batch (128 columns of d_model each)
     constexpr int kU = 1, kD = 2, kEnd = 3;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int wg = warp % G, grp = warp / G;
     const int g = lane >> 2, t = lane & 3;
-    const size_t wbytes = MmaSmem<CPL>::warp_bytes(a.nt);
+    const size_t wbytes = MmaSmem<CPLX>::warp_bytes(a.nt);
     uint8_t* wsm = smem + warp * wbytes;
     uint4* s_x = reinterpret_cast<uint4*>(wsm);
-    int* s_pref = reinterpret_cast<int*>(wsm + MmaSmem<CPL>::x_bytes());
-    BatchDesc* s_bd = reinterpret_cast<BatchDesc*>(wsm + MmaSmem<CPL>::x_bytes() + pref_bytes(a.nt));
-    uint8_t* gsm = smem + kCtaWarps * wbytes + grp * kGroupBytes;
-    int* s_tk = reinterpret_cast<int*>(gsm);
-    float* s_part = reinterpret_cast<float*>(gsm + 16);  // [2][G][16]
+    int* s_pref = reinterpret_cast<int*>(wsm + MmaSmem<CPLX>::x_bytes());
+    BatchDesc* s_bd = reinterpret_cast<BatchDesc*>(wsm + MmaSmem<CPLX>::x_bytes() + pref_bytes(a.nt));
+    int* s_tk = reinterpret_cast<int*>(smem + kCtaWarps * wbytes + warp * kGroupBytes);  // unused with G = 1
 
     const uint64_t pol = policy_evict_last();
-    const int dh = a.d / G;  // this warp's columns of the down projection: [wg * dh, (wg + 1) * dh)
 
     RowStream<E, CPLX, G> rs;
-    rs.init(a, s_x, s_pref, s_tk, lane, wg, 1 + grp);
+    rs.init(a, s_x, s_pref, s_tk, lane, 0, 1 + warp);
 
     // -------------------------------------------------------------- issue side: 4 KB steps
-    // A batch of k <= 16 nonzeros is nU up-projection steps (step i covers columns
-    // 256 * ((i / 2) * G + wg) + 128 * (i % 2) + [0, 128): lane (g, t) loads 32 bytes of Wu_s[j_g] and
-    // of Wu_s[j_{g+8}] at offset 64c + 16t, c = 0, 1) followed by ceil(k / EPS) down-projection steps
-    // (lane loads its CPL 32-byte chunks of Wd_s[j_e] for EPS nonzeros).
+    // A batch of k <= 16 nonzeros is nU up-projection steps (step i covers columns 128i + [0, 128):
+    // lane (g, t) loads 32 bytes of Wu_s[j_g] and of Wu_s[j_{g+8}] at offset 64c + 16t, c = 0, 1)
+    // followed by ceil(k / EPS) down-projection steps (lane loads its CPL 32-byte chunks of
+    // Wd_s[j_e] for EPS nonzeros).
     // The tag of a step: kind | batch slot << 2 | step << 4.
     int is_slot = 0, is_step = 0, is_nsteps = 0, is_k = 0, nslot = 0;
     bool ended = false;
@@ -625,7 +619,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
         }
         const BatchDesc* D = &s_bd[is_slot];
         if (is_step < nU) {
-            const int col = 256 * ((is_step >> 1) * G + wg) + 128 * (is_step & 1) + 16 * t;
+            const int col = 128 * is_step + 16 * t;
             if (g < is_k) {
                 const E* w = a.Wu + static_cast<size_t>(D->j[g]) * a.d + col;
                 ldg_keep32(B[0], w, pol);
@@ -642,9 +636,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
 #pragma unroll
             for (int ee = 0; ee < EPS; ++ee) {
                 if (e0 + ee < is_k) {
-                    const E* w = a.Wd + static_cast<size_t>(D->j[e0 + ee]) * a.d + wg * dh + 16 * lane;
+                    const E* w = a.Wd + static_cast<size_t>(D->j[e0 + ee]) * a.d + 16 * lane;
 #pragma unroll
-                    for (int m = 0; m < CPL; ++m) ldg_keep32(B[ee * CPL + m], w + 512 * m, pol);
+                    for (int m = 0; m < CPL; ++m)
+                        if (lane + 32 * m < N32) ldg_keep32(B[ee * CPL + m], w + 512 * m, pol);
                 }
             }
             tag = kD;
@@ -662,7 +657,6 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     for (int m = 0; m < CPL; ++m)
 #pragma unroll
         for (int w = 0; w < 8; ++w) acc[m][w] = 0;
-    int par = 0;
     auto process = [&](const uint32_t (&B)[4][8], int tag) {
         BatchDesc* D = &s_bd[(tag >> 2) & (kBatchSlots - 1)];
         const int step = tag >> 4;
@@ -686,25 +680,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
                 mma_bf16(macc[3], Wg[6], Wg8[6], Wg[7], Wg8[7], X1.z, X1.w);
             }
             if (step == nU - 1) {
-                // lane (g, t) holds this warp's part of u for nonzeros g (D row g) and g+8 (row
-                // g+8), the same in every column; the G parts are added in warp order by every warp
-                float u0 = (macc[0][0] + macc[1][0]) + (macc[2][0] + macc[3][0]);
-                float u1 = (macc[0][2] + macc[1][2]) + (macc[2][2] + macc[3][2]);
-                if constexpr (G > 1) {
-                    float* sp = s_part + par * G * 16;
-                    if (t == 0) {
-                        sp[wg * 16 + g] = u0;
-                        sp[wg * 16 + g + 8] = u1;
-                    }
-                    bar_sync_named(1 + grp, 32 * G);
-                    u0 = u1 = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < G; ++w) {
-                        u0 += sp[w * 16 + g];
-                        u1 += sp[w * 16 + g + 8];
-                    }
-                    par ^= 1;
-                }
+                // lane (g, t) holds u of nonzeros g (D row g) and g+8 (row g+8), the same in every
+                // column of D
+                const float u0 = (macc[0][0] + macc[1][0]) + (macc[2][0] + macc[3][0]);
+                const float u1 = (macc[0][2] + macc[1][2]) + (macc[2][2] + macc[3][2]);
                 if (t == 0) {
                     D->h[g] = D->a[g] * u0;
                     D->h[g + 8] = D->a[g + 8] * u1;
@@ -720,12 +699,14 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
                     const uint64_t h2 = f2pack(h, h);
 #pragma unroll
                     for (int m = 0; m < CPL; ++m)
+                        if (lane + 32 * m < N32) {
 #pragma unroll
-                        for (int w = 0; w < 8; ++w) fma2(acc[m][w], h2, bf2_to_f2(B[ee * CPL + m][w]));
+                            for (int w = 0; w < 8; ++w) fma2(acc[m][w], h2, bf2_to_f2(B[ee * CPL + m][w]));
+                        }
                 }
             }
             if (e0 + EPS >= D->k && (D->flags & kLast)) {
-                E* yr = a.y + static_cast<size_t>(D->row) * a.d + wg * dh + 16 * lane;
+                E* yr = a.y + static_cast<size_t>(D->row) * a.d + 16 * lane;
 #pragma unroll
                 for (int m = 0; m < CPL; ++m) {
                     float lo8[8], hi8[8];
@@ -734,8 +715,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
                         f2unpack(acc[m][w], lo8[2 * w], lo8[2 * w + 1]);
                         f2unpack(acc[m][w + 4], hi8[2 * w], hi8[2 * w + 1]);
                     }
-                    st_stream16(yr + 512 * m, pack16(lo8, static_cast<E*>(nullptr)));
-                    st_stream16(yr + 512 * m + 8, pack16(hi8, static_cast<E*>(nullptr)));
+                    if (lane + 32 * m < N32) {
+                        st_stream16(yr + 512 * m, pack16(lo8, static_cast<E*>(nullptr)));
+                        st_stream16(yr + 512 * m + 8, pack16(hi8, static_cast<E*>(nullptr)));
+                    }
 #pragma unroll
                     for (int w = 0; w < 8; ++w) acc[m][w] = 0;
                 }
@@ -795,10 +778,10 @@ static twell_status launch_rows(const RowArgs<E>& a, cudaStream_t s)
     return launch_persistent(ffn_rows_kernel<E, CPL, G>, a, RowSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, s);
 }
 
-template <int CPL, int G, int R>
+template <int CPLX, int R>
 static twell_status launch_mma(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
 {
-    return launch_persistent(ffn_mma_kernel<CPL, G, R>, a, MmaSmem<CPL>::cta_bytes(a.nt), kCtaWarps / G, s);
+    return launch_persistent(ffn_mma_kernel<CPLX, R>, a, MmaSmem<CPLX>::cta_bytes(a.nt), kCtaWarps, s);
 }
 
 // Kernel and layout for d_model = nchunks 16-byte chunks: the tensor-core kernel where it applies,
@@ -808,10 +791,19 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
 {
     if constexpr (std::is_same<E, __nv_bfloat16>::value) {
         const bool a32 = (reinterpret_cast<uintptr_t>(a.Wu) % 32 == 0) && (reinterpret_cast<uintptr_t>(a.Wd) % 32 == 0);
-        if (a32 && a.d == 512) return launch_mma<1, 1, 4>(a, s);
-        if (a32 && a.d == 1024) return launch_mma<2, 1, 3>(a, s);
-        if (a32 && a.d == 2048) return launch_mma<4, 1, 3>(a, s);
-        if (a32 && a.d == 4096) return launch_mma<4, 2, 3>(a, s);
+        // one warp per row: a warp's registers hold at most 2048 columns of y_r. Wider rows go to
+        // the general kernel (two warps per row), which measured faster at 2560 columns (1.43 ms)
+        // than this kernel with two warps per row (1.51 ms) on the 2B-like layer
+        if (a32 && a.d % 256 == 0) {
+            switch (a.d / 256) {
+            case 2: return launch_mma<2, 4>(a, s);
+            case 4: return launch_mma<4, 3>(a, s);
+            case 5: return launch_mma<5, 3>(a, s);
+            case 6: return launch_mma<6, 3>(a, s);
+            case 8: return launch_mma<8, 3>(a, s);
+            default: break;
+            }
+        }
     }
     const int n = a.nchunks;
     if (n <= 32 * 2) return launch_rows<E, 2, 1>(a, s);

@@ -182,9 +182,10 @@ def test_fused_wide_model_two_chunks_per_thread(cuda_dev):
     assert_close(y, y_ref, "fused d=5120")
 
 
-@pytest.mark.parametrize("d,dt", [(64, torch.bfloat16), (512, torch.bfloat16), (1024, torch.bfloat16), (2048, torch.bfloat16),
-                                  (2560, torch.bfloat16), (4096, torch.bfloat16), (1024, torch.float32),
-                                  (2048, torch.float32)])
+@pytest.mark.parametrize("d,dt", [(64, torch.bfloat16), (512, torch.bfloat16), (1024, torch.bfloat16),
+                                  (1280, torch.bfloat16), (1536, torch.bfloat16), (2048, torch.bfloat16),
+                                  (2560, torch.bfloat16), (3072, torch.bfloat16), (4096, torch.bfloat16),
+                                  (1000, torch.bfloat16), (1024, torch.float32), (2048, torch.float32)])
 def test_fused_every_row_layout(cuda_dev, d, dt):
     """Every (chunks per lane, warps per row) layout the fused kernel dispatches to, with a ragged
     last tile (f = 1000) and more rows than resident warps."""
