@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED
 EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cnt_bytes", "twell_workspace_bytes",
            "twell_gate_pack", "twell_ffn_fused_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
-           "twell_gate_gemm", "twell_gemm_test",
+           "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info")
 
 
@@ -88,6 +88,8 @@ def load(path: str = LIB_PATH):
                                                       sz, vp]),
                 "twell_hybrid_route_noalloc": (st, [ctypes.POINTER(_Packed), i32, ctypes.POINTER(_Hybrid), vp]),
                 "twell_gate_gemm": (st, [vp, vp, i32, i32, i32, vp, vp, vp]),
+                "twell_column_activity": (st, [ctypes.POINTER(_Packed), vp, vp, vp]),
+                "twell_gather_rows": (st, [vp, i32, vp, i32, i32, ctypes.c_int, vp, vp, vp]),
                 "twell_gemm_test": (st, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
                 "twell_read_status": (st, [vp, vp]),
                 "twell_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -262,6 +264,43 @@ def twell_unpack(a: TwELL, out: Optional[torch.Tensor] = None, status=None, stre
                                _ptr(status if status is not None else status_buffer(out.device)), _stream(stream)),
            "twell_unpack")
     return out
+
+
+def twell_column_activity(a: TwELL, counts: Optional[torch.Tensor] = None, status=None, stream=None) -> torch.Tensor:
+    """Per-column count of the rows of `a` that keep the column (added to `counts`, zeros if None)."""
+    counts = counts if counts is not None else torch.zeros(a.n_cols, dtype=torch.int32, device=a.vals.device)
+    s = a.c_struct()
+    _check(load().twell_column_activity(ctypes.byref(s), _ptr(counts),
+                                        _ptr(status if status is not None else status_buffer(counts.device)),
+                                        _stream(stream)),
+           "twell_column_activity")
+    return counts
+
+
+def twell_gather_rows(src: torch.Tensor, rows: torch.Tensor, out: Optional[torch.Tensor] = None, status=None,
+                      stream=None) -> torch.Tensor:
+    """out[i] = src[rows[i]] (rows: int32 device tensor)."""
+    n_src, d = src.shape
+    n = rows.numel()
+    out = out if out is not None else torch.empty((n, d), dtype=src.dtype, device=src.device)
+    _check(load().twell_gather_rows(_ptr(src), n_src, _ptr(rows), n, d, _dtype_code(src.dtype), _ptr(out),
+                                    _ptr(status if status is not None else status_buffer(src.device)),
+                                    _stream(stream)),
+           "twell_gather_rows")
+    return out
+
+
+def live_columns(counts: torch.Tensor) -> torch.Tensor:
+    """Ascending int32 indices (on the counts' device) of the columns that fired at least once;
+    computed on the host, once per model."""
+    import numpy as np
+    live = np.flatnonzero(counts.cpu().numpy() > 0).astype(np.int32)
+    return torch.from_numpy(live).to(counts.device)
+
+
+def compact_weights(Wg_s, Wu_s, Wd_s, live: torch.Tensor, status=None, stream=None):
+    """The rows of Wg_s, Wu_s, Wd_s of the live hidden units, in the order of `live`."""
+    return tuple(twell_gather_rows(W, live, status=status, stream=stream) for W in (Wg_s, Wu_s, Wd_s))
 
 
 def twell_pack_from_gate(G: torch.Tensor, T: int = 128, out: Optional[TwELL] = None, status=None,

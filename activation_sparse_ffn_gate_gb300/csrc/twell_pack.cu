@@ -1,4 +1,5 @@
-// twell_pack.cu -- TwELL pack of a given gate matrix and TwELL unpack (test exports).
+// twell_pack.cu -- TwELL pack of a given gate matrix and TwELL unpack (test exports); per-column
+// activity counts of a TwELL matrix and a row gather, the two steps of dead-column compaction.
 //
 // One warp per (token row, column tile): the lanes test 32 columns at a time, a warp ballot marks
 // the kept entries (g > 0) and each kept lane finds its slot as the population count of the
@@ -63,6 +64,48 @@ __global__ void unpack_kernel(const E* __restrict__ vals, const uint8_t* __restr
         const int j = t * T + idx[slot + k];
         if (j < f) out[j] = vals[slot + k];
         else report(status, TWELL_ERR_DEVICE_CHECK);
+    }
+}
+
+// One warp per (token row, column tile): each kept entry adds one to its column's count. A count
+// above the tile width or a column at or beyond n_cols is recorded and skipped.
+__global__ void column_activity_kernel(const uint8_t* __restrict__ idx, const uint16_t* __restrict__ cnt, int N,
+                                       int f, int T, int nt, int32_t* __restrict__ col_counts, int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= static_cast<long long>(N) * nt) return;
+    const int t = static_cast<int>(w % nt);
+    const int c = cnt[w];
+    if (c > T) {
+        if (lane == 0) report(status, TWELL_ERR_DEVICE_CHECK);
+        return;
+    }
+    for (int q = lane; q < c; q += 32) {
+        const int k = idx[w * T + q];
+        const int j = t * T + k;
+        if (k >= T || j >= f) {
+            report(status, TWELL_ERR_DEVICE_CHECK);
+            continue;
+        }
+        atomicAdd(&col_counts[j], 1);
+    }
+}
+
+// dst[i, :] = src[rows[i], :] in 16-byte chunks; a row index outside [0, n_src) is recorded and
+// its output row is zero.
+__global__ void gather_rows_checked_kernel(const uint4* __restrict__ src, int n_src, const int32_t* __restrict__ rows,
+                                           int n, int chunks, uint4* __restrict__ dst, int32_t* status)
+{
+    const long long total = static_cast<long long>(n) * chunks;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(e / chunks), q = static_cast<int>(e % chunks);
+        const int r = rows[i];
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r >= 0 && r < n_src) v = src[static_cast<size_t>(r) * chunks + q];
+        else if (q == 0) report(status, TWELL_ERR_DEVICE_CHECK);
+        dst[e] = v;
     }
 }
 
@@ -134,5 +177,44 @@ extern "C" twell_status twell_unpack(const twell_packed* a, void* dense_out, int
         twell::unpack_kernel<float><<<warp_blocks(warps, 8), 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx,
                                                                           a->cnt, N, f, T, nt,
                                                                           static_cast<float*>(dense_out), dev_status);
+    return launch_status();
+}
+
+extern "C" twell_status twell_column_activity(const twell_packed* a, int32_t* col_counts, int32_t* dev_status,
+                                              void* stream)
+{
+    if (a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (!dtype_ok(a->dtype)) return TWELL_ERR_UNSUPPORTED;
+    const int N = a->n_rows, f = a->n_cols, T = a->tile;
+    if (N < 0 || f <= 0 || col_counts == nullptr) return TWELL_ERR_INVALID;
+    twell_status st = check_packed(a, N, f, T, a->dtype);
+    if (st != TWELL_OK) return st;
+    if (N == 0) return TWELL_OK;
+    const int nt = (f + T - 1) / T;
+    const long long warps = static_cast<long long>(N) * nt;
+    if (warps / 8 + 1 > 0x7fffffffLL) return TWELL_ERR_UNSUPPORTED;
+    twell::column_activity_kernel<<<warp_blocks(warps, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        a->idx, a->cnt, N, f, T, nt, col_counts, dev_status);
+    return launch_status();
+}
+
+extern "C" twell_status twell_gather_rows(const void* src, int32_t n_src, const int32_t* rows, int32_t n, int32_t d,
+                                          twell_dtype dtype, void* dst, int32_t* dev_status, void* stream)
+{
+    if (dev_status == nullptr || n_src < 0 || n < 0 || d <= 0) return TWELL_ERR_INVALID;
+    if (!dtype_ok(dtype)) return TWELL_ERR_UNSUPPORTED;
+    const int esz = dtype == TWELL_BF16 ? 2 : 4;
+    if ((static_cast<long long>(d) * esz) % 16 != 0) return TWELL_ERR_INVALID;
+    if (n == 0) return TWELL_OK;
+    if (src == nullptr || rows == nullptr || dst == nullptr) return TWELL_ERR_INVALID;
+    if (!aligned16(src) || !aligned16(dst)) return TWELL_ERR_INVALID;
+    const int chunks = static_cast<int>(static_cast<long long>(d) * esz / 16);
+    DevInfo di;
+    if (dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    const long long total = static_cast<long long>(n) * chunks;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 8LL * di.sm_count) blocks = 8LL * di.sm_count;
+    twell::gather_rows_checked_kernel<<<static_cast<int>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(src), n_src, rows, n, chunks, static_cast<uint4*>(dst), dev_status);
     return launch_status();
 }

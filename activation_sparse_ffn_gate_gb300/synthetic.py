@@ -153,6 +153,15 @@ def per_token_layer(N, d, f, T, seed, base=0.005, normalise=True, seq_len=1024, 
                  target_density=float(p.mean()), recipe=recipe)
 
 
+def calibration_tokens(L: Layer, N: int, seed: int) -> np.ndarray:
+    """Another batch of tokens for layer L, drawn like L's own x (x[:,0] = 1, x[:,1:] ~ N(0,1),
+    rounded to L's dtype); for layers whose bias feature is x[:,0] = 1 (uniform_layer)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((N, L.d), dtype=np.float32)
+    x[:, 0] = 1.0
+    return _finish(x, L.dtype == "bf16")
+
+
 # --------------------------------------------------------------------------- presets
 
 SWEEP_DENSITIES = (0.001, 0.005, 0.01, 0.02, 0.05, 0.10, 0.50)

@@ -198,6 +198,30 @@ TWELL_API twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const v
                               float* dWd_s, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Dead-column compaction. The pages report that more than 30% of the gate's hidden units never
+ * fire once training has settled ([PUL] ¶5). A unit that never fires adds nothing to y, so the
+ * layer can run on the live units alone: count, per column, how often a calibration batch's TwELL
+ * matrix keeps it (twell_column_activity), gather the rows of Wg_s, Wu_s and Wd_s of the columns
+ * that fired (twell_gather_rows), and call twell_gate_pack / twell_ffn_fused_fwd with d_ff = the
+ * number of live units. With the live columns kept in ascending order the compacted layer gives
+ * the same y, bit for bit, on any batch whose active units are among them. The pages state the
+ * observation, not this procedure.
+ */
+
+/* col_counts[j] += the number of rows of `a` that keep column j (device int32 [a->n_cols]; the
+ * call adds to what is there, the caller clears it). A bad entry (count above the tile width,
+ * in-tile index >= tile, column >= n_cols) is reported as TWELL_ERR_DEVICE_CHECK in *dev_status
+ * and skipped. */
+TWELL_API twell_status twell_column_activity(const twell_packed* a, int32_t* col_counts, int32_t* dev_status,
+                                   void* stream);
+
+/* dst[i, :] = src[rows[i], :] for i < n (device; src [n_src, d], dst [n, d] row-major, element
+ * type dtype, d * element size a multiple of 16 bytes, both 16-byte aligned; rows int32 [n]). A
+ * row index outside [0, n_src) is reported as TWELL_ERR_DEVICE_CHECK and its output row is 0. */
+TWELL_API twell_status twell_gather_rows(const void* src, int32_t n_src, const int32_t* rows, int32_t n,
+                               int32_t d, twell_dtype dtype, void* dst, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Test exports. They run the same device code as the calls above on a gate matrix the caller
  * provides, so packing and routing can be compared bit for bit with an independent reference.
  */

@@ -102,6 +102,21 @@ def test_fused_rejects_bad_arguments(lib):
     assert call(dt=5) == 2
 
 
+def test_compaction_calls_reject_bad_arguments(lib):
+    p = _packed()
+    assert lib.twell_column_activity(ctypes.byref(p), None, STATUS, None) == 1
+    assert lib.twell_column_activity(ctypes.byref(p), ALIGNED, None, None) == 1
+    bad = _packed()
+    bad.cap = 64
+    assert lib.twell_column_activity(ctypes.byref(bad), ALIGNED, STATUS, None) == 1
+    rows = ALIGNED
+    assert lib.twell_gather_rows(ALIGNED, 10, rows, 4, 4, 0, ALIGNED, STATUS, None) == 1  # 8-byte rows
+    assert lib.twell_gather_rows(ALIGNED, 10, rows, 4, 8, 0, ctypes.c_void_p((1 << 20) + 8), STATUS, None) == 1
+    assert lib.twell_gather_rows(None, 10, rows, 4, 8, 0, ALIGNED, STATUS, None) == 1
+    assert lib.twell_gather_rows(ALIGNED, 10, rows, 4, 8, 7, ALIGNED, STATUS, None) == 2
+    assert lib.twell_gather_rows(None, 10, None, 0, 8, 0, None, STATUS, None) == 0  # nothing to gather
+
+
 def test_pack_unpack_reject_bad_arguments(lib):
     p = _packed()
     assert lib.twell_pack_from_gate(None, 4, 256, 128, 0, ctypes.byref(p), STATUS, None) == 1

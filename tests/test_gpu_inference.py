@@ -253,6 +253,56 @@ def test_fused_empty_batch(cuda_dev):
     assert y.shape == (0, 256)
 
 
+# ------------------------------------------------------------------------------------------ dead-column compaction
+
+def test_column_activity_matches_oracle_counts(cuda_dev):
+    """Per-column keep counts of a device TwELL equal the oracle's count of g > 0, exactly."""
+    L = synthetic.uniform_layer(700, 512, 1000, 128, 0.03, seed=21, dead_frac=0.3)
+    t = L.torch_inputs(cuda_dev)
+    tw = binding.twell_gate_pack(t["x"], t["Wg_s"], L.T)
+    counts = binding.twell_column_activity(tw)
+    dense = binding.twell_unpack(tw).double().cpu().numpy()
+    np.testing.assert_array_equal(counts.cpu().numpy(), (dense > 0).sum(0))
+    G = oracle.gate(L.x, L.Wg_s)
+    assert (counts.cpu().numpy() == 0).sum() >= 300  # the dead columns never fire
+    big = np.abs(G) > 1e-2  # away from the accumulation-order threshold both agree
+    np.testing.assert_array_equal(((G > 0) & big).sum(0) <= counts.cpu().numpy(), True)
+    np.testing.assert_array_equal(counts.cpu().numpy() <= ((G > 0) | ~big).sum(0), True)
+    twice = binding.twell_column_activity(tw, counts=counts.clone())
+    np.testing.assert_array_equal(twice.cpu().numpy(), 2 * counts.cpu().numpy())
+
+
+def test_gather_rows_copies_and_checks(cuda_dev):
+    src = torch.randn(50, 64, device=cuda_dev).to(torch.bfloat16)
+    rows = torch.tensor([3, 0, 49, 7, 7], dtype=torch.int32, device=cuda_dev)
+    out = binding.twell_gather_rows(src, rows)
+    assert torch.equal(out, src[rows.long()])
+    bad = torch.tensor([1, 50, 2], dtype=torch.int32, device=cuda_dev)
+    out = binding.twell_gather_rows(src, bad)
+    assert binding.twell_read_status(reset=True) == 5  # TWELL_ERR_DEVICE_CHECK
+    assert torch.equal(out[0], src[1]) and torch.equal(out[2], src[2])
+    assert torch.count_nonzero(out[1]).item() == 0
+
+
+def test_compacted_layer_gives_the_same_y(cuda_dev):
+    """Live columns from a calibration batch, weights gathered to them: y is bit-identical to the
+    uncompacted layer on a different batch (1.5B-like shapes, 30% dead columns, N = 1024)."""
+    L = synthetic.layer_1p5b(N=1024)
+    t = L.torch_inputs(cuda_dev)
+    x_cal = torch.from_numpy(synthetic.calibration_tokens(L, 2048, seed=77)).to(cuda_dev, torch.bfloat16)
+    counts = binding.twell_column_activity(binding.twell_gate_pack(x_cal, t["Wg_s"], L.T))
+    live = binding.live_columns(counts)
+    assert 0.68 * L.f <= live.numel() <= 0.72 * L.f
+    Wg_c, Wu_c, Wd_c = binding.compact_weights(t["Wg_s"], t["Wu_s"], t["Wd_s"], live)
+    tw = binding.twell_gate_pack(t["x"], t["Wg_s"], L.T)
+    y = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    # the batch's active units are among the calibration's live ones
+    active = binding.twell_column_activity(tw).cpu().numpy() > 0
+    assert not (active & (counts.cpu().numpy() == 0)).any()
+    y_c = binding.ffn_forward(t["x"], Wg_c, Wu_c, Wd_c, T=L.T)
+    assert torch.equal(y_c, y)
+
+
 # ------------------------------------------------------------------------------------------ end to end
 
 def test_end_to_end_tiny_fp32(cuda_dev):
