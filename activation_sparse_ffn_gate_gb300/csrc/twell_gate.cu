@@ -86,7 +86,7 @@ extern "C" twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t
     g.status = dev_status;
     GemmOperand A{x, N, d, d};
     GemmOperand B{Wg_s, f, d, d};
-    return launch_gemm<256, false, false, twell::Epi::PackTwell>(A, B, nullptr, g, s);
+    return launch_gemm<256, false, false, twell::Epi::PackTwell, true>(A, B, nullptr, g, s);
 }
 
 extern "C" twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t N, int32_t d, int32_t f,
@@ -105,5 +105,5 @@ extern "C" twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t
     g.status = dev_status;
     GemmOperand A{x, N, d, d};
     GemmOperand B{Wg_s, f, d, d};
-    return launch_gemm<256, false, false, twell::Epi::StoreF32>(A, B, nullptr, g, static_cast<cudaStream_t>(stream));
+    return launch_gemm<256, false, false, twell::Epi::StoreF32, true>(A, B, nullptr, g, static_cast<cudaStream_t>(stream));
 }

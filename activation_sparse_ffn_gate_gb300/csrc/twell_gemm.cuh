@@ -14,6 +14,19 @@
 // M and K may be read from device memory (rows of a device-side list, e.g. the hybrid backup
 // rows), so a launch sized for an upper bound does only the work that exists.
 //
+// PAIR (A and B K-major): CTAs run in clusters of two on an SM pair, and one tcgen05.mma of
+// cta_group::2 computes a 256 x BN tile. CTA r holds rows [128r, 128r + 128) of the A tile and
+// rows [r BN/2, (r + 1) BN/2) of the B tile, both at the same shared-memory offsets, and its
+// TMEM receives rows [128r, 128r + 128) of D. Per SM this halves the B bytes that TMA writes and
+// that the tensor core reads from shared memory (the 1-SM 128 x 256 tile needs 96 B/clk of
+// each, above what one SM's shared memory serves at the full MMA rate).
+//   * Both CTAs' TMA loads complete on the even CTA's full[s] (expect_tx of both halves, armed
+//     by the even CTA's producer); only the even CTA's MMA thread issues MMAs and commits.
+//   * Its commits free stage s on both CTAs' empty[s] and signal both CTAs' tfull[a]; the
+//     epilogue warps of both CTAs release an accumulator on the even CTA's tempty[a] (count 8).
+//   * A cluster barrier after TMEM allocation and before deallocation keeps each CTA's
+//     barriers, shared memory and TMEM alive while the other may still signal or write them.
+//
 // Every mbarrier wait is bounded (twell::wait_bounded). On a timeout the CTA raises its abort
 // flag, every role leaves its loop, the producer waits (bounded) for the TMA copies it issued,
 // the MMA thread waits (bounded) for its last tcgen05 operations, and TMEM is freed before exit.
@@ -56,24 +69,26 @@ constexpr int kGemmThreads = 192;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = (BN == 256 && !PAIR) ? 4 : 6;
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
-    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;  // this CTA's share of B
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 };
 
-template <int BN, bool A_MN, bool B_MN, Epi EPI>
+template <int BN, bool A_MN, bool B_MN, Epi EPI, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs g)
 {
-    using C = GemmCfg<BN>;
+    static_assert(!PAIR || (!A_MN && !B_MN && BN == 256), "the CTA-pair tile is 256 x 256 with K-major operands");
+    using C = GemmCfg<BN, PAIR>;
+    constexpr int CG = PAIR ? 2 : 1;
     constexpr int STAGES = C::STAGES;
-    constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = idesc_bf16_f32(CG * kBM, BN, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,7 +112,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tiles = M > 0 ? (M + kBM - 1) / kBM : 0;
     const int n_tiles = (g.N + BN - 1) / BN;
     const int kbs = K > 0 ? (K + kBK - 1) / kBK : 0;
-    const int tiles = kbs > 0 ? m_tiles * n_tiles : 0;
+    // work units: one 128 x BN tile per CTA, or with PAIR one 256 x BN tile per cluster, of which
+    // this CTA holds the 128 rows of its rank (past M its loads read zeros and its epilogue
+    // writes nothing)
+    const int crank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+    const bool leader = crank == 0;
+    const int unit0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int ustride = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+    const int units = kbs > 0 ? (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles : 0;
+    auto tile_m0 = [&](int u) { return (PAIR ? 2 * (u / n_tiles) + crank : u / n_tiles) * kBM; };
+    auto tile_n0 = [&](int u) { return (u % n_tiles) * BN; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -106,7 +130,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], 4 * CG);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -118,13 +142,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (g.kb_split < kbs) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and TMEM exist before either is used
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the even CTA's barriers, as shared::cluster addresses (PAIR)
+    const uint32_t full_lead = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
+    const uint32_t tempty_lead = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -132,31 +160,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-                const int m0 = (t / n_tiles) * kBM;
-                const int n0 = (t % n_tiles) * BN;
+            for (int t = unit0; ok && t < units; t += ustride) {
+                const int m0 = tile_m0(t);
+                const int n0 = tile_n0(t);
                 for (int kb = 0; kb < kbs; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     uint8_t* a = sA + stage * C::A_BYTES;
                     uint8_t* b = sB + stage * C::B_BYTES;
                     const int k0 = kb * kBK;
-                    if constexpr (!A_MN) {
-                        tma_load_2d(a, &tmA, k0, m0, &full[stage]);
+                    if constexpr (PAIR) {
+                        // this CTA's halves of A and B; both CTAs' copies complete on the even CTA's full[s]
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                        const uint32_t fb = full_lead + stage * 8u;
+                        tma_load_2d_pair(a, &tmA, k0, m0, fb);
+                        tma_load_2d_pair(b, &tmB, k0, n0 + crank * (BN / 2), fb);
                     } else {
-                        tma_load_2d(a, &tmA, m0, k0, &full[stage]);
-                        tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[stage]);
-                    }
-                    const CUtensorMap* tb = ((kb / g.kb_split) & 1) ? &tmB2 : &tmB;
-                    const int kk = (kb % g.kb_split) * kBK;
-                    if constexpr (!B_MN) {
-                        tma_load_2d(b, tb, kk, n0, &full[stage]);
-                    } else {
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        if constexpr (!A_MN) {
+                            tma_load_2d(a, &tmA, k0, m0, &full[stage]);
+                        } else {
+                            tma_load_2d(a, &tmA, m0, k0, &full[stage]);
+                            tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[stage]);
+                        }
+                        const CUtensorMap* tb = ((kb / g.kb_split) & 1) ? &tmB2 : &tmB;
+                        const int kk = (kb % g.kb_split) * kBK;
+                        if constexpr (!B_MN) {
+                            tma_load_2d(b, tb, kk, n0, &full[stage]);
+                        } else {
 #pragma unroll
-                        for (int s = 0; s < BN / 64; ++s) tma_load_2d(b + s * 8192, tb, n0 + 64 * s, kk, &full[stage]);
+                            for (int s = 0; s < BN / 64; ++s)
+                                tma_load_2d(b + s * 8192, tb, n0 + 64 * s, kk, &full[stage]);
+                        }
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -167,18 +204,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
             // Wait (bounded, even after an abort) for every copy this thread issued to land, so
-            // no TMA write into shared memory is still in flight when the CTA exits.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s))
-                    wait_bounded(&full[s], (issued_phase >> s) & 1u, nullptr, g.status, g.wait_limit_ns);
+            // no TMA write into shared memory is still in flight when the CTA exits. With PAIR the
+            // even CTA's full barriers count both CTAs' copies, and the cluster barrier at the end
+            // holds the odd CTA until they have landed.
+            if (leader)
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        wait_bounded(&full[s], (issued_phase >> s) & 1u, nullptr, g.status, g.wait_limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-                if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) break;
+            for (int t = unit0; ok && t < units; t += ustride) {
+                if (!wait_bounded<PAIR>(&tempty[acc], acc_phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < kbs; ++kb) {
@@ -194,35 +234,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // one MMA consumes K = 16: 32 bytes along a K-major row, 16 rows of an MN-major tile
                         const uint64_t da = A_MN ? desc_sw128(a_addr + k * 2048, 8192) : desc_sw128(a_addr + k * 32, 16);
                         const uint64_t db = B_MN ? desc_sw128(b_addr + k * 2048, 8192) : desc_sw128(b_addr + k * 32, 16);
-                        tc_mma_f16(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
-                    tc_commit(&empty[stage]);  // frees this stage once its MMAs have read it
+                    // frees this stage (in both CTAs with PAIR) once its MMAs have read it
+                    if constexpr (PAIR) tc_commit_mc<CG>(&empty[stage], 0x3);
+                    else tc_commit<CG>(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&tfull[acc]);  // accumulator complete
+                // accumulator complete
+                if constexpr (PAIR) tc_commit_mc<CG>(&tfull[acc], 0x3);
+                else tc_commit<CG>(&tfull[acc]);
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
             // Wait (bounded) for every tcgen05 operation this thread issued before TMEM is freed.
-            tc_commit(drain);
+            tc_commit<CG>(drain);
             wait_bounded(drain, 0, nullptr, g.status, g.wait_limit_ns);
         }
     } else {
         // ------------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        for (int t = unit0; t < units; t += ustride) {
             int ok = 1;
             if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, g.status, g.wait_limit_ns) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int m0 = (t / n_tiles) * kBM;
-            const int n0 = (t % n_tiles) * BN;
+            const int m0 = tile_m0(t);
+            const int n0 = tile_n0(t);
             const int row = m0 + 32 * q + lane;
             const bool row_ok = row < M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
@@ -307,7 +351,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(tempty_lead + acc * 8u);
+                else mbar_arrive(&tempty[acc]);
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -316,8 +363,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the pair's last copies, MMAs and arrivals have landed
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
 }
 
 }  // namespace twell
@@ -333,7 +381,7 @@ struct GemmOperand {
 // Launch C = A * B with the tcgen05 kernel. A: [M, K] (a_mn = false) or [K, M] (a_mn = true);
 // B: [N, K] (b_mn = false) or [K, N] (b_mn = true); B2 (optional) continues B along K from
 // k-block kb_split on. Returns TWELL_ERR_CUDA on a tensor-map or launch failure.
-template <int BN, bool A_MN, bool B_MN, twell::Epi EPI>
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR = false>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
                          cudaStream_t stream);
 
@@ -341,11 +389,13 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
 
 namespace twell_host {
 
-template <int BN, bool A_MN, bool B_MN, twell::Epi EPI>
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
                          cudaStream_t stream)
 {
-    using Cfg = twell::GemmCfg<BN>;
+    static_assert(!PAIR || (!A_MN && !B_MN), "the CTA-pair GEMM takes K-major operands");
+    using Cfg = twell::GemmCfg<BN, PAIR>;
+    if (PAIR && B2 != nullptr) return TWELL_ERR_UNSUPPORTED;
     DevInfo di;
     if (dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
     if (di.max_smem_optin < Cfg::SMEM_BYTES) return TWELL_ERR_UNSUPPORTED;
@@ -356,9 +406,10 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
     st = A_MN ? make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, 64)
               : make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, twell::kBM);
     if (st != TWELL_OK) return st;
-    // B: K-major box = 64 (K) x BN (N); MN-major box = 64 (N) x 64 (K), BN/64 per stage.
+    // B: K-major box = 64 (K) x BN (N), or BN/2 rows per CTA with PAIR; MN-major box = 64 (N) x
+    // 64 (K), BN/64 per stage.
     st = B_MN ? make_tmap_bf16(&tb, B.ptr, B.cols, B.rows, B.ld, 64, 64)
-              : make_tmap_bf16(&tb, B.ptr, B.cols, B.rows, B.ld, 64, BN);
+              : make_tmap_bf16(&tb, B.ptr, B.cols, B.rows, B.ld, 64, PAIR ? BN / 2 : BN);
     if (st != TWELL_OK) return st;
     if (B2 != nullptr) {
         st = B_MN ? make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, 64)
@@ -368,15 +419,38 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         tb2 = tb;
         g.kb_split = 1 << 30;
     }
-    auto kern = twell::tc_gemm_kernel<BN, A_MN, B_MN, EPI>;
+    auto kern = twell::tc_gemm_kernel<BN, A_MN, B_MN, EPI, PAIR>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM_BYTES)) !=
         cudaSuccess)
         return TWELL_ERR_CUDA;
-    const long long tiles = static_cast<long long>((g.M + twell::kBM - 1) / twell::kBM) * ((g.N + BN - 1) / BN);
-    const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
     g.wait_limit_ns = wait_limit_ns();
-    kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
-    return launch_status();
+    const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + BN - 1) / BN;
+    if constexpr (!PAIR) {
+        const long long tiles = m_tiles * n_tiles;
+        const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
+        kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
+        return launch_status();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(twell::kGemmThreads);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(di.sm_count / 2));
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return TWELL_ERR_CUDA;
+        const long long units = ((m_tiles + 1) / 2) * n_tiles;
+        if (clusters > units) clusters = static_cast<int>(units);
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(clusters));
+        if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g) != cudaSuccess) return TWELL_ERR_CUDA;
+        return launch_status();
+    }
 }
 
 }  // namespace twell_host
