@@ -6,38 +6,36 @@
 // ([AIM] ¶3; [TG] "Инференс"; [PUL] ¶3; [TC] §2).
 //
 // GB300 layout. The work is a gather of 2 * d_model * sizeof(E) bytes per nonzero out of weight
-// rows that stay resident in the 129 MB L2, plus ~2 * d_model multiply-adds per nonzero. Plain
-// loads into registers reach 10-20 TB/s on random 4 KB rows (whole-row cp.async.bulk copies
-// stayed near 2.8 TB/s on the same pattern), so weight rows go straight into registers; what is
-// left to engineer is keeping enough bytes in flight per SM while spending few instructions.
+// rows that stay resident in the 129 MB L2, plus ~2 * d_model multiply-adds per nonzero. What
+// there is to engineer is keeping enough bytes in flight per SM while spending few instructions
+// per nonzero. Three kernels share the row stream (RowStream below): one token row is owned by a
+// group of G warps; the TwELL metadata runs one 32-nonzero segment ahead: counts of the next row
+// are loaded a row ahead, scanned into per-tile offsets in shared memory, and one lane per nonzero
+// finds its tile by binary search and loads its index and value into registers. With G = 1 warps
+// take rows from a ticket counter (the caller's workspace, cleared on the launch stream), so
+// per-token nonzero counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
 //
-// Both kernels share the row stream (RowStream below): one token row is owned by a group of G
-// warps; x_r is staged in shared memory by cp.async one segment ahead (three buffers per warp);
-// the TwELL metadata runs one 32-nonzero segment ahead: counts of the next row are loaded a row
-// ahead, scanned into per-tile offsets in shared memory, and one lane per nonzero finds its tile
-// by binary search and loads its index and value into registers. With G = 1 warps take rows from
-// a ticket counter (the caller's workspace, cleared on the launch stream), so per-token nonzero
-// counts do not unbalance the SMs; groups of G > 1 warps take rows round-robin.
+// ffn_bulk_kernel (bf16, d_model 512 .. 2048 in steps of 256, 2560 and 3072): lane 0
+// of each warp copies whole weight rows into a shared-memory ring with 1-D bulk copies (see the
+// kernel); both projections run on the tensor cores (mma.sync) from ldmatrix fragments. Measured
+// on the 2048-wide layer: 0.189-0.209 ms, against 0.276 ms for ffn_mma_kernel.
 //
-// ffn_mma_kernel (bf16, d_model 512, 1024, 1280, 1536, 2048, 2560, 3072 or 4096): nonzeros are taken in batches of
-// up to 16 of one row. The 16 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
+// ffn_mma_kernel (bf16, d_model 512, 1024, 1280, 1536 or 2048, where the bulk kernel's ring does
+// not fit in shared memory, i.e. very many column tiles): nonzeros are taken in batches of up to
+// 16 of one row. The 16 dot products x_r . Wu_s[j] of a batch run on the tensor cores as
 // mma.sync m16n8k16 with the batch's weight rows as the 16 rows of A and x_r in every column of
 // B (the products need no bf16 -> fp32 conversion; the k order inside a 16-wide block is
 // permuted the same way on both sides, so that each lane reads 32 contiguous bytes). The
 // rank-1 updates y_r += h * Wd_s[j] run as packed fp32 FMAs on each lane's columns. Weight
 // rows move in 4 KB steps (32 bytes per lane per load, so four lanes cover a 128-byte line)
 // through a register ring, two or three steps ahead of use across batch and row boundaries.
-// Above 2048 columns two warps share a row, each with half the columns and half the k range
-// (the two partial dot products meet once per batch in shared memory). On the 2048-wide layer
-// one warp per row with a three-step ring measured faster (0.276 ms) than two warps per row
-// with three to five steps (0.31-0.47 ms): the kernel is bound by instruction issue, not by
-// bytes in flight.
 //
 // ffn_rows_kernel (every other shape, fp32): one nonzero at a time, the dot product as a warp
 // reduction (plus a named-barrier exchange between the G warps of a row), weight rows of the
 // next nonzero loaded while the current one is used.
 //
-// Neither kernel has a spin-wait. The TwELL is checked on the way in (a count above the tile
+// The bulk kernel's mbarrier waits are bounded (TWELL_ERR_TIMEOUT); the other kernels have no
+// spin-wait. The TwELL is checked on the way in (a count above the tile
 // width, an in-tile index at or beyond T, a column at or beyond d_ff): a bad entry is recorded
 // in the status word as TWELL_ERR_DEVICE_CHECK and contributes nothing, and every access stays
 // inside the TwELL's own arrays.
@@ -65,6 +63,7 @@ struct RowArgs {
     int* tickets;  // G == 1: row counter, zero at launch
     int32_t* status;
     int N, d, f, T, nt, nchunks, vals_bf16;
+    uint64_t wait_ns;  // bound of every mbarrier wait (ffn_bulk_kernel)
 };
 
 __host__ __device__ inline size_t pref_bytes(int nt) { return (static_cast<size_t>(nt + 1) * 4 + 15) & ~size_t(15); }
@@ -750,6 +749,203 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
     cp_async_wait<0>();
 }
 
+
+// ------------------------------------------------------------------------------------------
+// Bulk-copy tensor-core kernel (bf16, d_model = 256 * NS): one warp per token row.
+//
+// Staging. Lane 0 of every warp copies, per nonzero, the whole rows Wu_s[j] and Wd_s[j] (and x_r
+// at the row's first nonzero) into one slot of the warp's S-slot ring in shared memory with 1-D
+// bulk copies (cp.async.bulk) that complete on the slot's mbarrier, S - 1 nonzeros ahead of use
+// and across row boundaries. Many warps issuing such copies reach ~20 TB/s of random 4 KB rows out
+// of L2, and the bytes in flight cost no registers.
+//
+// Both projections run as mma.sync m16n8k16 on operands read with ldmatrix.trans. Chunk c is
+// columns [128c, 128c + 128) of d_model, with X[k][m] = x_r[128c + 8k + m] and
+// W[k][n] = row[128c + 8k + n] (k < 16; m, n < 8):
+//   up:   A = X^T in rows 0..7 (rows 8..15 zero), B = Wu_s[j] chunk, so D[m][m] = sum_k X[k][m] W[k][m]
+//         and the trace of D summed over the chunks is u = x_r . Wu_s[j]; the diagonal sits in the
+//         eight lanes (g, t) with g >> 1 = t, which sum it in three xor steps (4, 9, 18) that stay
+//         among them;
+//   down: A = h * I (only those eight lanes hold its diagonal), B = Wd_s[j] chunk, so D += h * W:
+//         the 16 x 8 accumulator of chunk c holds y_r[128c + 8m + n] in fp32, in pairs of adjacent
+//         columns per lane, and y_r is stored straight from it. h is fp32 and the operands bf16, so
+//         h goes in as two MMAs, with hi = bf16(h) and lo = bf16(h - hi) (h to ~16 bits).
+template <int NS>
+struct BulkLayout {
+    static constexpr uint32_t kRow = 512u * NS;  // bytes of one bf16 row of d_model
+    static constexpr uint32_t kSlot = 3 * kRow;   // Wu_s[j], Wd_s[j], x_r (row starts only)
+    __host__ __device__ static size_t warp_bytes(int S, int nt)
+    {
+        return (static_cast<size_t>(S) * (kSlot + 16 + 8) + pref_bytes(nt) + 127) & ~size_t(127);
+    }
+};
+struct __align__(16) SlotDesc {
+    int row, flags;
+    float a;
+    int pad;
+};
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// D = A * B (no accumulator input) for one m16n8k16 tile, bf16 inputs, fp32 result.
+__device__ __forceinline__ void mma_bf16_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%10, %10, %10, %10};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// NS: 256-column spans of d_model; S: ring slots per warp; WPC: warps per CTA.
+template <int NS, int S, int WPC>
+__global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__nv_bfloat16> a)
+{
+    using E = __nv_bfloat16;
+    using L = BulkLayout<NS>;
+    constexpr int NC = 2 * NS;  // 128-column chunks
+    static_assert(NC >= 4, "four accumulator chains in the up projection");
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t* wbase = smem + warp * L::warp_bytes(S, a.nt);
+    SlotDesc* desc = reinterpret_cast<SlotDesc*>(wbase + S * L::kSlot);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(desc + S);
+    int* s_pref = reinterpret_cast<int*>(bar + S);
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const uint64_t pol_w = policy_evict_last(), pol_x = policy_evict_first();
+    RowStream<E, 0, 1> rs;
+    rs.init(a, nullptr, s_pref, nullptr, lane, 0, 0);
+
+    // -------------------------------------------------------------- issue: one nonzero per slot
+    int n_issued = 0;
+    bool ended = false;
+    auto issue = [&]() {
+        if (ended) return;
+        if (!rs.ready(a)) {
+            ended = true;
+            return;
+        }
+        const int p = rs.pos;
+        const int j = __shfl_sync(0xffffffffu, rs.c_j, p);
+        const float av = __shfl_sync(0xffffffffu, rs.c_a, p);
+        const int flags = (p == 0 ? (rs.c_flags & kFirst) : 0) | (p == rs.c_n - 1 ? (rs.c_flags & kLast) : 0);
+        ++rs.pos;
+        const int s = n_issued % S;
+        if (lane == 0) {
+            desc[s] = SlotDesc{rs.c_row, flags, av, 0};
+            uint8_t* slot = wbase + s * L::kSlot;
+            mbar_arrive_expect_tx(&bar[s], (flags & kFirst) ? 3 * L::kRow : 2 * L::kRow);
+            bulk_load(slot, a.Wu + static_cast<size_t>(j) * a.d, L::kRow, &bar[s], pol_w);
+            bulk_load(slot + L::kRow, a.Wd + static_cast<size_t>(j) * a.d, L::kRow, &bar[s], pol_w);
+            if (flags & kFirst)
+                bulk_load(slot + 2 * L::kRow, a.x + static_cast<size_t>(rs.c_row) * a.d, L::kRow, &bar[s], pol_x);
+        }
+        ++n_issued;
+    };
+
+    // -------------------------------------------------------------- compute
+    const bool diag = (g >> 1) == t;  // this lane holds the diagonal element g & 1 of its pairs
+    const uint32_t hmask = diag ? ((g & 1) ? 0xFFFF0000u : 0x0000FFFFu) : 0u;
+    uint32_t xf[NC][2];  // x_r as the A fragments (a0, a2) of the up projection, chunk by chunk
+    float yacc[NC][4];   // y_r: chunk c, columns 128c + 8g + 2t (+1) and 128c + 64 + 8g + 2t (+1)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        xf[c][0] = xf[c][1] = 0u;
+        yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
+    }
+    for (int i = 0; i < S; ++i) issue();
+    __syncwarp();
+    int n_done = 0;
+    while (n_done < n_issued) {
+        const int s = n_done % S;
+        const bool ok =
+            __all_sync(0xffffffffu, wait_bounded(&bar[s], static_cast<uint32_t>(n_done / S) & 1u, nullptr, a.status,
+                                                 a.wait_ns));
+        if (!ok) break;
+        const SlotDesc D = desc[s];
+        const uint32_t su = smem_u32(wbase + s * L::kSlot) + 16u * lane;
+        if (D.flags & kFirst) {
+#pragma unroll
+            for (int q = 0; q < NS; ++q) {
+                uint32_t r[4];
+                ldsm_x4_trans(r, su + 2 * L::kRow + 512u * q);
+                xf[2 * q][0] = r[0];
+                xf[2 * q][1] = r[1];
+                xf[2 * q + 1][0] = r[2];
+                xf[2 * q + 1][1] = r[3];
+            }
+        }
+        // up projection: four independent accumulator chains
+        float uc[4][4];
+#pragma unroll
+        for (int q = 0; q < NS; ++q) {
+            uint32_t w[4];
+            ldsm_x4_trans(w, su + 512u * q);
+            if (q < 2) {
+                mma_bf16_first(uc[2 * q], xf[2 * q][0], 0u, xf[2 * q][1], 0u, w[0], w[1]);
+                mma_bf16_first(uc[2 * q + 1], xf[2 * q + 1][0], 0u, xf[2 * q + 1][1], 0u, w[2], w[3]);
+            } else {
+                mma_bf16(uc[(2 * q) & 3], xf[2 * q][0], 0u, xf[2 * q][1], 0u, w[0], w[1]);
+                mma_bf16(uc[(2 * q + 1) & 3], xf[2 * q + 1][0], 0u, xf[2 * q + 1][1], 0u, w[2], w[3]);
+            }
+        }
+        const float s0 = (uc[0][0] + uc[1][0]) + (uc[2][0] + uc[3][0]);
+        const float s1 = (uc[0][1] + uc[1][1]) + (uc[2][1] + uc[3][1]);
+        float u = diag ? ((g & 1) ? s1 : s0) : 0.0f;
+        u += __shfl_xor_sync(0xffffffffu, u, 4);
+        u += __shfl_xor_sync(0xffffffffu, u, 9);
+        u += __shfl_xor_sync(0xffffffffu, u, 18);
+        // h = hi + lo, both bf16: the pair carries h to ~16 significant bits
+        const float h = D.a * u;
+        const uint32_t hi2 = bf16x2_rn(h, h);
+        const float lo = h - __uint_as_float(hi2 << 16);
+        const uint32_t hd = hi2 & hmask, ld = bf16x2_rn(lo, lo) & hmask;
+        // down projection: y_r += h * Wd_s[j]
+#pragma unroll
+        for (int q = 0; q < NS; ++q) {
+            uint32_t w[4];
+            ldsm_x4_trans(w, su + L::kRow + 512u * q);
+            mma_bf16(yacc[2 * q], hd, 0u, 0u, hd, w[0], w[1]);
+            mma_bf16(yacc[2 * q + 1], hd, 0u, 0u, hd, w[2], w[3]);
+            mma_bf16(yacc[2 * q], ld, 0u, 0u, ld, w[0], w[1]);
+            mma_bf16(yacc[2 * q + 1], ld, 0u, 0u, ld, w[2], w[3]);
+        }
+        if (D.flags & kLast) {
+            uint32_t* yr = reinterpret_cast<uint32_t*>(a.y + static_cast<size_t>(D.row) * a.d) + 4 * g + t;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                yr[64 * c] = bf16x2_rn(yacc[c][0], yacc[c][1]);
+                yr[64 * c + 32] = bf16x2_rn(yacc[c][2], yacc[c][3]);
+                yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
+            }
+        }
+        __syncwarp();  // every lane is done with slot s before it is refilled
+        ++n_done;
+        issue();
+        __syncwarp();  // the new slot's descriptor is visible to every lane
+    }
+    // After a timed-out wait: let the copies still in flight land before the CTA exits.
+    for (int i = n_done; i < n_issued; ++i)
+        wait_bounded(&bar[i % S], static_cast<uint32_t>(i / S) & 1u, nullptr, a.status, a.wait_ns);
+}
+
 // ------------------------------------------------------------------------------------------
 // Launch
 
@@ -784,6 +980,27 @@ static twell_status launch_mma(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
     return launch_persistent(ffn_mma_kernel<CPLX, R>, a, MmaSmem<CPLX>::cta_bytes(a.nt), kCtaWarps, s);
 }
 
+template <int NS, int S, int WPC>
+static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
+{
+    auto kern = ffn_bulk_kernel<NS, S, WPC>;
+    const size_t smem = static_cast<size_t>(WPC) * BulkLayout<NS>::warp_bytes(S, a.nt);
+    twell_host::DevInfo di;
+    if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    if (smem > di.max_smem_optin) return TWELL_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return TWELL_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * WPC, smem) != cudaSuccess || per_sm < 1)
+        return TWELL_ERR_CUDA;
+    if (cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    const int need = (a.N + WPC - 1) / WPC;
+    int grid = di.sm_count * per_sm;
+    if (grid > need) grid = need;
+    kern<<<grid, 32 * WPC, smem, s>>>(a);
+    return twell_host::launch_status();
+}
+
 // Kernel and layout for d_model = nchunks 16-byte chunks: the tensor-core kernel where it applies,
 // else chunks per lane (CPL) and warps per row (G) of the general kernel.
 template <typename E>
@@ -794,6 +1011,25 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
         // one warp per row: a warp's registers hold at most 2048 columns of y_r. Wider rows go to
         // the general kernel (two warps per row), which measured faster at 2560 columns (1.43 ms)
         // than this kernel with two warps per row (1.51 ms) on the 2B-like layer
+        // the bulk-copy kernel where its ring fits in shared memory (d_model 512 .. 3072); 8 warps
+        // per SM with a two-slot ring measured fastest on the 2048-wide layer (0.189-0.209 ms; three
+        // slots and 6 warps 0.233, four slots and 4 warps 0.311, two warps per row 0.234)
+        if (a.d % 256 == 0 && a.d >= 512 && a.d <= 3072) {
+            twell_status st = TWELL_ERR_UNSUPPORTED;
+            switch (a.d / 256) {
+            case 2: st = launch_bulk<2, 2, 8>(a, s); break;
+            case 3: st = launch_bulk<3, 2, 8>(a, s); break;
+            case 4: st = launch_bulk<4, 2, 8>(a, s); break;
+            case 5: st = launch_bulk<5, 2, 8>(a, s); break;
+            case 6: st = launch_bulk<6, 2, 8>(a, s); break;
+            case 7: st = launch_bulk<7, 2, 8>(a, s); break;
+            case 8: st = launch_bulk<8, 2, 8>(a, s); break;
+            case 10: st = launch_bulk<10, 2, 7>(a, s); break;
+            case 12: st = launch_bulk<12, 2, 6>(a, s); break;
+            default: break;
+            }
+            if (st != TWELL_ERR_UNSUPPORTED) return st;  // else: ring too large for shared memory
+        }
         if (a32 && a.d % 256 == 0) {
             switch (a.d / 256) {
             case 2: return launch_mma<2, 4>(a, s);
@@ -844,10 +1080,12 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
         twell::RowArgs<bf> p{static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd_s),
                              a->vals, a->idx, a->cnt, static_cast<bf*>(y), static_cast<int*>(ws), dev_status,
                              N, d, f, a->tile, nt, d / twell::Elem<bf>::kPer16B, vals_bf16};
+        p.wait_ns = twell_host::wait_limit_ns();
         return twell::run_fused(p, s);
     }
     twell::RowArgs<float> p{static_cast<const float*>(x), static_cast<const float*>(Wu_s),
                             static_cast<const float*>(Wd_s), a->vals, a->idx, a->cnt, static_cast<float*>(y),
                             static_cast<int*>(ws), dev_status, N, d, f, a->tile, nt, d / twell::Elem<float>::kPer16B, 0};
+    p.wait_ns = twell_host::wait_limit_ns();
     return twell::run_fused(p, s);
 }
