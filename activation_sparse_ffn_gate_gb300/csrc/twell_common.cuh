@@ -157,7 +157,21 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-template <bool CLUSTER = false>
+// The same test, suspending the thread in hardware for up to `hint_ns` while the phase is open.
+__device__ __forceinline__ bool mbar_test_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+template <bool CLUSTER = false, uint32_t SUSPEND_NS = 0>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              int32_t* status, uint64_t limit_ns)
 {
@@ -165,7 +179,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
     if (!CLUSTER && mbar_test_now(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (CLUSTER ? mbar_test_cluster(a, parity) : mbar_test(a, parity)) return true;
+        if (CLUSTER ? mbar_test_cluster(a, parity)
+                    : (SUSPEND_NS ? mbar_test_suspend(a, parity, SUSPEND_NS) : mbar_test(a, parity)))
+            return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             if (abort_flag != nullptr) *abort_flag = 1;

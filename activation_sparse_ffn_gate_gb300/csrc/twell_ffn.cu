@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) ffn_mma_kernel(const RowArgs<_
 // Both projections run as mma.sync m16n8k16 on operands read with ldmatrix.trans. Chunk c is
 // columns [128c, 128c + 128) of d_model, with X[k][m] = x_r[128c + 8k + m] and
 // W[k][n] = row[128c + 8k + n] (k < 16; m, n < 8):
-//   up:   A = X^T in rows 0..7 (rows 8..15 zero), B = Wu_s[j] chunk, so D[m][m] = sum_k X[k][m] W[k][m]
+//   up:   A = X^T in rows 0..7 (rows 8..15 unused), B = Wu_s[j] chunk, so D[m][m] = sum_k X[k][m] W[k][m]
 //         and the trace of D summed over the chunks is u = x_r . Wu_s[j]; the diagonal sits in the
 //         eight lanes (g, t) with g >> 1 = t, which sum it in three xor steps (4, 9, 18) that stay
 //         among them;
@@ -863,11 +863,18 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
     // -------------------------------------------------------------- compute
     const bool diag = (g >> 1) == t;  // this lane holds the diagonal element g & 1 of its pairs
     const uint32_t hmask = diag ? ((g & 1) ? 0xFFFF0000u : 0x0000FFFFu) : 0u;
-    uint32_t xf[NC][2];  // x_r as the A fragments (a0, a2) of the up projection, chunk by chunk
-    float yacc[NC][4];   // y_r: chunk c, columns 128c + 8g + 2t (+1) and 128c + 64 + 8g + 2t (+1)
+    // x_r as the A operands of the up projection, one register quad per chunk: a0 and a2 are the
+    // chunk's X^T blocks, a1 and a3 (rows 8..15 of A, whose products are never read) the
+    // neighbouring chunk's, so one ldmatrix yields a whole operand. Lane offsets into a 512-byte
+    // span for the quad of its even chunk (order: even lo, odd lo, even hi, odd hi) and odd chunk.
+    const int mi = lane >> 3, mr = lane & 7;
+    const uint32_t xoff_e = 16u * mr + ((mi & 1) ? 256u : 0u) + ((mi & 2) ? 128u : 0u);
+    const uint32_t xoff_o = 16u * mr + ((mi & 1) ? 0u : 256u) + ((mi & 2) ? 128u : 0u);
+    uint32_t xq[NC][4];
+    float yacc[NC][4];  // y_r: chunk c, columns 128c + 8g + 2t (+1) and 128c + 64 + 8g + 2t (+1)
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        xf[c][0] = xf[c][1] = 0u;
+        xq[c][0] = xq[c][1] = xq[c][2] = xq[c][3] = 0u;
         yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
     }
     for (int i = 0; i < S; ++i) issue();
@@ -876,20 +883,17 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
     while (n_done < n_issued) {
         const int s = n_done % S;
         const bool ok =
-            __all_sync(0xffffffffu, wait_bounded(&bar[s], static_cast<uint32_t>(n_done / S) & 1u, nullptr, a.status,
-                                                 a.wait_ns));
+            __all_sync(0xffffffffu, wait_bounded<false, 20000>(&bar[s], static_cast<uint32_t>(n_done / S) & 1u,
+                                                              nullptr, a.status, a.wait_ns));
         if (!ok) break;
         const SlotDesc D = desc[s];
-        const uint32_t su = smem_u32(wbase + s * L::kSlot) + 16u * lane;
+        const uint32_t sb = smem_u32(wbase + s * L::kSlot);
+        const uint32_t su = sb + 16u * lane;
         if (D.flags & kFirst) {
 #pragma unroll
             for (int q = 0; q < NS; ++q) {
-                uint32_t r[4];
-                ldsm_x4_trans(r, su + 2 * L::kRow + 512u * q);
-                xf[2 * q][0] = r[0];
-                xf[2 * q][1] = r[1];
-                xf[2 * q + 1][0] = r[2];
-                xf[2 * q + 1][1] = r[3];
+                ldsm_x4_trans(xq[2 * q], sb + 2 * L::kRow + 512u * q + xoff_e);
+                ldsm_x4_trans(xq[2 * q + 1], sb + 2 * L::kRow + 512u * q + xoff_o);
             }
         }
         // up projection: four independent accumulator chains
@@ -898,12 +902,14 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
         for (int q = 0; q < NS; ++q) {
             uint32_t w[4];
             ldsm_x4_trans(w, su + 512u * q);
+            const uint32_t(&e)[4] = xq[2 * q];
+            const uint32_t(&o)[4] = xq[2 * q + 1];
             if (q < 2) {
-                mma_bf16_first(uc[2 * q], xf[2 * q][0], 0u, xf[2 * q][1], 0u, w[0], w[1]);
-                mma_bf16_first(uc[2 * q + 1], xf[2 * q + 1][0], 0u, xf[2 * q + 1][1], 0u, w[2], w[3]);
+                mma_bf16_first(uc[2 * q], e[0], e[1], e[2], e[3], w[0], w[1]);
+                mma_bf16_first(uc[2 * q + 1], o[0], o[1], o[2], o[3], w[2], w[3]);
             } else {
-                mma_bf16(uc[(2 * q) & 3], xf[2 * q][0], 0u, xf[2 * q][1], 0u, w[0], w[1]);
-                mma_bf16(uc[(2 * q + 1) & 3], xf[2 * q + 1][0], 0u, xf[2 * q + 1][1], 0u, w[2], w[3]);
+                mma_bf16(uc[(2 * q) & 3], e[0], e[1], e[2], e[3], w[0], w[1]);
+                mma_bf16(uc[(2 * q + 1) & 3], o[0], o[1], o[2], o[3], w[2], w[3]);
             }
         }
         const float s0 = (uc[0][0] + uc[1][0]) + (uc[2][0] + uc[3][0]);
