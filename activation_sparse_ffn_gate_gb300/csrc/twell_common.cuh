@@ -438,6 +438,9 @@ struct DevInfo {
 };
 twell_status dev_info(DevInfo* out);
 
+// Bytes of the workspace twell_ffn_fused_fwd needs for N token rows of d_model d (twell_ffn.cu).
+size_t fused_ws_bytes(int N, int d);
+
 // 2-D tensor map over a row-major matrix of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row pitch `ld` elements; box [box_inner, box_outer]; 128-byte swizzle; zero fill
 // out of bounds.

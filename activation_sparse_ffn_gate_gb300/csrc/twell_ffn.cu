@@ -51,6 +51,13 @@ constexpr int kCtaWarps = 4;
 constexpr int kCtaThreads = 32 * kCtaWarps;
 constexpr int kFirst = 1, kLast = 2;
 
+struct __align__(16) SplitItem {
+    int row, beg, end, h;  // nonzeros [beg, end) of row; h: the row's first item (kSkipPart: empty)
+};
+struct __align__(16) HeavyRow {
+    int row, nseg, base, done;  // done: items finished so far (zeroed by the plan)
+};
+
 template <typename E>
 struct RowArgs {
     const E* x;
@@ -60,10 +67,48 @@ struct RowArgs {
     const uint8_t* idx;
     const uint16_t* cnt;
     E* y;
-    int* tickets;  // G == 1: row counter, zero at launch
+    int* tickets;  // G == 1: work counter, zero at launch; with split: [1] items, [2..4] row classes
     int32_t* status;
     int N, d, f, T, nt, nchunks, vals_bf16;
     uint64_t wait_ns;  // bound of every mbarrier wait (ffn_bulk_kernel)
+    // Long-row splitting (ffn_bulk_kernel only, split != 0; see split_plan_kernel)
+    int split = 0;
+    int item_cap = 0;
+    const int* list = nullptr;         // [3, N] unsplit rows by class (longest first)
+    const SplitItem* items = nullptr;  // [item_cap]
+    HeavyRow* heavy = nullptr;         // [item_cap], indexed by a split row's first item
+    float* part = nullptr;             // [item_cap, d] fp32 partial y_r of each item
+};
+
+// Rows with more than kSplitMin nonzeros are cut into ceil(nnz / kSplitSeg) items of near-equal
+// length, handed out before whole rows; the item that finishes last sums the items' fp32 partial
+// rows in item order and stores y_r (so y does not depend on which warp ran what). Whole rows
+// follow in three classes, longest first: more than kClassA nonzeros, more than kClassB, the rest.
+// Per-token nonzero counts vary by two orders of magnitude ([TC] §3): one warp walking a row of a
+// thousand nonzeros would otherwise finish long after all the others.
+constexpr int kSplitSeg = 128;
+constexpr int kSplitMin = 128;
+constexpr int kClassA = 64;
+constexpr int kClassB = 32;
+constexpr int kSkipPart = -2;  // an item left over when the item list ran out of room: no work
+constexpr int kWholeRow = -1;  // c_part of a whole row
+
+// Workspace of twell_ffn_fused_fwd (byte offsets, 256-byte aligned): a 256-byte header (work
+// counter and the plan's counts), the row lists, the items, the split rows, the partials.
+struct FusedWs {
+    int item_cap = 0;
+    size_t list = 0, items = 0, heavy = 0, part = 0, total = 0;
+    __host__ __device__ static size_t up(size_t v) { return (v + 255) & ~size_t(255); }
+    __host__ __device__ FusedWs(int N, int d)
+    {
+        int c = (N / 8 + 1) & ~1;
+        item_cap = c < 64 ? 64 : (c > 4096 ? 4096 : c);
+        list = 256;
+        items = list + up(static_cast<size_t>(N) * 12);
+        heavy = items + up(static_cast<size_t>(item_cap) * 16);
+        part = heavy + up(static_cast<size_t>(item_cap) * 16);
+        total = part + up(static_cast<size_t>(item_cap) * d * 4);
+    }
 };
 
 __host__ __device__ inline size_t pref_bytes(int nt) { return (static_cast<size_t>(nt + 1) * 4 + 15) & ~size_t(15); }
@@ -185,6 +230,12 @@ struct RowStream {
     uint32_t nx_idx, nx_val;                               // next segment (one nonzero per lane)
     int c_row, c_n, c_flags, c_xs, c_j, pos;               // current segment
     float c_a;
+    int n_beg, n_end, n_part;  // next work item: nonzeros [n_beg, n_end) of n_row; its partial slot
+    int i_beg, i_part;         // the item being issued
+    int nx_part, c_part;       // partial slot of the next / current segment (kWholeRow: a whole row)
+    int s_items, s_cls[3];     // split mode: the plan's items and unsplit rows per class
+    int p_kind, p_t;           // lane 0, split mode: the ticket taken one advance ago and its entry,
+    int4 p_raw;                // loaded but not yet used (1: item, 2: list row, 3: past the end)
 
     __device__ void next_ticket(const RowArgs<E>& a)
     {
@@ -249,14 +300,70 @@ struct RowStream {
         __syncwarp();
         return run;
     }
+    // Split mode, lane 0: start the load of ticket t's entry (used one advance later).
+    __device__ void fetch(const RowArgs<E>& a, int t)
+    {
+        p_t = t;
+        if (t < s_items) {
+            p_kind = 1;
+            p_raw = *reinterpret_cast<const int4*>(a.items + t);
+            return;
+        }
+        int i = t - s_items;
+        p_kind = 3;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            if (p_kind == 3 && i < s_cls[k]) {
+                p_kind = 2;
+                p_raw.x = a.list[static_cast<size_t>(k) * a.N + i];
+            }
+            i -= s_cls[k];
+        }
+    }
+    // Split mode: the next work item from the entry fetched one advance ago; fetch the entry of the
+    // ticket taken one advance ago; take a new ticket.
+    __device__ void next_item(const RowArgs<E>& a)
+    {
+        int r = a.N, b = 0, e = 0, pp = kWholeRow;
+        if (lane == 0) {
+            if (p_kind == 1) {
+                if (p_raw.w == kSkipPart) {
+                    r = 0;
+                    pp = kSkipPart;
+                } else {
+                    r = p_raw.x;
+                    b = p_raw.y;
+                    e = p_raw.z;
+                    pp = p_t;
+                }
+            } else if (p_kind == 2) {
+                r = p_raw.x;
+                e = 0x7fffffff;
+            }
+            fetch(a, tk);
+        }
+        n_row = __shfl_sync(0xffffffffu, r, 0);
+        n_beg = __shfl_sync(0xffffffffu, b, 0);
+        n_end = __shfl_sync(0xffffffffu, e, 0);
+        n_part = __shfl_sync(0xffffffffu, pp, 0);
+        load_counts(a, n_row);
+        next_ticket(a);
+    }
     __device__ void advance_issue_row(const RowArgs<E>& a)
     {
         i_row = n_row;
-        i_nnz = i_row < a.N ? scan_row(a, i_row) : 0;
-        i_base = 0;
-        n_row = ticket_row();
-        load_counts(a, n_row);
-        next_ticket(a);
+        i_part = n_part;
+        const int tot = i_row < a.N ? scan_row(a, i_row) : 0;
+        i_nnz = min(n_end, tot);
+        i_beg = min(n_beg, i_nnz);
+        i_base = i_beg;
+        if (a.split) {
+            next_item(a);
+        } else {
+            n_row = ticket_row();
+            load_counts(a, n_row);
+            next_ticket(a);
+        }
     }
     // Describe the next segment (loads of its indices and values stay in flight) and, at a row
     // start, copy x of that row into the next x buffer. Commits exactly one cp.async group.
@@ -270,8 +377,9 @@ struct RowStream {
         const int n = min(kSeg, i_nnz - i_base);
         nx_row = i_row;
         nx_n = n;
-        nx_flags = (i_base == 0 ? kFirst : 0) | (i_base + n >= i_nnz ? kLast : 0);
-        if (i_base == 0 && n > 0) {
+        nx_part = i_part;
+        nx_flags = (i_base == i_beg ? kFirst : 0) | (i_base + n >= i_nnz ? kLast : 0);
+        if (i_base == i_beg && n > 0) {
             nx_xs = xs_next;
             xs_next = xs_next + 1 == kXBufs ? 0 : xs_next + 1;
             const E* xr = a.x + static_cast<size_t>(i_row) * a.d;
@@ -305,6 +413,7 @@ struct RowStream {
         c_n = nx_n;
         c_flags = nx_flags;
         c_xs = nx_xs;
+        c_part = nx_part;
         if (lane < c_n) {
             int j = nx_toff + static_cast<int>(nx_idx);
             float v = __uint_as_float(nx_val);
@@ -341,11 +450,29 @@ struct RowStream {
         nx_idx = nx_val = 0;
         c_row = c_n = c_flags = c_xs = c_j = pos = 0;
         c_a = 0.0f;
+        n_beg = 0;
+        n_end = 0x7fffffff;
+        n_part = i_beg = i_part = nx_part = c_part = kWholeRow;
+        p_kind = 3;
+        p_t = 0;
+        p_raw = make_int4(0, 0, 0, 0);
+        s_items = s_cls[0] = s_cls[1] = s_cls[2] = 0;
         // pipeline fill: first row's counts and offsets, the next row's counts, the first segment
-        next_ticket(a);
-        n_row = ticket_row();
-        load_counts(a, n_row);
-        next_ticket(a);
+        if (a.split) {  // one stage more: ticket -> item or list entry -> counts -> offsets
+            s_items = min(a.tickets[1], a.item_cap);
+            s_cls[0] = a.tickets[2];
+            s_cls[1] = a.tickets[3];
+            s_cls[2] = a.tickets[4];
+            next_ticket(a);
+            if (lane == 0) fetch(a, tk);
+            next_ticket(a);
+            next_item(a);
+        } else {
+            next_ticket(a);
+            n_row = ticket_row();
+            load_counts(a, n_row);
+            next_ticket(a);
+        }
         advance_issue_row(a);
         issue_segment(a);
     }
@@ -360,7 +487,7 @@ struct RowStream {
             pos = 0;
             if (c_n < 0) return false;
             if (c_n == 0) {
-                zero_row(a, c_row);
+                if (c_part == kWholeRow) zero_row(a, c_row);  // a row without nonzeros
                 continue;
             }
             if (c_flags & kFirst) {
@@ -782,7 +909,7 @@ struct BulkLayout {
 struct __align__(16) SlotDesc {
     int row, flags;
     float a;
-    int pad;
+    int part;  // partial slot of a split row's item, kWholeRow for a whole row
 };
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
@@ -849,7 +976,7 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
         ++rs.pos;
         const int s = n_issued % S;
         if (lane == 0) {
-            desc[s] = SlotDesc{rs.c_row, flags, av, 0};
+            desc[s] = SlotDesc{rs.c_row, flags, av, rs.c_part};
             uint8_t* slot = wbase + s * L::kSlot;
             mbar_arrive_expect_tx(&bar[s], (flags & kFirst) ? 3 * L::kRow : 2 * L::kRow);
             bulk_load(slot, a.Wu + static_cast<size_t>(j) * a.d, L::kRow, &bar[s], pol_w);
@@ -877,6 +1004,16 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
         xq[c][0] = xq[c][1] = xq[c][2] = xq[c][3] = 0u;
         yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
     }
+    // y_r out of the accumulators (bf16 pairs), which are cleared for the next row
+    auto store_y = [&](int row) {
+        uint32_t* yr = reinterpret_cast<uint32_t*>(a.y + static_cast<size_t>(row) * a.d) + 4 * g + t;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            yr[64 * c] = bf16x2_rn(yacc[c][0], yacc[c][1]);
+            yr[64 * c + 32] = bf16x2_rn(yacc[c][2], yacc[c][3]);
+            yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
+        }
+    };
     for (int i = 0; i < S; ++i) issue();
     __syncwarp();
     int n_done = 0;
@@ -934,12 +1071,47 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
             mma_bf16(yacc[2 * q + 1], ld, 0u, 0u, ld, w[2], w[3]);
         }
         if (D.flags & kLast) {
-            uint32_t* yr = reinterpret_cast<uint32_t*>(a.y + static_cast<size_t>(D.row) * a.d) + 4 * g + t;
+            if (D.part == kWholeRow) {
+                store_y(D.row);
+            } else {
+                // an item of a split row: its fp32 partial out; the last of the row's items to
+                // finish adds all of them up in item order and stores y_r
+                float2* pp = reinterpret_cast<float2*>(a.part + static_cast<size_t>(D.part) * a.d) + 4 * g + t;
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                yr[64 * c] = bf16x2_rn(yacc[c][0], yacc[c][1]);
-                yr[64 * c + 32] = bf16x2_rn(yacc[c][2], yacc[c][3]);
-                yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
+                for (int c = 0; c < NC; ++c) {
+                    __stcg(pp + 64 * c, make_float2(yacc[c][0], yacc[c][1]));
+                    __stcg(pp + 64 * c + 32, make_float2(yacc[c][2], yacc[c][3]));
+                    yacc[c][0] = yacc[c][1] = yacc[c][2] = yacc[c][3] = 0.0f;
+                }
+                __threadfence();
+                __syncwarp();
+                int h = -1, nseg = 0;
+                if (lane == 0) {
+                    const int hh = __ldcg(&a.items[D.part].h);
+                    const int ns = __ldcg(&a.heavy[hh].nseg);
+                    if (atomicAdd(&a.heavy[hh].done, 1) == ns - 1) {
+                        h = hh;
+                        nseg = ns;
+                    }
+                }
+                h = __shfl_sync(0xffffffffu, h, 0);
+                nseg = __shfl_sync(0xffffffffu, nseg, 0);
+                if (h >= 0) {
+                    __threadfence();
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const float2* ps =
+                            reinterpret_cast<const float2*>(a.part + static_cast<size_t>(h + sg) * a.d) + 4 * g + t;
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            const float2 v0 = __ldcg(ps + 64 * c), v1 = __ldcg(ps + 64 * c + 32);
+                            yacc[c][0] += v0.x;
+                            yacc[c][1] += v0.y;
+                            yacc[c][2] += v1.x;
+                            yacc[c][3] += v1.y;
+                        }
+                    }
+                    store_y(D.row);
+                }
             }
         }
         __syncwarp();  // every lane is done with slot s before it is refilled
@@ -950,6 +1122,73 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
     // After a timed-out wait: let the copies still in flight land before the CTA exits.
     for (int i = n_done; i < n_issued; ++i)
         wait_bounded(&bar[i % S], static_cast<uint32_t>(i / S) & 1u, nullptr, a.status, a.wait_ns);
+}
+
+// ------------------------------------------------------------------------------------------
+// Work plan of the bulk kernel: one thread per token row, warps of 32 consecutive rows. A row's
+// nonzeros are counted as the walk counts them (a tile count above T counts as 0), with eight
+// loads in flight per thread (the counts are L2-resident). Rows with more than kSplitMin nonzeros
+// get ceil(nnz / kSplitSeg) consecutive items while the item list has room (one atomic per warp
+// reserves the warp's items); the other rows go to the list of their class (above kClassA
+// nonzeros, above kClassB, the rest). hdr[1..4] (zero at launch): items reserved, rows per class.
+__global__ void __launch_bounds__(128) split_plan_kernel(const uint16_t* __restrict__ cnt, int N, int nt, int T,
+                                                         int item_cap, int* __restrict__ hdr, int* __restrict__ list,
+                                                         SplitItem* __restrict__ items, HeavyRow* __restrict__ heavy)
+{
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r - lane >= N) return;  // whole warp past the end
+    const bool live = r < N;
+    int nnz = 0;
+    if (live) {
+        const uint16_t* cr = cnt + static_cast<size_t>(r) * nt;
+        int t = 0;
+        for (; t + 8 <= nt; t += 8) {
+            int c[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) c[k] = __ldg(cr + t + k);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) nnz += c[k] > T ? 0 : c[k];
+        }
+        for (; t < nt; ++t) {
+            const int c = __ldg(cr + t);
+            nnz += c > T ? 0 : c;
+        }
+    }
+    const bool want = live && nnz > kSplitMin;
+    const int nseg = want ? (nnz + kSplitSeg - 1) / kSplitSeg : 0;
+    int inc = nseg;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    int base0 = 0;
+    if (lane == 0 && tot > 0) base0 = atomicAdd(&hdr[1], tot);
+    const int base = __shfl_sync(0xffffffffu, base0, 0) + inc - nseg;
+    bool split = false;
+    if (want) {
+        if (static_cast<long long>(base) + nseg <= item_cap) {
+            split = true;
+            heavy[base] = HeavyRow{r, nseg, base, 0};
+            for (int sg = 0; sg < nseg; ++sg)
+                items[base + sg] = SplitItem{r, static_cast<int>(static_cast<long long>(sg) * nnz / nseg),
+                                             static_cast<int>(static_cast<long long>(sg + 1) * nnz / nseg), base};
+        } else {  // no room: the reserved items that fall inside the list are left empty
+            for (int sg = 0; sg < nseg && base + sg < item_cap; ++sg) items[base + sg] = SplitItem{0, 0, 0, kSkipPart};
+        }
+    }
+    const int cls = (!live || split) ? -1 : (nnz > kClassA ? 0 : (nnz > kClassB ? 1 : 2));
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const unsigned m = __ballot_sync(0xffffffffu, cls == k);
+        int b = 0;
+        if (lane == 0 && m) b = atomicAdd(&hdr[2 + k], __popc(m));
+        b = __shfl_sync(0xffffffffu, b, 0);
+        if (cls == k) list[static_cast<size_t>(k) * N + b + __popc(m & below)] = r;
+    }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -999,11 +1238,18 @@ static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * WPC, smem) != cudaSuccess || per_sm < 1)
         return TWELL_ERR_CUDA;
-    if (cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    // the work counter and the plan's counts start at zero; the plan splits the long rows
+    if (cudaMemsetAsync(a.tickets, 0, 5 * sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    RowArgs<__nv_bfloat16> b = a;
+    b.split = 1;
+    split_plan_kernel<<<(a.N + 127) / 128, 128, 0, s>>>(a.cnt, a.N, a.nt, a.T, a.item_cap, a.tickets,
+                                                        const_cast<int*>(a.list), const_cast<SplitItem*>(a.items),
+                                                        a.heavy);
+    if (twell_host::launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     const int need = (a.N + WPC - 1) / WPC;
     int grid = di.sm_count * per_sm;
     if (grid > need) grid = need;
-    kern<<<grid, 32 * WPC, smem, s>>>(a);
+    kern<<<grid, 32 * WPC, smem, s>>>(b);
     return twell_host::launch_status();
 }
 
@@ -1059,7 +1305,22 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
 
 }  // namespace twell
 
+size_t twell_host::fused_ws_bytes(int N, int d) { return twell::FusedWs(N, d).total; }
+
 using namespace twell_host;
+
+// The bulk kernel's share of the workspace (see FusedWs); the first word is every kernel's counter.
+template <typename E>
+static void set_split_ws(twell::RowArgs<E>& p, void* ws, int N, int d)
+{
+    const twell::FusedWs L(N, d);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.item_cap = L.item_cap;
+    p.list = reinterpret_cast<const int*>(w + L.list);
+    p.items = reinterpret_cast<const twell::SplitItem*>(w + L.items);
+    p.heavy = reinterpret_cast<twell::HeavyRow*>(w + L.heavy);
+    p.part = reinterpret_cast<float*>(w + L.part);
+}
 
 extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, const void* Wd_s, const twell_packed* a,
                                             int32_t N, int32_t d, int32_t f, twell_dtype dtype, void* y, void* ws,
@@ -1087,6 +1348,7 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
                              a->vals, a->idx, a->cnt, static_cast<bf*>(y), static_cast<int*>(ws), dev_status,
                              N, d, f, a->tile, nt, d / twell::Elem<bf>::kPer16B, vals_bf16};
         p.wait_ns = twell_host::wait_limit_ns();
+        set_split_ws(p, ws, N, d);
         return twell::run_fused(p, s);
     }
     twell::RowArgs<float> p{static_cast<const float*>(x), static_cast<const float*>(Wu_s),

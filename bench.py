@@ -49,6 +49,7 @@ def _args():
                    help="density x tile-width sweep on the 1.5B-like shapes and the 2B-like layer, against dense "
                         "cuBLAS (one JSON line per point; not the default bench line)")
     p.add_argument("--sweep-iters", type=int, default=15)
+    p.add_argument("--sweep-only", default="", help="with --sweep: only the points whose label contains this text")
     return p.parse_args()
 
 
@@ -576,6 +577,7 @@ def run_sweep(a):
     points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
     layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
     layers.append(("layer2b", synthetic.layer_2b))
+    layers = [(label, make) for label, make in layers if a.sweep_only in label]
     for label, make in layers:
         L = make()
         t = L.torch_inputs(dev)

@@ -87,13 +87,14 @@ def test_gate_pack_rejects_bad_arguments(lib):
 
 def test_fused_rejects_bad_arguments(lib):
     p = _packed()
+    need = lib.twell_workspace_bytes(1, 4, 64, 256, 128, 0, 0)  # TWELL_OP_FFN_FUSED_FWD
     call = lambda **kw: lib.twell_ffn_fused_fwd(  # noqa: E731
         ALIGNED, ALIGNED, ALIGNED, ctypes.byref(kw.get("p", p)), kw.get("N", 4), kw.get("d", 64),
-        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), kw.get("ws", ALIGNED), kw.get("ws_bytes", 256),
+        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), kw.get("ws", ALIGNED), kw.get("ws_bytes", need),
         STATUS, None)
     assert call(y=None) == 1
-    assert call(ws=None) == 7  # TWELL_ERR_WORKSPACE: the row-ticket counter is required
-    assert call(ws_bytes=16) == 7
+    assert call(ws=None) == 7  # TWELL_ERR_WORKSPACE: the work counter is required
+    assert call(ws_bytes=need - 1) == 7
     assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0  # an empty batch needs no workspace
     assert call(N=5) == 1
     assert call(d=12) == 1
@@ -137,3 +138,16 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load(str(tmp_path / "missing.so"))
         finally:
             binding._lib = binding._lib_backup
+
+
+def test_fused_workspace_grows_with_rows_and_width(lib):
+    """The fused walk's workspace holds a 256-byte header, three row lists of N entries and, for
+    split rows, item records and fp32 partial rows of width d; its size depends on N and d only."""
+    ws = lambda N, d: lib.twell_workspace_bytes(1, N, d, 5632, 128, 0, 0)  # noqa: E731
+    assert ws(1, 64) > 256
+    assert ws(8192, 2048) > ws(4096, 2048) > ws(64, 2048)
+    assert ws(8192, 2560) > ws(8192, 2048)
+    # item capacity N/8 between 64 and 4096: partial rows dominate, linear in d
+    assert ws(8192, 2048) >= 1024 * 2048 * 4 + 3 * 8192 * 4
+    assert ws(1 << 20, 1024) < ws(1 << 20, 2048) < 4096 * 2048 * 4 + 3 * (1 << 20) * 4 + 4096 * 32 + 4096
+    assert all(ws(N, 1024) % 256 == 0 for N in (1, 7, 100, 8192))

@@ -237,6 +237,41 @@ def test_fused_long_rows_cross_list_windows(cuda_dev):
     assert_close(y, y_ref, "fused long rows")
 
 
+def _long_row_layer(N, d, f, seed, base=0.008):
+    """Per-token density (lognormal spread, ten times denser sequence starts): rows from none to
+    over a thousand nonzeros, so the fused walk cuts the long rows into items."""
+    return synthetic.per_token_layer(N, d, f, 128, seed, base=base, normalise=True, seq_len=128, first=4)
+
+
+@pytest.mark.parametrize("d", [512, 2048, 2560])
+def test_fused_splits_long_rows(cuda_dev, d):
+    """Rows above 128 nonzeros are walked as several items whose fp32 partial rows the last one to
+    finish adds up in item order: the result matches the oracle and repeats bit for bit."""
+    L = _long_row_layer(1500, d, 3072, seed=d + 11)
+    G = oracle.gate(L.x, L.Wg_s)
+    nnz = (G > 0).sum(1)
+    assert (nnz > 128).sum() >= 20 and nnz.max() > 600
+    Ga = np.where(G > 0, G, 0.0).astype(np.float32)
+    tw = binding.twell_pack_from_gate(_to(cuda_dev, Ga, torch.float32), L.T)
+    t = L.torch_inputs(cuda_dev)
+    y1 = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    y2 = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
+    assert torch.equal(y1, y2)
+    vals, idx, cnt = oracle.twell_pack(Ga.astype(np.float64), L.T)
+    y_ref = oracle.twell_walk(vals, idx, cnt, L.T, L.x, L.Wu_s, L.Wd_s)
+    y = y1.double().cpu().numpy()
+    assert_close(y, y_ref, f"fused split rows d={d}")
+    assert_close(y[nnz > 128], y_ref[nnz > 128], f"fused, the split rows alone, d={d}")
+
+
+def test_fused_split_item_list_full(cuda_dev):
+    """More long rows than the item list holds (64 items; 100 rows of ~300 nonzeros want 300):
+    the rows that find no room are walked whole, the others split; every row matches the oracle."""
+    L = synthetic.uniform_layer(100, 2048, 3072, 128, 0.1, seed=21)
+    y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16, torch.float32)
+    assert_close(y, y_ref, "fused split, item list full")
+
+
 def test_fused_zero_density_is_exact_zero(cuda_dev):
     L = synthetic.uniform_layer(130, 256, 512, 128, 0.02, seed=1)
     L.Wg_s[:, 0] = -1e4
@@ -366,7 +401,9 @@ def test_full_size_layers_sampled(cuda_dev, which):
     tw = binding.twell_gate_pack(t["x"], t["Wg_s"], L.T)
     y = binding.twell_ffn_fused_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw)
     torch.cuda.synchronize()
-    rows = _sampled_rows(L.N, 24, seed=1)
+    # sampled rows plus the eight longest ones (on the 2B-like layer those are split into items)
+    longest = torch.argsort(tw.counts().sum(1), descending=True)[:8].cpu().numpy()
+    rows = np.unique(np.concatenate([_sampled_rows(L.N, 24, seed=1), longest]))
     y_ref, G, _ = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows, return_gu=True)
     assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, which)
     # the row counts agree with the oracle's except where |g| is at the accumulation-error level
