@@ -154,10 +154,16 @@ TWELL_API twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t 
  * y = 0. x [N, d], Wu_s / Wd_s [f, d], y [N, d] (device, element type `dtype`; the TwELL
  * values may be bf16 or fp32 independently, except that fp32 inputs need fp32 values).
  * d <= 8192 (bf16) / 4096 (fp32); f / tile <= 1024 tiles.
- * ws/ws_bytes: device workspace of at least twell_workspace_bytes(TWELL_OP_FFN_FUSED_FWD, ...)
- * bytes (256), 16-byte aligned, required when N > 0 (else TWELL_ERR_WORKSPACE). The call clears
- * its first word on `stream` and the kernel hands out token rows from it, so two calls in flight
- * at the same time must not share one workspace. Its contents need not be initialised.
+ * ws/ws_bytes: device workspace of at least twell_workspace_bytes(TWELL_OP_FFN_FUSED_FWD, N, d,
+ * ...) bytes, 16-byte aligned, required when N > 0 (else TWELL_ERR_WORKSPACE). It holds the work
+ * counter the kernel hands out rows from, a work plan (rows above 128 nonzeros are cut into items
+ * of at most 128, walked by different warps, and their fp32 partial rows are added up in item
+ * order by the last one to finish; the other rows are handed out longest class first) and those
+ * partial rows: about 12 B per row plus N/8 (64 .. 4096) partial rows of 4*d bytes. The call
+ * clears its header on `stream`, so two calls in flight at the same time must not share one
+ * workspace. Its contents need not be initialised. y is the same bit for bit from call to call,
+ * unless more rows want splitting than the N/8 item slots hold (those that find no room are
+ * walked whole, and which ones those are depends on scheduling).
  * A corrupt TwELL (count above the tile width, in-tile index >= tile, column >= f) is reported
  * as TWELL_ERR_DEVICE_CHECK in *dev_status; such entries contribute nothing.
  */
