@@ -40,6 +40,7 @@
 // in the status word as TWELL_ERR_DEVICE_CHECK and contributes nothing, and every access stays
 // inside the TwELL's own arrays.
 #include "twell_common.cuh"
+#include "twell_mma.cuh"
 
 namespace twell {
 
@@ -195,15 +196,6 @@ __device__ __forceinline__ void bar_sync_named(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-                 "{%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // Shared memory of one group of G warps: two ticket mailboxes, then the 2 x G partial dot
 // products of the general kernel (G <= 4).
@@ -912,28 +904,6 @@ struct __align__(16) SlotDesc {
     int part;  // partial slot of a split row's item, kWholeRow for a whole row
 };
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
-{
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-// D = A * B (no accumulator input) for one m16n8k16 tile, bf16 inputs, fp32 result.
-__device__ __forceinline__ void mma_bf16_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-                 "{%10, %10, %10, %10};"
-                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
-}
 
 // NS: 256-column spans of d_model; S: ring slots per warp; WPC: warps per CTA.
 template <int NS, int S, int WPC>

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "twell_gemm.cuh"
+#include "twell_light.cuh"
 
 namespace twell {
 
@@ -29,9 +30,9 @@ struct HybridWs {
     int nt, nblk, f_pad;
     size_t capr;  // backup rows rounded up to a 64-row k-block (zero-padded rows)
     // routing / forward
-    size_t tw_vals, tw_idx, tw_cnt, blk, l1acc, route_total, x_b, h_b, fwd_total;
+    size_t tw_vals, tw_idx, tw_cnt, blk, l1acc, tick, route_total, x_b, h_b, fwd_total;
     // backward
-    size_t ent, ccount, coff, ccur, rec, bx_b, dy_b, dh_b, dug, bh_b, bwd_total;
+    size_t ent, btick, ccount, coff, ccur, rec, bx_b, dy_b, dh_b, dug, bh_b, bwd_total;
     static size_t al(size_t v) { return (v + 255) & ~size_t(255); }
     HybridWs(int N, int d, int f, int K, int cap)
     {
@@ -50,6 +51,8 @@ struct HybridWs {
         o = al(o + static_cast<size_t>(nblk) * 4);
         l1acc = o;
         o = al(o + 16);
+        tick = o;  // row counter of the light-row kernel
+        o = al(o + 16);
         x_b = o;
         o = al(o + capr * d * 2);
         route_total = o;
@@ -59,6 +62,8 @@ struct HybridWs {
         o = 0;
         ent = o;
         o = al(o + static_cast<size_t>(N) * K * 12);
+        btick = o;
+        o = al(o + 16);
         ccount = o;
         o = al(o + static_cast<size_t>(f) * 4);
         coff = o;
@@ -769,13 +774,18 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
     st = run_route(L, w, N, f, K, static_cast<const bf*>(x), d, ctx, s);
     if (st != TWELL_OK) return st;
     double* l1acc = reinterpret_cast<double*>(w + L.l1acc);
-    // 3. light rows
-    const int threads = (d / 8 + 31) / 32 * 32;
-    twell::hybrid_light_fwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
-        static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd_s), N, d, f, K,
-        static_cast<const float*>(ctx->a), ctx->col, ctx->cnt, static_cast<float*>(ctx->u), static_cast<bf*>(y), l1acc,
-        ctx->dev_status);
-    if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
+    // 3. light rows: the tensor-core walk where d_model allows, else one CTA per row
+    st = light_fwd_bulk(x, Wu_s, Wd_s, N, d, f, K, static_cast<const float*>(ctx->a), ctx->col, ctx->cnt,
+                        static_cast<float*>(ctx->u), y, l1acc, reinterpret_cast<int*>(w + L.tick), ctx->dev_status, s);
+    if (st == TWELL_ERR_UNSUPPORTED) {
+        const int threads = (d / 8 + 31) / 32 * 32;
+        twell::hybrid_light_fwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
+            static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd_s), N, d, f, K,
+            static_cast<const float*>(ctx->a), ctx->col, ctx->cnt, static_cast<float*>(ctx->u), static_cast<bf*>(y),
+            l1acc, ctx->dev_status);
+        st = launch_status();
+    }
+    if (st != TWELL_OK) return st;
     // 4-6. backup rows: U_b = x_b Wu_s^T, H_b = A_b * U_b, y[rows] = H_b Wd_s
     if (cap > 0) {
         bf* x_b = reinterpret_cast<bf*>(w + L.x_b);
@@ -853,13 +863,19 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
     int* ccur = reinterpret_cast<int*>(w + L.ccur);
     twell::EntRec* rec = reinterpret_cast<twell::EntRec*>(w + L.rec);
 
-    // 1. light rows: dh, du, dg per entry and dx_r
+    // 1. light rows: dh, du, dg per entry and dx_r (the tensor-core walk where d_model allows)
     if (N > 0) {
-        twell::hybrid_light_bwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
-            static_cast<const bf*>(dy), static_cast<const bf*>(Wg_s), static_cast<const bf*>(Wu_s),
-            static_cast<const bf*>(Wd_s), N, d, f, K, static_cast<const float*>(ctx->a),
-            static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx, ctx->dev_status);
-        if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
+        st = light_bwd_bulk(dy, Wg_s, Wu_s, Wd_s, N, d, f, K, static_cast<const float*>(ctx->a),
+                            static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx,
+                            reinterpret_cast<int*>(w + L.btick), ctx->dev_status, s);
+        if (st == TWELL_ERR_UNSUPPORTED) {
+            twell::hybrid_light_bwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
+                static_cast<const bf*>(dy), static_cast<const bf*>(Wg_s), static_cast<const bf*>(Wu_s),
+                static_cast<const bf*>(Wd_s), N, d, f, K, static_cast<const float*>(ctx->a),
+                static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx, ctx->dev_status);
+            st = launch_status();
+        }
+        if (st != TWELL_OK) return st;
     }
     // 2. weight gradients of the light entries, per hidden unit (overwrites dW)
     const long long ne = static_cast<long long>(N) * K;

@@ -113,6 +113,22 @@ def _run_hybrid(dev, L, cap):
 @pytest.mark.parametrize("K,base", [(16, 0.01), (4, 0.02), (64, 0.02)])
 def test_hybrid_small_all_outputs(cuda_dev, K, base):
     L = synthetic.small_train(seed=K, N=300, d=256, f=1024, K=K, base=base, bf16=True)
+    _check_all_outputs(cuda_dev, L)
+
+
+@pytest.mark.parametrize("d", [512, 1024, 2048, 2560])
+def test_hybrid_tensor_core_light_rows(cuda_dev, d):
+    """Every d_model the tensor-core light-row walk serves, with light rows longer than one
+    32-entry segment, light rows without entries and backup rows: all outputs against the oracle."""
+    L = synthetic.small_train(seed=d, N=400, d=d, f=2048, K=48, base=0.012, bf16=True)
+    L.x[[5, 17, 200], 0] = 50.0  # threshold far above every gate: rows without entries
+    nnz = (oracle.gate(L.x, L.Wg_s) > 0).sum(1)
+    assert (nnz == 0).sum() >= 3 and ((nnz > 32) & (nnz <= 48)).sum() >= 5
+    _check_all_outputs(cuda_dev, L)
+
+
+def _check_all_outputs(cuda_dev, L):
+    K = L.K
     G = oracle.gate(L.x, L.Wg_s)
     n_over = ((G > 0).sum(1) > K).sum()
     assert n_over > 0  # the dense backup path is exercised
