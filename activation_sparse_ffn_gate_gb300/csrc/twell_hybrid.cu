@@ -501,12 +501,17 @@ __global__ void col_scatter_kernel(const uint16_t* __restrict__ hcol, const uint
     }
 }
 
-// Sort each column's records by row (a small insertion sort per column), so the per-column sums
+// Columns with more than this many records are sorted in global memory by col_sort_kernel, the
+// others in shared memory by col_dw_kernel.
+constexpr int kDwSmemRecs = 512;
+
+// Sort each long column's records by row (an insertion sort per column), so the per-column sums
 // below run in a fixed order whatever order the scatter's atomics produced.
 __global__ void col_sort_kernel(const int* __restrict__ coff, int f, EntRec* __restrict__ rec)
 {
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < f; j += gridDim.x * blockDim.x) {
         const int s = coff[j], e = coff[j + 1];
+        if (e - s <= kDwSmemRecs) continue;
         for (int i = s + 1; i < e; ++i) {
             const EntRec v = rec[i];
             int k = i - 1;
@@ -520,28 +525,63 @@ __global__ void col_sort_kernel(const int* __restrict__ coff, int f, EntRec* __r
 }
 
 // dWd_s[j] = sum h dy_r, dWu_s[j] = sum du x_r, dWg_s[j] = sum dg x_r over the records of
-// column j (one CTA per hidden unit, one thread per 8 elements of d_model); overwrites dW.
+// column j in ascending row order (one CTA per hidden unit, one thread per 8 elements of d_model);
+// overwrites dW. A column of at most kDwSmemRecs records is ranked by row in shared memory (rows
+// are distinct within a column); longer ones were sorted in place by col_sort_kernel. Records are
+// taken four at a time so that each thread has eight 16-byte loads in flight.
 __global__ void __launch_bounds__(512) col_dw_kernel(const int* __restrict__ coff, const EntRec* __restrict__ rec,
                                                      int f, int d, const __nv_bfloat16* __restrict__ x,
                                                      const __nv_bfloat16* __restrict__ dy, float* __restrict__ dWg,
                                                      float* __restrict__ dWu, float* __restrict__ dWd)
 {
+    __shared__ EntRec s_in[kDwSmemRecs], s_out[kDwSmemRecs];
     const int q = threadIdx.x, nchunks = d / 8;
     for (int j = blockIdx.x; j < f; j += gridDim.x) {
-        const int s = coff[j], e = coff[j + 1];
+        const int s = coff[j], m = coff[j + 1] - s;
+        const bool smem = m <= kDwSmemRecs;
+        __syncthreads();  // the previous column's records are no longer read
+        if (smem) {
+            for (int i = q; i < m; i += blockDim.x) s_in[i] = rec[s + i];
+            __syncthreads();
+            for (int i = q; i < m; i += blockDim.x) {
+                const int r = s_in[i].row;
+                int rank = 0;
+                for (int k = 0; k < m; ++k) rank += s_in[k].row < r ? 1 : 0;
+                s_out[rank] = s_in[i];
+            }
+            __syncthreads();
+        }
+        const EntRec* R = smem ? s_out : rec + s;
         float ag[8] = {}, au[8] = {}, ad[8] = {};
         if (q < nchunks) {
-            for (int i = s; i < e; ++i) {
-                const EntRec rc = rec[i];
+            auto step = [&](const EntRec& rc, const uint4& xr, const uint4& dr) {
                 float xv[8], dv[8];
-                bf8(ldg_stream16(x + static_cast<size_t>(rc.row) * d + q * 8), xv);
-                bf8(ldg_stream16(dy + static_cast<size_t>(rc.row) * d + q * 8), dv);
+                bf8(xr, xv);
+                bf8(dr, dv);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     ag[t] = fmaf(rc.dg, xv[t], ag[t]);
                     au[t] = fmaf(rc.du, xv[t], au[t]);
                     ad[t] = fmaf(rc.h, dv[t], ad[t]);
                 }
+            };
+            int i = 0;
+            for (; i + 4 <= m; i += 4) {
+                EntRec rc[4];
+                uint4 xr[4], dr[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    rc[k] = R[i + k];
+                    xr[k] = ldg_stream16(x + static_cast<size_t>(rc[k].row) * d + q * 8);
+                    dr[k] = ldg_stream16(dy + static_cast<size_t>(rc[k].row) * d + q * 8);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) step(rc[k], xr[k], dr[k]);
+            }
+            for (; i < m; ++i) {
+                const EntRec rc = R[i];
+                step(rc, ldg_stream16(x + static_cast<size_t>(rc.row) * d + q * 8),
+                     ldg_stream16(dy + static_cast<size_t>(rc.row) * d + q * 8));
             }
             const size_t o = static_cast<size_t>(j) * d + q * 8;
             *reinterpret_cast<float4*>(dWg + o) = make_float4(ag[0], ag[1], ag[2], ag[3]);

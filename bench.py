@@ -45,6 +45,8 @@ def _args():
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-train", action="store_true", help="skip the hybrid training-step measurement")
     p.add_argument("--train-steps", type=int, default=20)
+    p.add_argument("--train-only", action="store_true",
+                   help="only the hybrid training step against the dense cuBLAS step (one JSON line)")
     p.add_argument("--sweep", action="store_true",
                    help="density x tile-width sweep on the 1.5B-like shapes and the 2B-like layer, against dense "
                         "cuBLAS (one JSON line per point; not the default bench line)")
@@ -543,6 +545,20 @@ def train_step_measure(a, dev, flush, peaks):
             "launches_per_step": 23, "l2": "flushed before every step"}
 
 
+def run_train_only(a):
+    """The training-step measurement alone, as one JSON line."""
+    import torch
+
+    from activation_sparse_ffn_gate_gb300 import binding, build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    print(json.dumps({"train_step": train_step_measure(a, dev, flush, _peaks())}), flush=True)
+
+
 def run_sweep(a):
     """Density x tile-width sweep on the 1.5B-like shapes (N=8192, d=2048, f=5632, uniform density
     p, no dead columns) and the 2B-like layer, each against a dense cuBLAS bf16 FFN of the same
@@ -612,6 +628,10 @@ def main():
     if a.sweep:
         if rank == 0:
             run_sweep(a)
+        return
+    if a.train_only:
+        if rank == 0:
+            run_train_only(a)
         return
     if a.impl == "reference":
         run_reference(a, rank, world)
