@@ -214,7 +214,8 @@ def _source_hash(files):
 KERNEL_SOURCES = {
     "gate": ["activation_sparse_ffn_gate_gb300/csrc/twell_gemm.cuh", "activation_sparse_ffn_gate_gb300/csrc/twell_gate.cu",
              "activation_sparse_ffn_gate_gb300/csrc/twell_common.cuh"],
-    "fused": ["activation_sparse_ffn_gate_gb300/csrc/twell_ffn.cu", "activation_sparse_ffn_gate_gb300/csrc/twell_common.cuh"],
+    "fused": ["activation_sparse_ffn_gate_gb300/csrc/twell_ffn.cu", "activation_sparse_ffn_gate_gb300/csrc/twell_common.cuh",
+              "activation_sparse_ffn_gate_gb300/csrc/twell_mma.cuh"],
 }
 
 
@@ -472,7 +473,7 @@ def run_ours(a, rank, world):
         "cpu_baseline": cpu,
         "e2e": {"value": N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": N * d * 2,
                 "d2h_bytes_per_step": N * d * 2, "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * a.steps,
+        "gpu_launches": 3 * a.steps,  # per step: gate + pack, the walk's plan, the walk
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
