@@ -150,15 +150,15 @@ def status_buffer(device=None) -> torch.Tensor:
 _fused_ws = {}
 
 
-def fused_workspace(N: int, d: int, device=None, stream=None) -> torch.Tensor:
-    """The workspace twell_ffn_fused_fwd needs for N rows of width d (work counter, split plan and
-    the partial rows of split rows), one per device and stream, grown on demand: calls on one
-    stream run one after the other, so they can share it."""
+def fused_workspace(N: int, d: int, f: int, device=None, stream=None) -> torch.Tensor:
+    """The workspace twell_ffn_fused_fwd needs for N rows, d_model d, d_ff f (work counter, split
+    plan and the partial rows of split rows), one per device and stream, grown on demand: calls on
+    one stream run one after the other, so they can share it."""
     dev = torch.device(device if device is not None else torch.cuda.current_device())
     if dev.index is None:
         dev = torch.device("cuda", torch.cuda.current_device())
     key = (dev.index, _stream(stream).value or 0)
-    n = int(load().twell_workspace_bytes(OP_FFN_FUSED_FWD, N, d, 8, 8, 0, 0))
+    n = int(load().twell_workspace_bytes(OP_FFN_FUSED_FWD, N, d, f, 8, 0, 0))
     buf = _fused_ws.get(key)
     if buf is None or buf.numel() < n:
         buf = torch.empty(n, dtype=torch.uint8, device=dev)
@@ -241,7 +241,7 @@ def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
     N, d = x.shape
     f = Wu_s.shape[0]
     y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
-    ws = ws if ws is not None else fused_workspace(N, d, x.device, stream)
+    ws = ws if ws is not None else fused_workspace(N, d, f, x.device, stream)
     s = a.c_struct()
     _check(load().twell_ffn_fused_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), N, d, f,
                                       _dtype_code(x.dtype), _ptr(y), _ptr(ws), ws.numel(),

@@ -438,8 +438,8 @@ struct DevInfo {
 };
 twell_status dev_info(DevInfo* out);
 
-// Bytes of the workspace twell_ffn_fused_fwd needs for N token rows of d_model d (twell_ffn.cu).
-size_t fused_ws_bytes(int N, int d);
+// Bytes of the workspace twell_ffn_fused_fwd needs for N token rows, d_model d, d_ff f (twell_ffn.cu).
+size_t fused_ws_bytes(int N, int d, int f);
 
 // 2-D tensor map over a row-major matrix of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row pitch `ld` elements; box [box_inner, box_outer]; 128-byte swizzle; zero fill

@@ -81,14 +81,16 @@ struct RowArgs {
     float* part = nullptr;             // [item_cap, d] fp32 partial y_r of each item
 };
 
-// Rows with more than kSplitMin nonzeros are cut into ceil(nnz / kSplitSeg) items of near-equal
-// length, handed out before whole rows; the item that finishes last sums the items' fp32 partial
-// rows in item order and stores y_r (so y does not depend on which warp ran what). Whole rows
-// follow in three classes, longest first: more than kClassA nonzeros, more than kClassB, the rest.
-// Per-token nonzero counts vary by two orders of magnitude ([TC] §3): one warp walking a row of a
-// thousand nonzeros would otherwise finish long after all the others.
+// Rows with more than `seg` nonzeros are cut into ceil(nnz / seg) items of near-equal length,
+// handed out before whole rows; the item that finishes last sums the items' fp32 partial rows in
+// item order and stores y_r (so y does not depend on which warp ran what). Whole rows follow in
+// three classes, longest first: more than kClassA nonzeros, more than kClassB, the rest. Per-token
+// nonzero counts vary by two orders of magnitude ([TC] §3): one warp walking a row of a thousand
+// nonzeros would otherwise finish long after all the others. seg is kSplitSeg for large batches
+// and shrinks with N down to kSplitSegMin, so that a small batch (decoding a few tokens) spreads
+// each row's nonzeros over many warps instead of leaving all but N of them idle.
 constexpr int kSplitSeg = 128;
-constexpr int kSplitMin = 128;
+constexpr int kSplitSegMin = 4;
 constexpr int kClassA = 64;
 constexpr int kClassB = 32;
 constexpr int kSkipPart = -2;  // an item left over when the item list ran out of room: no work
@@ -100,10 +102,15 @@ struct FusedWs {
     int item_cap = 0;
     size_t list = 0, items = 0, heavy = 0, part = 0, total = 0;
     __host__ __device__ static size_t up(size_t v) { return (v + 255) & ~size_t(255); }
-    __host__ __device__ FusedWs(int N, int d)
+    // Item slots: N/8 within [4096, 16384] (so that a small batch cut into short items rarely runs
+    // out, which would make the split depend on scheduling), and no more than a batch can use.
+    __host__ __device__ FusedWs(int N, int d, int f)
     {
-        int c = (N / 8 + 1) & ~1;
-        item_cap = c < 64 ? 64 : (c > 4096 ? 4096 : c);
+        const long long most = static_cast<long long>(N) * ((f + kSplitSegMin - 1) / kSplitSegMin);
+        long long c = N / 8;
+        c = c < 4096 ? 4096 : (c > 16384 ? 16384 : c);
+        if (c > most) c = most;
+        item_cap = static_cast<int>(c < 64 ? 64 : c);
         list = 256;
         items = list + up(static_cast<size_t>(N) * 12);
         heavy = items + up(static_cast<size_t>(item_cap) * 16);
@@ -1097,12 +1104,13 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
 // ------------------------------------------------------------------------------------------
 // Work plan of the bulk kernel: one thread per token row, warps of 32 consecutive rows. A row's
 // nonzeros are counted as the walk counts them (a tile count above T counts as 0), with eight
-// loads in flight per thread (the counts are L2-resident). Rows with more than kSplitMin nonzeros
-// get ceil(nnz / kSplitSeg) consecutive items while the item list has room (one atomic per warp
+// loads in flight per thread (the counts are L2-resident). Rows with more than seg nonzeros
+// get ceil(nnz / seg) consecutive items while the item list has room (one atomic per warp
 // reserves the warp's items); the other rows go to the list of their class (above kClassA
 // nonzeros, above kClassB, the rest). hdr[1..4] (zero at launch): items reserved, rows per class.
 __global__ void __launch_bounds__(128) split_plan_kernel(const uint16_t* __restrict__ cnt, int N, int nt, int T,
-                                                         int item_cap, int* __restrict__ hdr, int* __restrict__ list,
+                                                         int seg, int item_cap, int* __restrict__ hdr,
+                                                         int* __restrict__ list,
                                                          SplitItem* __restrict__ items, HeavyRow* __restrict__ heavy)
 {
     const int lane = threadIdx.x & 31;
@@ -1125,8 +1133,8 @@ __global__ void __launch_bounds__(128) split_plan_kernel(const uint16_t* __restr
             nnz += c > T ? 0 : c;
         }
     }
-    const bool want = live && nnz > kSplitMin;
-    const int nseg = want ? (nnz + kSplitSeg - 1) / kSplitSeg : 0;
+    const bool want = live && nnz > seg;
+    const int nseg = want ? (nnz + seg - 1) / seg : 0;
     int inc = nseg;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1212,13 +1220,21 @@ static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
     if (cudaMemsetAsync(a.tickets, 0, 5 * sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
     RowArgs<__nv_bfloat16> b = a;
     b.split = 1;
-    split_plan_kernel<<<(a.N + 127) / 128, 128, 0, s>>>(a.cnt, a.N, a.nt, a.T, a.item_cap, a.tickets,
+    // Items of up to 128 nonzeros; for a small batch the largest power of two with at least one item
+    // per resident warp if rows carried 32 nonzeros (seg <= 32 N / warps), but no fewer than 4.
+    int seg = kSplitSeg;
+    const long long warps = static_cast<long long>(di.sm_count) * per_sm * WPC;
+    while (seg > kSplitSegMin && seg * warps > 32ll * a.N) seg >>= 1;
+    split_plan_kernel<<<(a.N + 127) / 128, 128, 0, s>>>(a.cnt, a.N, a.nt, a.T, seg, a.item_cap, a.tickets,
                                                         const_cast<int*>(a.list), const_cast<SplitItem*>(a.items),
                                                         a.heavy);
     if (twell_host::launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    const int need = (a.N + WPC - 1) / WPC;
+    // a warp per work item at most: the rows plus the items split rows can be cut into
+    const long long most_items = static_cast<long long>(a.N) * ((a.f + seg - 1) / seg);
+    const long long work = a.N + (most_items < a.item_cap ? most_items : a.item_cap);
+    const long long need = (work + WPC - 1) / WPC;
     int grid = di.sm_count * per_sm;
-    if (grid > need) grid = need;
+    if (grid > need) grid = static_cast<int>(need);
     kern<<<grid, 32 * WPC, smem, s>>>(b);
     return twell_host::launch_status();
 }
@@ -1275,15 +1291,15 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
 
 }  // namespace twell
 
-size_t twell_host::fused_ws_bytes(int N, int d) { return twell::FusedWs(N, d).total; }
+size_t twell_host::fused_ws_bytes(int N, int d, int f) { return twell::FusedWs(N, d, f).total; }
 
 using namespace twell_host;
 
 // The bulk kernel's share of the workspace (see FusedWs); the first word is every kernel's counter.
 template <typename E>
-static void set_split_ws(twell::RowArgs<E>& p, void* ws, int N, int d)
+static void set_split_ws(twell::RowArgs<E>& p, void* ws, int N, int d, int f)
 {
-    const twell::FusedWs L(N, d);
+    const twell::FusedWs L(N, d, f);
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.item_cap = L.item_cap;
     p.list = reinterpret_cast<const int*>(w + L.list);
@@ -1318,7 +1334,7 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
                              a->vals, a->idx, a->cnt, static_cast<bf*>(y), static_cast<int*>(ws), dev_status,
                              N, d, f, a->tile, nt, d / twell::Elem<bf>::kPer16B, vals_bf16};
         p.wait_ns = twell_host::wait_limit_ns();
-        set_split_ws(p, ws, N, d);
+        set_split_ws(p, ws, N, d, f);
         return twell::run_fused(p, s);
     }
     twell::RowArgs<float> p{static_cast<const float*>(x), static_cast<const float*>(Wu_s),

@@ -13,7 +13,7 @@ layer roofline of the method's byte model, the speedup over a dense cuBLAS bf16 
 shape, an end-to-end figure with host buffers, and the fp64 CPU oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-    python bench.py --sweep     # density x tile-width sweep and the 2B-like layer, one line each
+    python bench.py --sweep     # density x tile-width sweep, the 2B-like layer, decode batches: one line each
 N > 1 is launched with torchrun: every rank runs its own batch (weak scaling, no collective on
 the data path; a barrier and a max over ranks of the timed region only).
 """
@@ -48,8 +48,9 @@ def _args():
     p.add_argument("--train-only", action="store_true",
                    help="only the hybrid training step against the dense cuBLAS step (one JSON line)")
     p.add_argument("--sweep", action="store_true",
-                   help="density x tile-width sweep on the 1.5B-like shapes and the 2B-like layer, against dense "
-                        "cuBLAS (one JSON line per point; not the default bench line)")
+                   help="density x tile-width sweep on the 1.5B-like shapes, the 2B-like layer and small decode "
+                        "batches of the 1.5B-like layer, against dense cuBLAS (one JSON line per point; not the "
+                        "default bench line)")
     p.add_argument("--sweep-iters", type=int, default=15)
     p.add_argument("--sweep-only", default="", help="with --sweep: only the points whose label contains this text")
     return p.parse_args()
@@ -591,9 +592,25 @@ def run_sweep(a):
             ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
+    def graphed(fn):
+        """fn captured once into a CUDA graph; returns its replay. Small decode batches run for tens
+        of microseconds, less than the host needs to issue the calls, so their GPU time is taken
+        from graph replays (the kernels of one step, launched back to back)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
     points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
     layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
     layers.append(("layer2b", synthetic.layer_2b))
+    layers += [(f"decode N={n}", lambda n=n: synthetic.layer_1p5b(N=n)) for n in (1, 8, 64, 512)]
     layers = [(label, make) for label, make in layers if a.sweep_only in label]
     for label, make in layers:
         L = make()
@@ -604,12 +621,18 @@ def run_sweep(a):
         binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)
         nnz = int(packed.counts().sum().item())
         n_it = a.sweep_iters if nnz / L.N < 400 else max(3, a.sweep_iters // 3)
-        ms_gate = timed(lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status), n_it)
-        ms_fused = timed(lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status), n_it)
+        gate_fn = lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)  # noqa: E731
+        fused_fn = lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
 
         def dense_fn():
             return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
 
+        use_graphs = label.startswith("decode")
+        if use_graphs:
+            gate_fn, fused_fn, dense_fn = graphed(gate_fn), graphed(fused_fn), graphed(dense_fn)
+            n_it = max(n_it, 50)
+        ms_gate = timed(gate_fn, n_it)
+        ms_fused = timed(fused_fn, n_it)
         ms_dense = timed(dense_fn, n_it)
         binding.check_device_status(label, status)
         ms = ms_gate + ms_fused
@@ -617,7 +640,7 @@ def run_sweep(a):
                           "density": nnz / (L.N * L.f), "nnz_per_token": nnz / L.N, "ms_gate_pack": ms_gate,
                           "ms_fused": ms_fused, "ms_sparse": ms, "tokens_per_s": L.N / (ms * 1e-3),
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
-                          "l2": "flushed before every iteration"}), flush=True)
+                          "cuda_graphs": use_graphs, "l2": "flushed before every iteration"}), flush=True)
         del t, x, Wg, Wu, Wd, packed, y
         torch.cuda.empty_cache()
 

@@ -142,12 +142,15 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 def test_fused_workspace_grows_with_rows_and_width(lib):
     """The fused walk's workspace holds a 256-byte header, three row lists of N entries and, for
-    split rows, item records and fp32 partial rows of width d; its size depends on N and d only."""
-    ws = lambda N, d: lib.twell_workspace_bytes(1, N, d, 5632, 128, 0, 0)  # noqa: E731
+    split rows, item records and fp32 partial rows of width d; its size depends on N, d and f."""
+    ws = lambda N, d, f=5632: lib.twell_workspace_bytes(1, N, d, f, 128, 0, 0)  # noqa: E731
+    item = lambda d: 32 + 4 * d  # noqa: E731  (item record, split-row record, partial row)
     assert ws(1, 64) > 256
     assert ws(8192, 2048) > ws(4096, 2048) > ws(64, 2048)
     assert ws(8192, 2560) > ws(8192, 2048)
-    # item capacity N/8 between 64 and 4096: partial rows dominate, linear in d
-    assert ws(8192, 2048) >= 1024 * 2048 * 4 + 3 * 8192 * 4
-    assert ws(1 << 20, 1024) < ws(1 << 20, 2048) < 4096 * 2048 * 4 + 3 * (1 << 20) * 4 + 4096 * 32 + 4096
+    # item slots: N/8 within [4096, 16384], at most N * ceil(f / 4) (items of at least 4 nonzeros), at least 64
+    assert ws(8192, 2048) >= 4096 * item(2048) + 3 * 8192 * 4
+    assert ws(1, 2048, 64) < 64 * item(2048) + 4096  # at least 64 slots
+    assert ws(1 << 20, 1024) < ws(1 << 20, 2048) < 16384 * item(2048) + 3 * (1 << 20) * 4 + 4096
+    assert ws(1 << 20, 2048) >= 16384 * item(2048)
     assert all(ws(N, 1024) % 256 == 0 for N in (1, 7, 100, 8192))

@@ -245,8 +245,9 @@ def _long_row_layer(N, d, f, seed, base=0.008):
 
 @pytest.mark.parametrize("d", [512, 2048, 2560])
 def test_fused_splits_long_rows(cuda_dev, d):
-    """Rows above 128 nonzeros are walked as several items whose fp32 partial rows the last one to
-    finish adds up in item order: the result matches the oracle and repeats bit for bit."""
+    """Long rows are walked as several items (here of at most 32 nonzeros: 1500 rows are a small
+    batch) whose fp32 partial rows the last one to finish adds up in item order: the result
+    matches the oracle and repeats bit for bit."""
     L = _long_row_layer(1500, d, 3072, seed=d + 11)
     G = oracle.gate(L.x, L.Wg_s)
     nnz = (G > 0).sum(1)
@@ -265,11 +266,25 @@ def test_fused_splits_long_rows(cuda_dev, d):
 
 
 def test_fused_split_item_list_full(cuda_dev):
-    """More long rows than the item list holds (64 items; 100 rows of ~300 nonzeros want 300):
-    the rows that find no room are walked whole, the others split; every row matches the oracle."""
+    """More long rows than the item list holds (1024 items; 100 rows of ~300 nonzeros in items of 4
+    want ~7,700): the rows that find no room are walked whole, the others split; every row matches
+    the oracle."""
     L = synthetic.uniform_layer(100, 2048, 3072, 128, 0.1, seed=21)
     y, y_ref = _fused_from_oracle_pack(cuda_dev, L, torch.bfloat16, torch.float32)
     assert_close(y, y_ref, "fused split, item list full")
+
+
+@pytest.mark.parametrize("N", [1, 3, 64])
+def test_small_batch_decode(cuda_dev, N):
+    """Decoding a few tokens of the 1.5B-like layer (d_model 2048, d_ff 5632, ~29 nonzeros per
+    token): each row's nonzeros are spread over items of 4 nonzeros on different warps; gate + pack
+    and the walk end to end against the oracle, and a second call repeats bit for bit."""
+    L = synthetic.layer_1p5b(N=N)
+    t = L.torch_inputs(cuda_dev)
+    y1 = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=L.T)
+    y2 = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=L.T)
+    assert torch.equal(y1, y2)
+    assert_close(y1.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"decode N={N}")
 
 
 def test_fused_zero_density_is_exact_zero(cuda_dev):
