@@ -541,10 +541,20 @@ def train_step_measure(a, dev, flush, peaks):
         raise RuntimeError(f"hybrid training step reported status {code}")
     ms_dense = timed(dense, max(5, a.train_steps // 2))
     nb = int(ctx.n_backup.item())
+    # Activation memory the backward needs from the forward, per layer (x itself is common to both):
+    # the hybrid context (a, u fp32 and the column at each of the N*K block slots, the row counts,
+    # the backup list and the backup rows' dense a and u in fp32) against the dense step's saved
+    # gate pre-activation and up projection ([N, d_ff] bf16 each).
+    def hybrid_bytes(cap_rows):
+        return N * K * (4 + 4 + 2) + N * 2 + cap_rows * 4 + 2 * cap_rows * f * 4
+    act = {"hybrid_bytes_as_run": hybrid_bytes(cap), "hybrid_bytes_tight": hybrid_bytes(nb),
+           "dense_bytes": 2 * N * f * 2, "backup_cap_as_run": cap,
+           "note": "what the backward reads from the forward per layer; hybrid_bytes_tight sizes the backup "
+                   "buffers to this batch's backup rows; dense = g and u, [N, d_ff] bf16 each"}
     return {"workload": f"train2b_N{N}_d{d}_f{f}_K{K} (hybrid fwd + bwd, L1 {L.l1_coef})", "ms": ms,
             "tokens_per_s": N / (ms * 1e-3), "backup_rows": nb, "backup_frac": nb / N,
             "dense_cublas_ms": ms_dense, "speedup_vs_dense": ms_dense / ms,
-            "launches_per_step": 23, "l2": "flushed before every step"}
+            "activation_memory": act, "launches_per_step": 23, "l2": "flushed before every step"}
 
 
 def run_train_only(a):
