@@ -300,6 +300,20 @@ __device__ __forceinline__ void st_stream16(void* p, const uint4& v)
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
+// Two fp32 values, streaming (written once, not read again soon: first to leave L2).
+__device__ __forceinline__ void st_stream8(void* p, float a, float b)
+{
+    asm volatile("st.global.cs.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+// Read-only 16-byte load, not allocated in L1, with an L2 eviction policy (createpolicy).
+__device__ __forceinline__ uint4 ldg_l2hint16(const void* p, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
 
 // --------------------------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)

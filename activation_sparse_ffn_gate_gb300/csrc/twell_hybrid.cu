@@ -524,18 +524,22 @@ __global__ void col_sort_kernel(const int* __restrict__ coff, int f, EntRec* __r
     }
 }
 
-// dWd_s[j] = sum h dy_r, dWu_s[j] = sum du x_r, dWg_s[j] = sum dg x_r over the records of
-// column j in ascending row order (one CTA per hidden unit, one thread per 8 elements of d_model);
-// overwrites dW. A column of at most kDwSmemRecs records is ranked by row in shared memory (rows
-// are distinct within a column); longer ones were sorted in place by col_sort_kernel. Records are
-// taken four at a time so that each thread has eight 16-byte loads in flight.
+// Weight gradients of the light entries, per hidden unit j over the records of column j in
+// ascending row order (one CTA per hidden unit, one thread per 8 elements of d_model); overwrites
+// dW. Two passes, so that the rows one pass gathers fit in L2 (x and dy together are twice its
+// size at the 2B-like training shapes): PASS 0 dWg_s[j] = sum dg x_r and dWu_s[j] = sum du x_r,
+// PASS 1 dWd_s[j] = sum h dy_r; the gathered rows are loaded with an evict-last L2 policy. A column
+// of at most kDwSmemRecs records is ranked by row in shared memory (rows are distinct within a
+// column); longer ones were sorted in place by col_sort_kernel. Records are taken four at a time
+// so that each thread has four 16-byte loads in flight.
+template <int PASS>
 __global__ void __launch_bounds__(512) col_dw_kernel(const int* __restrict__ coff, const EntRec* __restrict__ rec,
-                                                     int f, int d, const __nv_bfloat16* __restrict__ x,
-                                                     const __nv_bfloat16* __restrict__ dy, float* __restrict__ dWg,
-                                                     float* __restrict__ dWu, float* __restrict__ dWd)
+                                                     int f, int d, const __nv_bfloat16* __restrict__ v,
+                                                     float* __restrict__ dWa, float* __restrict__ dWb)
 {
     __shared__ EntRec s_in[kDwSmemRecs], s_out[kDwSmemRecs];
     const int q = threadIdx.x, nchunks = d / 8;
+    const uint64_t pol = policy_evict_last();
     for (int j = blockIdx.x; j < f; j += gridDim.x) {
         const int s = coff[j], m = coff[j + 1] - s;
         const bool smem = m <= kDwSmemRecs;
@@ -552,44 +556,44 @@ __global__ void __launch_bounds__(512) col_dw_kernel(const int* __restrict__ cof
             __syncthreads();
         }
         const EntRec* R = smem ? s_out : rec + s;
-        float ag[8] = {}, au[8] = {}, ad[8] = {};
+        float aa[8] = {}, ab[8] = {};
         if (q < nchunks) {
-            auto step = [&](const EntRec& rc, const uint4& xr, const uint4& dr) {
-                float xv[8], dv[8];
-                bf8(xr, xv);
-                bf8(dr, dv);
+            auto step = [&](const EntRec& rc, const uint4& vr) {
+                float vv[8];
+                bf8(vr, vv);
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    ag[t] = fmaf(rc.dg, xv[t], ag[t]);
-                    au[t] = fmaf(rc.du, xv[t], au[t]);
-                    ad[t] = fmaf(rc.h, dv[t], ad[t]);
+                    if (PASS == 0) {
+                        aa[t] = fmaf(rc.dg, vv[t], aa[t]);
+                        ab[t] = fmaf(rc.du, vv[t], ab[t]);
+                    } else {
+                        aa[t] = fmaf(rc.h, vv[t], aa[t]);
+                    }
                 }
             };
             int i = 0;
             for (; i + 4 <= m; i += 4) {
                 EntRec rc[4];
-                uint4 xr[4], dr[4];
+                uint4 vr[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     rc[k] = R[i + k];
-                    xr[k] = ldg_stream16(x + static_cast<size_t>(rc[k].row) * d + q * 8);
-                    dr[k] = ldg_stream16(dy + static_cast<size_t>(rc[k].row) * d + q * 8);
+                    vr[k] = ldg_l2hint16(v + static_cast<size_t>(rc[k].row) * d + q * 8, pol);
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) step(rc[k], xr[k], dr[k]);
+                for (int k = 0; k < 4; ++k) step(rc[k], vr[k]);
             }
             for (; i < m; ++i) {
                 const EntRec rc = R[i];
-                step(rc, ldg_stream16(x + static_cast<size_t>(rc.row) * d + q * 8),
-                     ldg_stream16(dy + static_cast<size_t>(rc.row) * d + q * 8));
+                step(rc, ldg_l2hint16(v + static_cast<size_t>(rc.row) * d + q * 8, pol));
             }
             const size_t o = static_cast<size_t>(j) * d + q * 8;
-            *reinterpret_cast<float4*>(dWg + o) = make_float4(ag[0], ag[1], ag[2], ag[3]);
-            *reinterpret_cast<float4*>(dWg + o + 4) = make_float4(ag[4], ag[5], ag[6], ag[7]);
-            *reinterpret_cast<float4*>(dWu + o) = make_float4(au[0], au[1], au[2], au[3]);
-            *reinterpret_cast<float4*>(dWu + o + 4) = make_float4(au[4], au[5], au[6], au[7]);
-            *reinterpret_cast<float4*>(dWd + o) = make_float4(ad[0], ad[1], ad[2], ad[3]);
-            *reinterpret_cast<float4*>(dWd + o + 4) = make_float4(ad[4], ad[5], ad[6], ad[7]);
+            *reinterpret_cast<float4*>(dWa + o) = make_float4(aa[0], aa[1], aa[2], aa[3]);
+            *reinterpret_cast<float4*>(dWa + o + 4) = make_float4(aa[4], aa[5], aa[6], aa[7]);
+            if (PASS == 0) {
+                *reinterpret_cast<float4*>(dWb + o) = make_float4(ab[0], ab[1], ab[2], ab[3]);
+                *reinterpret_cast<float4*>(dWb + o + 4) = make_float4(ab[4], ab[5], ab[6], ab[7]);
+            }
         }
     }
 }
@@ -927,8 +931,10 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
         twell::col_scatter_kernel<<<grid_for(ne, 256, di.sm_count * 8), 256, 0, s>>>(ctx->col, ctx->cnt, N, K, f, ent,
                                                                                      ccur, rec);
     twell::col_sort_kernel<<<grid_for(f, 128, di.sm_count * 4), 128, 0, s>>>(coff, f, rec);
-    twell::col_dw_kernel<<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
-        coff, rec, f, d, static_cast<const bf*>(x), static_cast<const bf*>(dy), dWg_s, dWu_s, dWd_s);
+    twell::col_dw_kernel<0><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+        coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s);
+    twell::col_dw_kernel<1><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+        coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     if (cap == 0 || N == 0) return TWELL_OK;
 

@@ -341,9 +341,9 @@ __global__ void __launch_bounds__(32 * WPC, 1) light_kernel(const LightArgs a)
             } else {
                 float2* o = reinterpret_cast<float2*>(a.dx + static_cast<size_t>(D.row) * a.d) + 4 * g + t;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    o[64 * c] = make_float2(acc[c][0], acc[c][1]);
-                    o[64 * c + 32] = make_float2(acc[c][2], acc[c][3]);
+                for (int c = 0; c < NC; ++c) {  // streaming stores: dx must not push the weight rows out of L2
+                    st_stream8(o + 64 * c, acc[c][0], acc[c][1]);
+                    st_stream8(o + 64 * c + 32, acc[c][2], acc[c][3]);
                 }
             }
 #pragma unroll
