@@ -14,6 +14,12 @@
 // M and K may be read from device memory (rows of a device-side list, e.g. the hybrid backup
 // rows), so a launch sized for an upper bound does only the work that exists.
 //
+// Split K (k_splits > 1, StoreF32, one CTA per tile): the k-blocks of each tile are cut into
+// k_splits near-equal ranges, each a work unit of its own, and split s stores its partial sum at
+// out + s * split_stride; the caller adds the partials in split order (a fixed order, so the
+// result does not depend on scheduling). For products with few rows and a long K (the hybrid
+// backup rows), where whole tiles would leave most SMs idle.
+//
 // PAIR (A and B K-major): CTAs run in clusters of two on an SM pair, and one tcgen05.mma of
 // cta_group::2 computes a 256 x BN tile. CTA r holds rows [128r, 128r + 128) of the A tile and
 // rows [r BN/2, (r + 1) BN/2) of the B tile, both at the same shared-memory offsets, and its
@@ -51,6 +57,8 @@ struct GemmArgs {
     const int32_t* K_dyn;    // optional device scalar: K = min(K, *K_dyn)
     int kb_split;            // B source period in k-blocks: block kb reads map (kb / kb_split) & 1 at
                              // k-block kb % kb_split (one map: kb_split larger than every kb)
+    int k_splits;            // split K into this many ranges (0 or 1: no split; StoreF32 only)
+    int64_t split_stride;    // elements between the partial outputs of consecutive splits
     void* out;               // epilogue output
     int64_t ldo;             // its leading dimension (elements)
     const int32_t* rowmap;   // ScatterBF16: destination row of each m
@@ -112,6 +120,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tiles = M > 0 ? (M + kBM - 1) / kBM : 0;
     const int n_tiles = (g.N + BN - 1) / BN;
     const int kbs = K > 0 ? (K + kBK - 1) / kBK : 0;
+    // k-block ranges per tile: ks of them, each non-empty
+    const int ks = (PAIR || EPI != Epi::StoreF32 || g.k_splits <= 1) ? 1 : min(g.k_splits, max(kbs, 1));
     // work units: one 128 x BN tile per CTA, or with PAIR one 256 x BN tile per cluster, of which
     // this CTA holds the 128 rows of its rank (past M its loads read zeros and its epilogue
     // writes nothing)
@@ -119,9 +129,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool leader = crank == 0;
     const int unit0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int ustride = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
-    const int units = kbs > 0 ? (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles : 0;
-    auto tile_m0 = [&](int u) { return (PAIR ? 2 * (u / n_tiles) + crank : u / n_tiles) * kBM; };
-    auto tile_n0 = [&](int u) { return (u % n_tiles) * BN; };
+    const int units = kbs > 0 ? (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles * ks : 0;
+    // unit u: tile u / ks, k-block range u % ks
+    auto tile_m0 = [&](int u) { return (PAIR ? 2 * (u / ks / n_tiles) + crank : u / ks / n_tiles) * kBM; };
+    auto tile_n0 = [&](int u) { return (u / ks % n_tiles) * BN; };
+    auto kb_begin = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks) * kbs / ks); };
+    auto kb_end = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks + 1) * kbs / ks); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -163,7 +176,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int t = unit0; ok && t < units; t += ustride) {
                 const int m0 = tile_m0(t);
                 const int n0 = tile_n0(t);
-                for (int kb = 0; kb < kbs; ++kb) {
+                const int kb1 = kb_end(t);
+                for (int kb = kb_begin(t); kb < kb1; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) {
                         ok = false;
                         break;
@@ -221,7 +235,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!wait_bounded<PAIR>(&tempty[acc], acc_phase ^ 1u, abort_flag, g.status, g.wait_limit_ns)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < kbs; ++kb) {
+                const int kb0 = kb_begin(t), kb1 = kb_end(t);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(&full[stage], phase, abort_flag, g.status, g.wait_limit_ns)) {
                         ok = false;
                         break;
@@ -234,7 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // one MMA consumes K = 16: 32 bytes along a K-major row, 16 rows of an MN-major tile
                         const uint64_t da = A_MN ? desc_sw128(a_addr + k * 2048, 8192) : desc_sw128(a_addr + k * 32, 16);
                         const uint64_t db = B_MN ? desc_sw128(b_addr + k * 2048, 8192) : desc_sw128(b_addr + k * 32, 16);
-                        tc_mma_f16<CG>(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, da, db, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     // frees this stage (in both CTAs with PAIR) once its MMAs have read it
                     if constexpr (PAIR) tc_commit_mc<CG>(&empty[stage], 0x3);
@@ -307,7 +322,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int nvalid = min(32, g.N - col0);
                     if constexpr (EPI == Epi::StoreF32 || EPI == Epi::AccumF32 || EPI == Epi::ScatterF32) {
                         const int orow = (EPI == Epi::ScatterF32) ? g.rowmap[row] : row;
-                        float* o = static_cast<float*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0;
+                        float* o = static_cast<float*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0 +
+                                   (ks > 1 ? static_cast<size_t>(t % ks) * g.split_stride : size_t(0));
                         if (nvalid == 32) {
 #pragma unroll
                             for (int k = 0; k < 32; k += 4) {
@@ -425,8 +441,9 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         return TWELL_ERR_CUDA;
     g.wait_limit_ns = wait_limit_ns();
     const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + BN - 1) / BN;
+    if (g.k_splits > 1 && (PAIR || EPI != twell::Epi::StoreF32)) return TWELL_ERR_UNSUPPORTED;
     if constexpr (!PAIR) {
-        const long long tiles = m_tiles * n_tiles;
+        const long long tiles = m_tiles * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
         const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
         kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
         return launch_status();

@@ -12,6 +12,7 @@
 // Loss whose gradients are computed: L = <y, dy> + lambda * mean|h| over all N*f entries of h
 // ([AIM] ¶4; [PUL] ¶4: L1 coefficient 2e-5 on the hidden activations).
 #include <mutex>
+#include <type_traits>
 
 #include "twell_gemm.cuh"
 #include "twell_light.cuh"
@@ -22,6 +23,7 @@ constexpr int kHybTile = 128;   // TwELL tile of the gate epilogue inside the hy
 constexpr int kRouteRows = 128; // rows per routing block
 constexpr int kRowBatch = 8;    // nonzeros per batch in the light-row kernels
 constexpr int kMaxK = 65534;    // largest capacity K (counts are uint16, 0xFFFF marks a backup row)
+constexpr int kBackupSplits = 4; // K ranges of the backup rows' y and dx products (few rows, long K)
 
 // ------------------------------------------------------------------------------------------
 // Workspace layout (offsets in bytes from ws, each 256-byte aligned)
@@ -30,9 +32,9 @@ struct HybridWs {
     int nt, nblk, f_pad;
     size_t capr;  // backup rows rounded up to a 64-row k-block (zero-padded rows)
     // routing / forward
-    size_t tw_vals, tw_idx, tw_cnt, blk, l1acc, tick, route_total, x_b, h_b, fwd_total;
+    size_t tw_vals, tw_idx, tw_cnt, blk, l1acc, tick, route_total, x_b, h_b, y_part, fwd_total;
     // backward
-    size_t ent, btick, ccount, coff, ccur, rec, bx_b, dy_b, dh_b, dug, bh_b, bwd_total;
+    size_t ent, btick, ccount, coff, ccur, rec, bx_b, dy_b, dh_b, dug, bh_b, dx_part, bwd_total;
     static size_t al(size_t v) { return (v + 255) & ~size_t(255); }
     HybridWs(int N, int d, int f, int K, int cap)
     {
@@ -58,6 +60,8 @@ struct HybridWs {
         route_total = o;
         h_b = o;
         o = al(o + capr * 2 * f_pad * 2);  // [h_hi | h_lo] bf16
+        y_part = o;
+        o = al(o + kBackupSplits * capr * d * 4);  // fp32 partial y of the backup rows, per K range
         fwd_total = o;
         o = 0;
         ent = o;
@@ -82,6 +86,8 @@ struct HybridWs {
         o = al(o + capr * 4 * f_pad * 2);  // [du_hi | dg_hi | du_lo | dg_lo] bf16
         bh_b = o;
         o = al(o + capr * f_pad * 2);
+        dx_part = o;
+        o = al(o + kBackupSplits * capr * d * 4);  // fp32 partial dx of the backup rows, per K range
         bwd_total = o;
     }
 };
@@ -637,6 +643,38 @@ __global__ void backup_h_kernel(const float* __restrict__ A_b, const float* __re
     if ((threadIdx.x & 31) == 0 && l1 != 0.0f) atomicAdd(l1acc, static_cast<double>(l1));
 }
 
+// out[rowmap[m]] = the sum of part[s][m] over s = 0 .. splits-1 in that order, for m < min(*n, cap)
+// (bf16 or fp32 rows of d elements; part: splits blocks of `stride` elements, row pitch d).
+template <typename O>
+__global__ void reduce_rows_kernel(const float* __restrict__ part, int splits, long long stride,
+                                   const int32_t* __restrict__ n_dyn, int cap, int d, const int32_t* __restrict__ rowmap,
+                                   O* __restrict__ out)
+{
+    const int nb = min(*n_dyn, cap);
+    const int q4 = d / 4;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < static_cast<long long>(nb) * q4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int m = static_cast<int>(i / q4), c = static_cast<int>(i % q4) * 4;
+        float4 acc = *reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * d + c);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 v = *reinterpret_cast<const float4*>(part + sp * stride + static_cast<size_t>(m) * d + c);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        O* o = out + static_cast<size_t>(rowmap[m]) * d + c;
+        if constexpr (std::is_same<O, float>::value) {
+            *reinterpret_cast<float4*>(o) = acc;
+        } else {
+            o[0] = __float2bfloat16_rn(acc.x);
+            o[1] = __float2bfloat16_rn(acc.y);
+            o[2] = __float2bfloat16_rn(acc.z);
+            o[3] = __float2bfloat16_rn(acc.w);
+        }
+    }
+}
+
 __global__ void l1_finalize_kernel(const double* l1acc, float scale, float* l1)
 {
     *l1 = static_cast<float>(*l1acc * static_cast<double>(scale));
@@ -849,21 +887,28 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
             static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), ctx->n_backup, cap, f, L.f_pad,
             H_b, l1acc);
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-        // y[rows] = [h_hi | h_lo] [Wd_s ; Wd_s]
+        // y[rows] = [h_hi | h_lo] [Wd_s ; Wd_s]: kBackupSplits K ranges into fp32 partials, added
+        // up in order into the bf16 rows
+        float* y_part = reinterpret_cast<float*>(w + L.y_part);
         twell::GemmArgs g2{};
         g2.M = cap;
         g2.N = d;
         g2.K = 2 * L.f_pad;
         g2.kb_split = L.f_pad / 64;
+        g2.k_splits = twell::kBackupSplits;
+        g2.split_stride = static_cast<int64_t>(L.capr) * d;
         g2.M_dyn = ctx->n_backup;
-        g2.out = y;
+        g2.out = y_part;
         g2.ldo = d;
-        g2.rowmap = ctx->backup_rows;
         g2.status = ctx->dev_status;
         const GemmOperand Bd{Wd_s, f, d, d};
-        st = launch_gemm<256, false, true, twell::Epi::ScatterBF16>(
+        st = launch_gemm<256, false, true, twell::Epi::StoreF32>(
             GemmOperand{H_b, (int64_t)L.capr, 2 * L.f_pad, 2 * L.f_pad}, Bd, &Bd, g2, s);
         if (st != TWELL_OK) return st;
+        twell::reduce_rows_kernel<bf><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
+            y_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows,
+            static_cast<bf*>(y));
+        if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     }
     // 7. L1 term
     twell::l1_finalize_kernel<<<1, 1, 0, s>>>(l1acc, static_cast<float>(static_cast<double>(l1_coef) /
@@ -966,21 +1011,27 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
         static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), dH, ctx->n_backup, cap, f, L.f_pad,
         l1_scale, DUG, H_b);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    {  // dx[rows] = [du_hi | dg_hi | du_lo | dg_lo] [Wu_s ; Wg_s ; Wu_s ; Wg_s]  (fp32 output)
+    {  // dx[rows] = [du_hi | dg_hi | du_lo | dg_lo] [Wu_s ; Wg_s ; Wu_s ; Wg_s]  (fp32 output), in
+       // kBackupSplits K ranges added up in order
+        float* dx_part = reinterpret_cast<float*>(w + L.dx_part);
         twell::GemmArgs g{};
         g.M = cap;
         g.N = d;
         g.K = 4 * L.f_pad;
         g.M_dyn = ctx->n_backup;
         g.kb_split = L.f_pad / 64;
-        g.out = dx;
+        g.k_splits = twell::kBackupSplits;
+        g.split_stride = static_cast<int64_t>(L.capr) * d;
+        g.out = dx_part;
         g.ldo = d;
-        g.rowmap = ctx->backup_rows;
         g.status = ctx->dev_status;
         const GemmOperand B2{Wg_s, f, d, d};
-        st = launch_gemm<256, false, true, twell::Epi::ScatterF32>(
+        st = launch_gemm<256, false, true, twell::Epi::StoreF32>(
             GemmOperand{DUG, (int64_t)L.capr, 4 * L.f_pad, 4 * L.f_pad}, GemmOperand{Wu_s, f, d, d}, &B2, g, s);
         if (st != TWELL_OK) return st;
+        twell::reduce_rows_kernel<float><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
+            dx_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows, dx);
+        if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     }
     // dW += (backup rows)^T (...): A = [K = backup rows, M = f] (MN-major, the bf16 h / du / dg),
     // B = [K, N = d] (MN-major, dy_b or x_b); fp32 accumulation into the sparse part's result
