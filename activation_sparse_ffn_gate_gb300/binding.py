@@ -22,14 +22,14 @@ LIB_PATH = os.path.join(_PKG, "libtwell_gb300.so")
 TWELL_OK = 0
 TWELL_BF16 = 0
 TWELL_F32 = 1
-OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE = range(5)
+OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD = range(6)
 STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED", 3: "TWELL_ERR_BACKUP_FULL",
                 4: "TWELL_ERR_TIMEOUT", 5: "TWELL_ERR_DEVICE_CHECK", 6: "TWELL_ERR_CUDA",
                 7: "TWELL_ERR_WORKSPACE"}
 
 # Every function the header declares; the CPU tests check that the library exports each one.
 EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cnt_bytes", "twell_workspace_bytes",
-           "twell_gate_pack", "twell_ffn_fused_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
+           "twell_gate_pack", "twell_ffn_fused_fwd", "twell_ffn_union_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info")
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
                 "twell_gate_pack": (st, [vp, vp, i32, i32, i32, i32, ctypes.c_int, ctypes.POINTER(_Packed), vp, sz,
                                          vp, vp]),
                 "twell_ffn_fused_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
+                                             sz, vp, vp]),
+                "twell_ffn_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
                                              sz, vp, vp]),
                 "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
                                           ctypes.POINTER(_Hybrid), vp, vp, sz, vp]),
@@ -251,10 +253,41 @@ def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
     return y
 
 
+_union_ws = {}
+
+
+def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, a: TwELL,
+                        y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                        stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The same y as twell_ffn_fused_fwd, as two tensor-core GEMMs over all of d_ff (for dense layers)."""
+    N, d = x.shape
+    f = Wu_s.shape[0]
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    if ws is None:
+        n = twell_workspace_bytes(OP_FFN_UNION_FWD, N, d, f)
+        key = (x.device.index, _stream(stream).value or 0)
+        ws = _union_ws.get(key)
+        if ws is None or ws.numel() < n:
+            ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+            _union_ws[key] = ws
+    s = a.c_struct()
+    _check(load().twell_ffn_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), N, d, f,
+                                      _dtype_code(x.dtype), _ptr(y), _ptr(ws), ws.numel(),
+                                      _ptr(status if status is not None else status_buffer(x.device)),
+                                      _stream(stream)),
+           "twell_ffn_union_fwd")
+    return y
+
+
 def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
-                vals_dtype: torch.dtype = torch.float32):
-    """The sparse inference FFN: twell_gate_pack then twell_ffn_fused_fwd (two kernels)."""
+                vals_dtype: torch.dtype = torch.float32, path: str = "walk"):
+    """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk") or, for a
+    layer too dense for the walk, twell_ffn_union_fwd (path "union")."""
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
+    if path == "union":
+        return twell_ffn_union_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
+    if path != "walk":
+        raise ValueError(f"unknown path {path!r}")
     return twell_ffn_fused_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
 
 

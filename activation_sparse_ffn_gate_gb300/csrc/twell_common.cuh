@@ -454,6 +454,8 @@ twell_status dev_info(DevInfo* out);
 
 // Bytes of the workspace twell_ffn_fused_fwd needs for N token rows, d_model d, d_ff f (twell_ffn.cu).
 size_t fused_ws_bytes(int N, int d, int f);
+// Bytes of the workspace twell_ffn_union_fwd needs (twell_union.cu).
+size_t union_ws_bytes(int N, int f);
 
 // 2-D tensor map over a row-major matrix of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row pitch `ld` elements; box [box_inner, box_outer]; 128-byte swizzle; zero fill

@@ -49,6 +49,8 @@ enum class Epi : int {
     ScatterBF16 = 3, // out[rowmap[m], n] = bf16(acc)
     AccumF32 = 4,    // out[m, n] += acc (fp32)
     ScatterF32 = 5,  // out[rowmap[m], n] = acc (fp32)
+    MulBF16 = 6,     // out[m, n] = bf16(acc * aux[m, n]), aux bf16
+    MulHiLoBF16 = 7, // v = acc * aux[m, n]: out[m, n] = hi = bf16(v), out[m, n + lo_offset] = bf16(v - hi)
 };
 
 struct GemmArgs {
@@ -62,6 +64,9 @@ struct GemmArgs {
     void* out;               // epilogue output
     int64_t ldo;             // its leading dimension (elements)
     const int32_t* rowmap;   // ScatterBF16: destination row of each m
+    const void* aux;         // MulBF16, MulHiLoBF16: bf16 factor matrix [M, ldaux]
+    int64_t ldaux;
+    int64_t lo_offset;       // MulHiLoBF16: columns between a value's hi and lo parts
     // PackTwell
     int vals_f32;  // packed values stored as fp32 (else bf16, rounded to nearest even)
     void* vals;
@@ -349,7 +354,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     } else {
                         const int orow = (EPI == Epi::ScatterBF16) ? g.rowmap[row] : row;
                         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0;
-                        if (nvalid == 32) {
+                        if constexpr (EPI == Epi::MulBF16 || EPI == Epi::MulHiLoBF16) {  // v *= aux[row, col0 ..]
+                            const __nv_bfloat16* ax = static_cast<const __nv_bfloat16*>(g.aux) +
+                                                      static_cast<size_t>(row) * g.ldaux + col0;
+                            if (nvalid == 32) {
+#pragma unroll
+                                for (int k = 0; k < 32; k += 8) {
+                                    float f8[8];
+                                    unpack16(*reinterpret_cast<const uint4*>(ax + k), f8,
+                                             static_cast<__nv_bfloat16*>(nullptr));
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) v[k + e] *= f8[e];
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    if (k < nvalid) v[k] *= __bfloat162float(ax[k]);
+                            }
+                        }
+                        if constexpr (EPI == Epi::MulHiLoBF16) {  // hi, and the rounding remainder as lo
+                            if (nvalid == 32) {
+#pragma unroll
+                                for (int k = 0; k < 32; k += 8) {
+                                    float hi8[8], lo8[8];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        hi8[e] = __bfloat162float(__float2bfloat16_rn(v[k + e]));
+                                        lo8[e] = v[k + e] - hi8[e];
+                                    }
+                                    *reinterpret_cast<uint4*>(o + k) = pack16(hi8, static_cast<__nv_bfloat16*>(nullptr));
+                                    *reinterpret_cast<uint4*>(o + g.lo_offset + k) =
+                                        pack16(lo8, static_cast<__nv_bfloat16*>(nullptr));
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    if (k < nvalid) {
+                                        const __nv_bfloat16 hb = __float2bfloat16_rn(v[k]);
+                                        o[k] = hb;
+                                        o[g.lo_offset + k] = __float2bfloat16_rn(v[k] - __bfloat162float(hb));
+                                    }
+                            }
+                        } else if (nvalid == 32) {
 #pragma unroll
                             for (int k = 0; k < 32; k += 8) {
                                 float f8[8];

@@ -633,23 +633,30 @@ def run_sweep(a):
         n_it = a.sweep_iters if nnz / L.N < 400 else max(3, a.sweep_iters // 3)
         gate_fn = lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)  # noqa: E731
         fused_fn = lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
+        union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
 
         def dense_fn():
             return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
 
         use_graphs = label.startswith("decode")
         if use_graphs:
-            gate_fn, fused_fn, dense_fn = graphed(gate_fn), graphed(fused_fn), graphed(dense_fn)
+            gate_fn, fused_fn, union_fn, dense_fn = graphed(gate_fn), graphed(fused_fn), graphed(union_fn), \
+                graphed(dense_fn)
             n_it = max(n_it, 50)
         ms_gate = timed(gate_fn, n_it)
         ms_fused = timed(fused_fn, n_it)
+        ms_union = timed(union_fn, max(3, min(n_it, 15)))
         ms_dense = timed(dense_fn, n_it)
         binding.check_device_status(label, status)
         ms = ms_gate + ms_fused
+        ms_u = ms_gate + ms_union
+        best = "walk" if ms <= ms_u else "union"
         print(json.dumps({"sweep": label, "workload": L.name, "N": L.N, "d_model": L.d, "d_ff": L.f, "T": L.T,
                           "density": nnz / (L.N * L.f), "nnz_per_token": nnz / L.N, "ms_gate_pack": ms_gate,
                           "ms_fused": ms_fused, "ms_sparse": ms, "tokens_per_s": L.N / (ms * 1e-3),
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
+                          "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
+                          "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u),
                           "cuda_graphs": use_graphs, "l2": "flushed before every iteration"}), flush=True)
         del t, x, Wg, Wu, Wd, packed, y
         torch.cuda.empty_cache()

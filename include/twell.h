@@ -65,7 +65,8 @@ typedef enum {
     TWELL_OP_FFN_FUSED_FWD = 1,
     TWELL_OP_HYBRID_FWD = 2,
     TWELL_OP_HYBRID_BWD = 3,
-    TWELL_OP_HYBRID_ROUTE = 4
+    TWELL_OP_HYBRID_ROUTE = 4,
+    TWELL_OP_FFN_UNION_FWD = 5
 } twell_op;
 
 /* A TwELL matrix of gate activations a = ReLU(G), [n_rows, n_cols] ([TG] "Вот тут и решает TwELL";
@@ -168,6 +169,25 @@ TWELL_API twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t 
  * as TWELL_ERR_DEVICE_CHECK in *dev_status; such entries contribute nothing.
  */
 TWELL_API twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, const void* Wd_s,
+                                 const twell_packed* a, int32_t N, int32_t d, int32_t f,
+                                 twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream);
+
+/* The same y from the same TwELL for a layer too dense for the walk: with more than ~1% of
+ * d_ff kept per token the union of the units a tile of 128 tokens keeps is most of d_ff, so the
+ * up and down projections are dense contractions over all of it, on the tensor cores ([TC] §3:
+ * tensor cores for the heavy work). Steps: a = the TwELL expanded to dense bf16 [N, f_pad]
+ * (f_pad = f rounded up to 64); H = (x Wu_s^T) * a (tcgen05 GEMM, product in its epilogue) kept
+ * as two bf16 terms hi + lo (~16 significant bits, as in the walk); y = [hi | lo] [Wd_s ; Wd_s]
+ * (tcgen05 GEMM over 2 f_pad). Which of
+ * the two to call is the caller's policy, e.g. from the density of the previous batch
+ * (twell_column_activity); the walk wins below ~0.6% of d_ff per token on the 1.5B-like shapes.
+ * bf16 only; d and f multiples of 8; x [N, d], Wu_s / Wd_s [f, d], y [N, d], device, 16-byte
+ * aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (dense a and
+ * [hi | lo] of H, 6*N*f_pad bytes), required when N > 0. A corrupt TwELL (count above the tile width, column >= f) is
+ * reported as TWELL_ERR_DEVICE_CHECK in *dev_status; such entries contribute nothing.
+ */
+TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd_s,
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);

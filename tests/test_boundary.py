@@ -154,3 +154,21 @@ def test_fused_workspace_grows_with_rows_and_width(lib):
     assert ws(1 << 20, 1024) < ws(1 << 20, 2048) < 16384 * item(2048) + 3 * (1 << 20) * 4 + 4096
     assert ws(1 << 20, 2048) >= 16384 * item(2048)
     assert all(ws(N, 1024) % 256 == 0 for N in (1, 7, 100, 8192))
+
+
+def test_union_rejects_bad_arguments(lib):
+    p = _packed()
+    need = lib.twell_workspace_bytes(5, 4, 64, 256, 128, 0, 0)  # TWELL_OP_FFN_UNION_FWD
+    assert need >= 3 * 4 * 256 * 2  # dense a [N, f_pad] and [hi | lo] of H [N, 2 f_pad], bf16
+    call = lambda **kw: lib.twell_ffn_union_fwd(  # noqa: E731
+        ALIGNED, ALIGNED, ALIGNED, ctypes.byref(kw.get("p", p)), kw.get("N", 4), kw.get("d", 64),
+        kw.get("f", 256), kw.get("dt", 0), kw.get("y", ALIGNED), kw.get("ws", ALIGNED), kw.get("ws_bytes", need),
+        STATUS, None)
+    assert call(y=None) == 1
+    assert call(ws=None) == 7
+    assert call(ws_bytes=need - 1) == 7
+    assert call(dt=1) == 2  # bf16 only
+    assert call(d=12) == 1
+    assert call(N=5) == 1  # the TwELL describes 4 rows
+    assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0
+    assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1

@@ -287,6 +287,34 @@ def test_small_batch_decode(cuda_dev, N):
     assert_close(y1.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"decode N={N}")
 
 
+# ------------------------------------------------------------------------------------------ union path
+
+@pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
+def test_union_small_ragged(cuda_dev, vals_dtype):
+    """twell_ffn_union_fwd on an oracle-packed TwELL with a ragged last tile (d_ff = 1000)."""
+    L = synthetic.uniform_layer(300, 512, 1000, 128, 0.05, seed=31)
+    G = oracle.gate(L.x, L.Wg_s)
+    Ga = np.where(G > 0, G, 0.0)
+    Gs = synthetic.round_bf16_np(Ga.astype(np.float32)) if vals_dtype == torch.bfloat16 else Ga.astype(np.float32)
+    tw = binding.twell_pack_from_gate(_to(cuda_dev, Gs, vals_dtype), L.T)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.twell_ffn_union_fwd(t["x"], t["Wu_s"], t["Wd_s"], tw).double().cpu().numpy()
+    vals, idx, cnt = oracle.twell_pack(Gs.astype(np.float64), L.T)
+    assert_close(y, oracle.twell_walk(vals, idx, cnt, L.T, L.x, L.Wu_s, L.Wd_s), f"union {vals_dtype}")
+
+
+@pytest.mark.parametrize("p", [0.01, 0.05, 0.5])
+def test_union_sweep_shapes_end_to_end_sampled(cuda_dev, p):
+    """The union path end to end (gate + pack, then the two GEMMs) at the sweep's shapes
+    (d_model 2048, d_ff 5632, N = 1024) on sampled rows, against the oracle."""
+    L = synthetic.sweep_point(p, 128, N=1024)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128, path="union")
+    rows = _sampled_rows(L.N, 12, seed=3)
+    y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
+    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"union p={p}")
+
+
 def test_fused_zero_density_is_exact_zero(cuda_dev):
     L = synthetic.uniform_layer(130, 256, 512, 128, 0.02, seed=1)
     L.Wg_s[:, 0] = -1e4
