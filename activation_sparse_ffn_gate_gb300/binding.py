@@ -253,6 +253,53 @@ def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
     return y
 
 
+class StreamedFFN:
+    """The sparse inference FFN over a sequence of batches held in pinned host memory, with each
+    batch's copy to the device and its result's copy back overlapped with the neighbouring batches'
+    compute: host-to-device copies on one stream, gate + walk (or union path) on a second,
+    device-to-host copies on a third, ordered by events, with two device buffers of x and of y
+    used in turn. A serving loop so keeps the copy engines and the SMs busy at the same time; the
+    kernels and their results are those of ffn_forward."""
+
+    def __init__(self, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, N: int, T: int = 128,
+                 path: str = "walk", vals_dtype: torch.dtype = torch.float32, status: Optional[torch.Tensor] = None):
+        dev = Wg_s.device
+        f, d = Wg_s.shape
+        self.W, self.T, self.path, self.status, self.N, self.d = (Wg_s, Wu_s, Wd_s), T, path, status, N, d
+        self.copy_in, self.compute, self.copy_out = (torch.cuda.Stream(dev) for _ in range(3))
+        self.x = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
+        self.y = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
+        self.packed = TwELL.empty(N, f, T, vals_dtype, dev)
+        self.x_in = [torch.cuda.Event() for _ in range(2)]    # x[b] holds the batch
+        self.done = [torch.cuda.Event() for _ in range(2)]    # x[b] read, y[b] written
+        self.y_out = [torch.cuda.Event() for _ in range(2)]   # y[b] copied to the host
+        self.count = 0
+
+    def submit(self, x_host: torch.Tensor, y_host: torch.Tensor):
+        """Queue one batch: x_host [N, d] pinned input, y_host a pinned output of the same shape (valid
+        once the copy-out stream has passed it, e.g. after torch.cuda.synchronize())."""
+        if tuple(x_host.shape) != (self.N, self.d) or tuple(y_host.shape) != (self.N, self.d):
+            raise ValueError("batch shape differs from the pipeline's")
+        b, later = self.count % 2, self.count >= 2
+        with torch.cuda.stream(self.copy_in):
+            if later:
+                self.copy_in.wait_event(self.done[b])  # batch count-2 is done reading x[b]
+            self.x[b].copy_(x_host, non_blocking=True)
+            self.x_in[b].record(self.copy_in)
+        with torch.cuda.stream(self.compute):
+            self.compute.wait_event(self.x_in[b])
+            if later:
+                self.compute.wait_event(self.y_out[b])  # y[b] of batch count-2 is on the host
+            ffn_forward(self.x[b], *self.W, T=self.T, packed=self.packed, y=self.y[b], status=self.status,
+                        stream=self.compute, path=self.path)
+            self.done[b].record(self.compute)
+        with torch.cuda.stream(self.copy_out):
+            self.copy_out.wait_event(self.done[b])
+            y_host.copy_(self.y[b], non_blocking=True)
+            self.y_out[b].record(self.copy_out)
+        self.count += 1
+
+
 _union_ws = {}
 
 

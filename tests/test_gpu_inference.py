@@ -287,6 +287,22 @@ def test_small_batch_decode(cuda_dev, N):
     assert_close(y1.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"decode N={N}")
 
 
+def test_streamed_batches_match_ffn_forward(cuda_dev):
+    """binding.StreamedFFN (copies overlapped with compute on three streams, double-buffered device
+    buffers) returns, for five different host batches, exactly what ffn_forward returns for each."""
+    L = synthetic.uniform_layer(5 * 256, 512, 1024, 128, 0.02, seed=41)
+    t = L.torch_inputs(cuda_dev)
+    pipe = binding.StreamedFFN(t["Wg_s"], t["Wu_s"], t["Wd_s"], 256, T=L.T)
+    xs = [t["x"][256 * i:256 * (i + 1)].cpu().pin_memory() for i in range(5)]
+    ys = [torch.empty((256, L.d), dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    for xh, yh in zip(xs, ys):
+        pipe.submit(xh, yh)
+    torch.cuda.synchronize()
+    for i in range(5):
+        ref = binding.ffn_forward(t["x"][256 * i:256 * (i + 1)].contiguous(), t["Wg_s"], t["Wu_s"], t["Wd_s"], T=L.T)
+        assert torch.equal(ys[i], ref.cpu()), i
+
+
 # ------------------------------------------------------------------------------------------ union path
 
 @pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
