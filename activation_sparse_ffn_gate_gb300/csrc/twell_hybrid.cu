@@ -34,7 +34,7 @@ struct HybridWs {
     // routing / forward
     size_t tw_vals, tw_idx, tw_cnt, blk, l1acc, tick, route_total, x_b, h_b, y_part, fwd_total;
     // backward
-    size_t ent, btick, ccount, coff, ccur, rec, bx_b, dy_b, dh_b, dug, bh_b, dx_part, bwd_total;
+    size_t ent, btick, ccount, coff, ccur, rec, dy_b, dh_b, dug, dx_part, bwd_total;
     static size_t al(size_t v) { return (v + 255) & ~size_t(255); }
     HybridWs(int N, int d, int f, int K, int cap)
     {
@@ -74,18 +74,14 @@ struct HybridWs {
         o = al(o + static_cast<size_t>(f + 1) * 4);
         ccur = o;
         o = al(o + static_cast<size_t>(f) * 4);
-        rec = o;
-        o = al(o + static_cast<size_t>(N) * K * 16);
-        bx_b = o;
-        o = al(o + capr * d * 2);
+        rec = o;  // records of the light entries and of the backup rows' kept entries
+        o = al(o + (static_cast<size_t>(N) * K + static_cast<size_t>(cap) * f) * 16);
         dy_b = o;
         o = al(o + capr * d * 2);
         dh_b = o;
         o = al(o + capr * f_pad * 4);
         dug = o;
         o = al(o + capr * 4 * f_pad * 2);  // [du_hi | dg_hi | du_lo | dg_lo] bf16
-        bh_b = o;
-        o = al(o + capr * f_pad * 2);
         dx_part = o;
         o = al(o + kBackupSplits * capr * d * 4);  // fp32 partial dx of the backup rows, per K range
         bwd_total = o;
@@ -699,12 +695,14 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ src, const 
 
 // Backup-row gradients at every column: dh = dH + lambda sgn(h)/(N f); du = dh a; dg = dh u [a>0].
 // Writes DUG = [du_hi | dg_hi | du_lo | dg_lo] (bf16, row pitch 4 f_pad; the dx GEMM runs over all
-// four against [Wu ; Wg ; Wu ; Wg]) and H_hi = bf16(h) (pitch f_pad, for the dW GEMMs); rows
-// [nb, ceil64(nb)) and pad columns are zero.
+// four against [Wu ; Wg ; Wu ; Wg]); rows [nb, ceil64(nb)) and pad columns are zero. Every kept
+// entry (a > 0) of a backup row also becomes a column record {row, h, du, dg} for the per-unit
+// weight gradients (its slot from the column cursor), as the light rows' entries do: a backup row
+// keeps a few hundred of the d_ff units, so its weight gradients are sparse too.
 __global__ void backup_grad_kernel(const float* __restrict__ A_b, const float* __restrict__ U_b,
                                    const float* __restrict__ dH, const int32_t* __restrict__ n_backup, int cap, int f,
-                                   int f_pad, float l1_scale, __nv_bfloat16* __restrict__ DUG,
-                                   __nv_bfloat16* __restrict__ H_hi)
+                                   int f_pad, float l1_scale, const int32_t* __restrict__ brows, int* __restrict__ ccur,
+                                   EntRec* __restrict__ rec, __nv_bfloat16* __restrict__ DUG)
 {
     const int nb = min(*n_backup, cap);
     const int rows = min((nb + 63) / 64 * 64, (cap + 63) / 64 * 64);
@@ -721,6 +719,7 @@ __global__ void backup_grad_kernel(const float* __restrict__ A_b, const float* _
             const float g = dH[static_cast<size_t>(i) * f_pad + j] + l1_scale * sg;
             du = g * a;
             dg = a > 0.0f ? g * u : 0.0f;
+            if (a > 0.0f) rec[atomicAdd(&ccur[j], 1)] = EntRec{brows[i], h, du, dg};
         }
         __nv_bfloat16 du_hi, du_lo, dg_hi, dg_lo;
         split_bf16(du, du_hi, du_lo);
@@ -730,8 +729,17 @@ __global__ void backup_grad_kernel(const float* __restrict__ A_b, const float* _
         row[f_pad + j] = dg_hi;
         row[2 * f_pad + j] = du_lo;
         row[3 * f_pad + j] = dg_lo;
-        H_hi[static_cast<size_t>(i) * f_pad + j] = __float2bfloat16_rn(h);
     }
+}
+
+// Kept entries (a > 0) of the backup rows, per column: ccount[j] += #{i < min(nb, cap): A_b[i, j] > 0}.
+__global__ void col_hist_backup_kernel(const float* __restrict__ A_b, const int32_t* __restrict__ n_backup, int cap,
+                                       int f, int* __restrict__ ccount)
+{
+    const int nb = min(*n_backup, cap);
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < static_cast<long long>(nb) * f;
+         e += static_cast<long long>(gridDim.x) * blockDim.x)
+        if (A_b[e] > 0.0f) atomicAdd(&ccount[e % f], 1);
 }
 
 }  // namespace twell
@@ -967,35 +975,31 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
         }
         if (st != TWELL_OK) return st;
     }
-    // 2. weight gradients of the light entries, per hidden unit (overwrites dW)
+    // 2. column records of the kept entries (light rows from the sparse block, backup rows from
+    //    their dense a), per hidden unit, for the weight gradients
     const long long ne = static_cast<long long>(N) * K;
+    const bool backup = cap > 0 && N > 0;
     twell::fill_i32_kernel<<<grid_for(f, 256, 256), 256, 0, s>>>(ccount, f, 0);
     if (ne > 0)
         twell::col_hist_kernel<<<grid_for(ne, 256, di.sm_count * 8), 256, 0, s>>>(ctx->col, ctx->cnt, N, K, f, ccount);
+    if (backup)
+        twell::col_hist_backup_kernel<<<grid_for(static_cast<long long>(cap) * f, 256, di.sm_count * 8), 256, 0, s>>>(
+            static_cast<const float*>(ctx->A_b), ctx->n_backup, cap, f, ccount);
     twell::col_scan_kernel<<<1, 1024, 0, s>>>(ccount, f, coff, ccur);
     if (ne > 0)
         twell::col_scatter_kernel<<<grid_for(ne, 256, di.sm_count * 8), 256, 0, s>>>(ctx->col, ctx->cnt, N, K, f, ent,
                                                                                      ccur, rec);
-    twell::col_sort_kernel<<<grid_for(f, 128, di.sm_count * 4), 128, 0, s>>>(coff, f, rec);
-    twell::col_dw_kernel<0><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
-        coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s);
-    twell::col_dw_kernel<1><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
-        coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    if (cap == 0 || N == 0) return TWELL_OK;
 
-    // 3. backup rows: dense tensor-core GEMMs on the gathered rows
-    bf* x_b = reinterpret_cast<bf*>(w + L.bx_b);
+    // 3. backup rows: dH_b = dy_b Wd_s^T (tcgen05), then du, dg (and their column records)
     bf* dy_b = reinterpret_cast<bf*>(w + L.dy_b);
     float* dH = reinterpret_cast<float*>(w + L.dh_b);
     bf* DUG = reinterpret_cast<bf*>(w + L.dug);
-    bf* H_b = reinterpret_cast<bf*>(w + L.bh_b);
-    const unsigned gg = grid_for(static_cast<long long>(L.capr) * d / 8, 256, di.sm_count * 8);
-    twell::gather_rows_kernel<<<gg, 256, 0, s>>>(static_cast<const bf*>(x), ctx->backup_rows, ctx->n_backup, cap, d, x_b);
-    twell::gather_rows_kernel<<<gg, 256, 0, s>>>(static_cast<const bf*>(dy), ctx->backup_rows, ctx->n_backup, cap, d,
-                                                 dy_b);
-    if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    {  // dH_b = dy_b Wd_s^T  [cap, f] fp32
+    if (backup) {
+        const unsigned gg = grid_for(static_cast<long long>(L.capr) * d / 8, 256, di.sm_count * 8);
+        twell::gather_rows_kernel<<<gg, 256, 0, s>>>(static_cast<const bf*>(dy), ctx->backup_rows, ctx->n_backup, cap,
+                                                     d, dy_b);
+        if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
         twell::GemmArgs g{};
         g.M = cap;
         g.N = f;
@@ -1007,55 +1011,42 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
         st = launch_gemm<256, false, false, twell::Epi::StoreF32>(GemmOperand{dy_b, (int64_t)L.capr, d, d},
                                                                   GemmOperand{Wd_s, f, d, d}, nullptr, g, s);
         if (st != TWELL_OK) return st;
-    }
-    twell::backup_grad_kernel<<<grid_for(static_cast<long long>(L.capr) * L.f_pad, 256, di.sm_count * 8), 256, 0, s>>>(
-        static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), dH, ctx->n_backup, cap, f, L.f_pad,
-        l1_scale, DUG, H_b);
-    if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    {  // dx[rows] = [du_hi | dg_hi | du_lo | dg_lo] [Wu_s ; Wg_s ; Wu_s ; Wg_s]  (fp32 output), in
-       // kBackupSplits K ranges added up in order
-        float* dx_part = reinterpret_cast<float*>(w + L.dx_part);
-        twell::GemmArgs g{};
-        g.M = cap;
-        g.N = d;
-        g.K = 4 * L.f_pad;
-        g.M_dyn = ctx->n_backup;
-        g.kb_split = L.f_pad / 64;
-        g.k_splits = twell::kBackupSplits;
-        g.split_stride = static_cast<int64_t>(L.capr) * d;
-        g.out = dx_part;
-        g.ldo = d;
-        g.status = ctx->dev_status;
-        const GemmOperand B2{Wg_s, f, d, d};
-        st = launch_gemm<256, false, true, twell::Epi::StoreF32>(
-            GemmOperand{DUG, (int64_t)L.capr, 4 * L.f_pad, 4 * L.f_pad}, GemmOperand{Wu_s, f, d, d}, &B2, g, s);
-        if (st != TWELL_OK) return st;
-        twell::reduce_rows_kernel<float><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
-            dx_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows, dx);
+        twell::backup_grad_kernel<<<grid_for(static_cast<long long>(L.capr) * L.f_pad, 256, di.sm_count * 8), 256, 0,
+                                    s>>>(static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), dH,
+                                         ctx->n_backup, cap, f, L.f_pad, l1_scale, ctx->backup_rows, ccur, rec, DUG);
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     }
-    // dW += (backup rows)^T (...): A = [K = backup rows, M = f] (MN-major, the bf16 h / du / dg),
-    // B = [K, N = d] (MN-major, dy_b or x_b); fp32 accumulation into the sparse part's result
-    struct DW {
-        const void* A;
-        int64_t lda;
-        const void* B;
-        float* out;
-    } dws[3] = {{H_b, L.f_pad, dy_b, dWd_s}, {DUG, 4 * L.f_pad, x_b, dWu_s}, {DUG + L.f_pad, 4 * L.f_pad, x_b, dWg_s}};
-    for (const DW& q : dws) {
-        twell::GemmArgs g{};
-        g.M = f;
-        g.N = d;
-        g.K = cap;
-        g.K_dyn = ctx->n_backup;
-        g.out = q.out;
-        g.ldo = d;
-        g.status = ctx->dev_status;
-        st = launch_gemm<256, true, true, twell::Epi::AccumF32>(GemmOperand{q.A, (int64_t)L.capr, f, q.lda},
-                                                                GemmOperand{q.B, (int64_t)L.capr, d, d}, nullptr, g, s);
-        if (st != TWELL_OK) return st;
-    }
-    return TWELL_OK;
+
+    // 4. weight gradients of every kept entry, per hidden unit, in row order (overwrites dW)
+    twell::col_sort_kernel<<<grid_for(f, 128, di.sm_count * 4), 128, 0, s>>>(coff, f, rec);
+    twell::col_dw_kernel<0><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+        coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s);
+    twell::col_dw_kernel<1><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+        coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr);
+    if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
+    if (!backup) return TWELL_OK;
+
+    // 5. dx[rows] = [du_hi | dg_hi | du_lo | dg_lo] [Wu_s ; Wg_s ; Wu_s ; Wg_s] (fp32 output), in
+    //    kBackupSplits K ranges added up in order
+    float* dx_part = reinterpret_cast<float*>(w + L.dx_part);
+    twell::GemmArgs g{};
+    g.M = cap;
+    g.N = d;
+    g.K = 4 * L.f_pad;
+    g.M_dyn = ctx->n_backup;
+    g.kb_split = L.f_pad / 64;
+    g.k_splits = twell::kBackupSplits;
+    g.split_stride = static_cast<int64_t>(L.capr) * d;
+    g.out = dx_part;
+    g.ldo = d;
+    g.status = ctx->dev_status;
+    const GemmOperand B2{Wg_s, f, d, d};
+    st = launch_gemm<256, false, true, twell::Epi::StoreF32>(GemmOperand{DUG, (int64_t)L.capr, 4 * L.f_pad, 4 * L.f_pad},
+                                                             GemmOperand{Wu_s, f, d, d}, &B2, g, s);
+    if (st != TWELL_OK) return st;
+    twell::reduce_rows_kernel<float><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
+        dx_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows, dx);
+    return launch_status();
 }
 
 // Test export: C = A * B in fp32 from the tcgen05 GEMM with any operand major-ness.

@@ -214,7 +214,9 @@ TWELL_API twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const v
  *   dWg_s, dWu_s, dWd_s [f, d] (fp32, overwritten) = sum_r dg x_r, du x_r, h dy_r.
  * Gradients are written in fp32: a bf16 copy of dx rounds its largest element by up to 2^-8 of
  * itself, more than the accuracy the layer is held to.
- * Backup rows use dense tensor-core GEMMs for the same terms. Same shape limits as the forward.
+ * Backup rows take dh and dx from dense tensor-core GEMMs; the weight gradients of every kept
+ * entry, light or backup, are summed per hidden unit in row order (deterministic). Same shape
+ * limits as the forward.
  * ws: at least twell_workspace_bytes(TWELL_OP_HYBRID_BWD, N, d, f, 0, K, backup_cap) bytes; it
  * need not hold anything from the forward call (the context carries what the backward needs).
  */
