@@ -91,15 +91,22 @@ struct HybridWs {
 // ------------------------------------------------------------------------------------------
 // Routing
 
-// Per row (one warp): nnz from the TwELL counts; light rows written into the sparse block in
-// ascending column order and padded; heavy rows marked 0xFFFF. Per block: number of heavy rows.
-__global__ void route_rows_kernel(const float* __restrict__ vals, const uint8_t* __restrict__ idx,
-                                  const uint16_t* __restrict__ cnt, int N, int f, int nt, int K, float* __restrict__ ha,
-                                  uint16_t* __restrict__ hcol, uint16_t* __restrict__ hcnt, int* __restrict__ blk,
-                                  double* l1acc, int32_t* status)
+constexpr int kRouteWarps = 16;                          // warps of a routing block (8 rows each)
+constexpr int kRouteMaxTiles = (65535 + kHybTile - 1) / kHybTile;  // d_ff <= 65535
+
+// Per row (one warp): nnz from the TwELL counts, scanned into per-tile offsets in shared memory;
+// a light row (nnz <= K) is written into the sparse block in ascending column order, one entry per
+// lane at a time (its tile found by binary search over the offsets), and padded; a heavy row is
+// marked 0xFFFF. Per block: number of heavy rows.
+__global__ void __launch_bounds__(32 * kRouteWarps) route_rows_kernel(
+    const float* __restrict__ vals, const uint8_t* __restrict__ idx, const uint16_t* __restrict__ cnt, int N, int f,
+    int nt, int K, float* __restrict__ ha, uint16_t* __restrict__ hcol, uint16_t* __restrict__ hcnt,
+    int* __restrict__ blk, double* l1acc, int32_t* status)
 {
+    __shared__ int s_pref[kRouteWarps][kRouteMaxTiles + 1];
     __shared__ int s_heavy;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int* pref = s_pref[warp];
     if (threadIdx.x == 0) s_heavy = 0;
     if (blockIdx.x == 0 && threadIdx.x == 0 && l1acc != nullptr) *l1acc = 0.0;
     __syncthreads();
@@ -107,7 +114,6 @@ __global__ void route_rows_kernel(const float* __restrict__ vals, const uint8_t*
     for (int rr = warp; rr < kRouteRows; rr += nw) {
         const int r = r0 + rr;
         if (r >= N) break;
-        // per-tile exclusive offsets (warp scan in chunks of 32 tiles)
         int run = 0;
         for (int t0 = 0; t0 < nt; t0 += 32) {
             const int t = t0 + lane;
@@ -122,30 +128,33 @@ __global__ void route_rows_kernel(const float* __restrict__ vals, const uint8_t*
                 const int u = __shfl_up_sync(0xffffffffu, inc, o);
                 if (lane >= o) inc += u;
             }
-            const int total = __shfl_sync(0xffffffffu, inc, 31);
-            if (run + total <= K) {
-                // tile t's entries go to slots [run + inc - c, run + inc)
-                const size_t sb = (static_cast<size_t>(r) * nt + t) * kHybTile;
-                for (int k = 0; k < c; ++k) {
-                    const int slot = run + inc - c + k;
-                    ha[static_cast<size_t>(r) * K + slot] = vals[sb + k];
-                    hcol[static_cast<size_t>(r) * K + slot] = static_cast<uint16_t>(t * kHybTile + idx[sb + k]);
-                }
-            }
-            run += total;
+            if (t < nt) pref[t] = run + inc - c;
+            run += __shfl_sync(0xffffffffu, inc, 31);
         }
+        if (lane == 0) pref[nt] = run;
+        __syncwarp();
         if (run <= K) {
+            for (int p = lane; p < run; p += 32) {
+                int lo = 0, hi = nt;  // the last tile with pref[tile] <= p holds entry p
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (pref[mid] <= p) lo = mid;
+                    else hi = mid;
+                }
+                const size_t e = (static_cast<size_t>(r) * nt + lo) * kHybTile + (p - pref[lo]);
+                ha[static_cast<size_t>(r) * K + p] = vals[e];
+                hcol[static_cast<size_t>(r) * K + p] = static_cast<uint16_t>(lo * kHybTile + idx[e]);
+            }
             for (int k = run + lane; k < K; k += 32) {
                 ha[static_cast<size_t>(r) * K + k] = 0.0f;
                 hcol[static_cast<size_t>(r) * K + k] = 0;
             }
             if (lane == 0) hcnt[r] = static_cast<uint16_t>(run);
-        } else {
-            if (lane == 0) {
-                hcnt[r] = 0xFFFF;
-                atomicAdd(&s_heavy, 1);
-            }
+        } else if (lane == 0) {
+            hcnt[r] = 0xFFFF;
+            atomicAdd(&s_heavy, 1);
         }
+        __syncwarp();  // every lane is done with the offsets before the next row overwrites them
     }
     __syncthreads();
     if (threadIdx.x == 0) blk[blockIdx.x] = s_heavy;
@@ -153,7 +162,8 @@ __global__ void route_rows_kernel(const float* __restrict__ vals, const uint8_t*
 
 // Backup slots in ascending row order: block b's heavy rows start after all heavy rows of blocks
 // < b (their counts are summed directly, no inter-CTA waiting). For each heavy row with a slot
-// below cap: backup_rows[slot] = r, A_b[slot] = its dense ReLU(g) row (fp32), x_b[slot] = x_r.
+// below cap (one warp per row): backup_rows[slot] = r, A_b[slot] = its dense ReLU(g) row (fp32),
+// x_b[slot] = x_r.
 __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_t* __restrict__ idx,
                                     const uint16_t* __restrict__ cnt, const uint16_t* __restrict__ hcnt,
                                     const int* __restrict__ blk, int nblk, int N, int f, int nt, int cap,
@@ -162,7 +172,7 @@ __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_
                                     __nv_bfloat16* __restrict__ x_b, int32_t* status)
 {
     __shared__ int s_off, s_total, s_rank[kRouteRows];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     if (tid < 32) {
         int before = 0, total = 0;
         for (int b = tid; b < nblk; b += 32) {
@@ -194,17 +204,19 @@ __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_
         }
     }
     __syncthreads();
+    int seen = 0;  // heavy rows of this block met so far: the warp takes every nw-th
     for (int rr = 0; rr < kRouteRows; ++rr) {
         const int rank = s_rank[rr];
         if (rank < 0) continue;
+        if (seen++ % nw != warp) continue;
         const int slot = s_off + rank;
         if (slot >= cap) continue;
         const int r = blockIdx.x * kRouteRows + rr;
-        if (tid == 0) brows[slot] = r;
+        if (lane == 0) brows[slot] = r;
         float* arow = A_b + static_cast<size_t>(slot) * f;
-        for (int j = tid; j < f; j += blockDim.x) arow[j] = 0.0f;
-        __syncthreads();
-        for (int t = tid; t < nt; t += blockDim.x) {
+        for (int j = lane; j < f; j += 32) arow[j] = 0.0f;
+        __syncwarp();  // zeros before the kept values, across lanes
+        for (int t = lane; t < nt; t += 32) {
             const int c = cnt[static_cast<size_t>(r) * nt + t];
             const size_t sb = (static_cast<size_t>(r) * nt + t) * kHybTile;
             for (int k = 0; k < c && k < kHybTile; ++k) {
@@ -215,9 +227,8 @@ __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_
         if (x != nullptr) {
             const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * d);
             uint4* dst = reinterpret_cast<uint4*>(x_b + static_cast<size_t>(slot) * d);
-            for (int q = tid; q < d / 8; q += blockDim.x) dst[q] = src[q];
+            for (int q = lane; q < d / 8; q += 32) dst[q] = src[q];
         }
-        __syncthreads();
     }
     // zero x_b rows of the partly used last 64-row block (k padding of the backward GEMMs)
     if (blockIdx.x == 0 && x != nullptr) {
@@ -786,8 +797,8 @@ twell_status run_route(const twell::HybridWs& L, uint8_t* ws, int N, int f, int 
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(ws + L.tw_cnt);
     int* blk = reinterpret_cast<int*>(ws + L.blk);
     double* l1acc = reinterpret_cast<double*>(ws + L.l1acc);
-    twell::route_rows_kernel<<<L.nblk, 256, 0, s>>>(vals, idx, cnt, N, f, L.nt, K, static_cast<float*>(c->a), c->col,
-                                                    c->cnt, blk, l1acc, c->dev_status);
+    twell::route_rows_kernel<<<L.nblk, 32 * twell::kRouteWarps, 0, s>>>(
+        vals, idx, cnt, N, f, L.nt, K, static_cast<float*>(c->a), c->col, c->cnt, blk, l1acc, c->dev_status);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     twell::route_backup_kernel<<<L.nblk, 256, 0, s>>>(vals, idx, cnt, c->cnt, blk, L.nblk, N, f, L.nt, c->backup_cap, x,
                                                       d, c->backup_rows, c->n_backup, static_cast<float*>(c->A_b),
@@ -1128,9 +1139,9 @@ extern "C" twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_
     if (st != TWELL_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int nt = (f + twell::kHybTile - 1) / twell::kHybTile;
-    twell::route_rows_kernel<<<nblk, 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx, a->cnt, N, f, nt, K,
-                                                  static_cast<float*>(ctx->a), ctx->col, ctx->cnt, blk, nullptr,
-                                                  ctx->dev_status);
+    twell::route_rows_kernel<<<nblk, 32 * twell::kRouteWarps, 0, s>>>(
+        static_cast<const float*>(a->vals), a->idx, a->cnt, N, f, nt, K, static_cast<float*>(ctx->a), ctx->col, ctx->cnt,
+        blk, nullptr, ctx->dev_status);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     twell::route_backup_kernel<<<nblk, 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx, a->cnt, ctx->cnt, blk,
                                                     nblk, N, f, nt, ctx->backup_cap, nullptr, 8, ctx->backup_rows,
