@@ -32,7 +32,7 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_gate_pack", "twell_ffn_fused_fwd", "twell_ffn_union_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
-           "twell_read_status", "twell_status_string", "twell_device_info")
+           "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe")
 
 
 class TwellError(RuntimeError):
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH):
                                              sz, vp, vp]),
                 "twell_ffn_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
                                              sz, vp, vp]),
+                "twell_wait_probe": (st, [i32, i32, vp, vp]),
                 "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
                                           ctypes.POINTER(_Hybrid), vp, vp, sz, vp]),
                 "twell_hybrid_bwd": (st, [vp, vp, vp, vp, ctypes.POINTER(_Hybrid), vp, i32, i32, i32, ctypes.c_float,
@@ -175,6 +176,14 @@ def twell_read_status(status: Optional[torch.Tensor] = None, stream=None, reset:
     if reset and code != TWELL_OK:
         status.zero_()
     return code
+
+
+def twell_wait_probe(arrive: bool, limit_ms: int, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Run the library's bounded mbarrier wait on its own (test export): with arrive=False it runs
+    out after limit_ms and records TWELL_ERR_TIMEOUT in the status word."""
+    _check(load().twell_wait_probe(1 if arrive else 0, int(limit_ms), _ptr(status if status is not None else
+                                                                             status_buffer()), _stream(stream)),
+           "twell_wait_probe")
 
 
 def check_device_status(where: str = "device", status: Optional[torch.Tensor] = None, stream=None):

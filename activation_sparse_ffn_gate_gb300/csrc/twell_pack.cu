@@ -218,3 +218,30 @@ extern "C" twell_status twell_gather_rows(const void* src, int32_t n_src, const 
         static_cast<const uint4*>(src), n_src, rows, n, chunks, static_cast<uint4*>(dst), dev_status);
     return launch_status();
 }
+
+// ------------------------------------------------------------------------------------------
+// The bounded wait on its own (see twell_wait_probe in include/twell.h).
+
+namespace twell {
+namespace {
+__global__ void wait_probe_kernel(int arrive, uint64_t limit_ns, int32_t* status)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (arrive && threadIdx.x == 0) mbar_arrive(&bar);
+    wait_bounded(&bar, 0u, nullptr, status, limit_ns);
+}
+}  // namespace
+}  // namespace twell
+
+extern "C" twell_status twell_wait_probe(int32_t arrive, int32_t limit_ms, int32_t* dev_status, void* stream)
+{
+    if (dev_status == nullptr || limit_ms < 1 || limit_ms > 10000) return TWELL_ERR_INVALID;
+    twell::wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        arrive != 0, static_cast<uint64_t>(limit_ms) * 1000000ull, dev_status);
+    return launch_status();
+}

@@ -292,6 +292,15 @@ TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t 
 TWELL_API twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_t K,
                                                   const twell_hybrid* ctx, void* stream);
 
+/* The bounded mbarrier wait every kernel of the library uses, on its own: one warp initialises an
+ * mbarrier that expects one arrival and waits on it with a limit of limit_ms milliseconds. With
+ * arrive != 0 the warp's lane 0 arrives first and the wait ends at once; with arrive == 0 nothing
+ * ever arrives, the wait gives up after limit_ms, records TWELL_ERR_TIMEOUT in *dev_status and
+ * the kernel returns, leaving the context usable. This is how failure detection is tested without
+ * hanging or faulting a GPU: the limit of the real kernels' waits (TWELL_WAIT_LIMIT_MS, 2 s by
+ * default) takes the same path. limit_ms in [1, 10000], else TWELL_ERR_INVALID. */
+TWELL_API twell_status twell_wait_probe(int32_t arrive, int32_t limit_ms, int32_t* dev_status, void* stream);
+
 /* C[M, N] = A * B in fp32 from the tcgen05 GEMM used by the hybrid backup rows, bf16 operands:
  * A is [M, K] row-major (a_mn = 0) or [K, M] row-major (a_mn = 1); B is [N, K] row-major
  * (b_mn = 0) or [K, N] row-major (b_mn = 1); C is [M, N] row-major. N and the contiguous

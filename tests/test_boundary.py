@@ -172,3 +172,9 @@ def test_union_rejects_bad_arguments(lib):
     assert call(N=5) == 1  # the TwELL describes 4 rows
     assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0
     assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
+
+
+def test_wait_probe_rejects_bad_limits(lib):
+    assert lib.twell_wait_probe(0, 0, STATUS, None) == 1
+    assert lib.twell_wait_probe(0, 10001, STATUS, None) == 1
+    assert lib.twell_wait_probe(1, 50, None, None) == 1
