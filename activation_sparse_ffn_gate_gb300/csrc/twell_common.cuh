@@ -265,6 +265,13 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
         ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// Start bringing `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 (no completion
+// to wait for): a row needed a little later then comes from L2 instead of HBM.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;

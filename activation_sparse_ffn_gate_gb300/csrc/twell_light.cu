@@ -92,6 +92,8 @@ struct LightStream {
         nrow = r < a.N ? r : a.N;
         nn = r < a.N ? static_cast<int>(a.hcnt[r]) : 0;
         load_segment(a, r, 0, nj, na, nu);
+        // the row vector of that row, copied into a slot a row from now, on its way from HBM to L2
+        if (lane == 0 && r < a.N) bulk_prefetch_l2(a.v + static_cast<size_t>(r) * a.d, static_cast<uint32_t>(a.d) * 2u);
     }
     __device__ void take_ticket(const LightArgs& a)
     {
