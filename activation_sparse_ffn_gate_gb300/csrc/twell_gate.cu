@@ -86,6 +86,13 @@ extern "C" twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t
     g.status = dev_status;
     GemmOperand A{x, N, d, d};
     GemmOperand B{Wg_s, f, d, d};
+    // A small batch (decoding a few tokens) fills one or two 128-row tiles: 128 x T tiles on single
+    // SMs spread d_ff over more SMs and pad M to 128 rows instead of 256 (the 256 x 256 pair tiles
+    // left the decode gate tensor-bound on padding rows, 44 SMs busy at N = 8).
+    if (N <= 256) {
+        if (T == 64) return launch_gemm<64, false, false, twell::Epi::PackTwell>(A, B, nullptr, g, s);
+        if (T == 128) return launch_gemm<128, false, false, twell::Epi::PackTwell>(A, B, nullptr, g, s);
+    }
     return launch_gemm<256, false, false, twell::Epi::PackTwell, true>(A, B, nullptr, g, s);
 }
 

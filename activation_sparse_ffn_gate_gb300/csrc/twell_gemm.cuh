@@ -60,6 +60,8 @@ struct GemmArgs {
     int kb_split;            // B source period in k-blocks: block kb reads map (kb / kb_split) & 1 at
                              // k-block kb % kb_split (one map: kb_split larger than every kb)
     int k_splits;            // split K into this many ranges (0 or 1: no split; StoreF32 only)
+    int a_box_rows;          // rows of A a stage loads (0: the whole 128-row tile); fewer when M is small,
+                             // the tile's other rows then hold stale data whose products are never stored
     int64_t split_stride;    // elements between the partial outputs of consecutive splits
     void* out;               // epilogue output
     int64_t ldo;             // its leading dimension (elements)
@@ -197,7 +199,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d_pair(a, &tmA, k0, m0, fb);
                         tma_load_2d_pair(b, &tmB, k0, n0 + crank * (BN / 2), fb);
                     } else {
-                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        mbar_arrive_expect_tx(&full[stage], g.a_box_rows > 0 && !A_MN
+                                                                ? static_cast<uint32_t>(g.a_box_rows) * kBK * 2 + C::B_BYTES
+                                                                : C::STAGE_BYTES);
                         if constexpr (!A_MN) {
                             tma_load_2d(a, &tmA, k0, m0, &full[stage]);
                         } else {
@@ -464,9 +468,11 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return TWELL_OK;
     CUtensorMap ta, tb, tb2;
     twell_status st;
-    // A: K-major box = 64 (K) x 128 (M); MN-major box = 64 (M) x 64 (K), two per stage.
+    // A: K-major box = 64 (K) x 128 (M), or x M rounded up to 8 when M is below 128 (one tile, most
+    // of whose rows would be zero fill); MN-major box = 64 (M) x 64 (K), two per stage.
+    g.a_box_rows = (!PAIR && !A_MN && g.M_dyn == nullptr && g.M <= twell::kBM - 8) ? (g.M + 7) / 8 * 8 : 0;
     st = A_MN ? make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, 64)
-              : make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, twell::kBM);
+              : make_tmap_bf16(&ta, A.ptr, A.cols, A.rows, A.ld, 64, g.a_box_rows > 0 ? g.a_box_rows : twell::kBM);
     if (st != TWELL_OK) return st;
     // B: K-major box = 64 (K) x BN (N), or BN/2 rows per CTA with PAIR; MN-major box = 64 (N) x
     // 64 (K), BN/64 per stage.

@@ -104,8 +104,11 @@ def test_pack_empty_batch(cuda_dev):
 
 @pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("T", [64, 128, 256])
-@pytest.mark.parametrize("N,d,f", [(300, 136, 700), (257, 256, 1024), (64, 2048, 5632)])
+@pytest.mark.parametrize("N,d,f", [(300, 136, 700), (257, 256, 1024), (64, 2048, 5632), (1, 512, 1000),
+                                   (200, 256, 1024)])
 def test_gate_pack_integer_bit_exact(cuda_dev, T, N, d, f, vals_dtype):
+    """Bit-exact TwELL pack from the gate GEMM epilogue, on SM-pair 256 x 256 tiles (N > 256) and on
+    single-SM 128 x T tiles (batches of up to 256 tokens)."""
     x, W = _int_layer(N, d, f, seed=T + N)
     tw = binding.twell_gate_pack(_to(cuda_dev, x), _to(cuda_dev, W), T, vals_dtype=vals_dtype)
     G = oracle.gate(x, W)  # exact integers
