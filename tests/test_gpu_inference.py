@@ -308,10 +308,12 @@ def test_streamed_batches_match_ffn_forward(cuda_dev):
 
 # ------------------------------------------------------------------------------------------ union path
 
+@pytest.mark.parametrize("N", [7, 300])
 @pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
-def test_union_small_ragged(cuda_dev, vals_dtype):
-    """twell_ffn_union_fwd on an oracle-packed TwELL with a ragged last tile (d_ff = 1000)."""
-    L = synthetic.uniform_layer(300, 512, 1000, 128, 0.05, seed=31)
+def test_union_small_ragged(cuda_dev, vals_dtype, N):
+    """twell_ffn_union_fwd on an oracle-packed TwELL with a ragged last tile (d_ff = 1000), for a
+    batch that fills part of one 128-row tile and for one that spans three."""
+    L = synthetic.uniform_layer(N, 512, 1000, 128, 0.05, seed=31 + N)
     G = oracle.gate(L.x, L.Wg_s)
     Ga = np.where(G > 0, G, 0.0)
     Gs = synthetic.round_bf16_np(Ga.astype(np.float32)) if vals_dtype == torch.bfloat16 else Ga.astype(np.float32)
