@@ -1030,9 +1030,9 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
 
     // 4. weight gradients of every kept entry, per hidden unit, in row order (overwrites dW)
     twell::col_sort_kernel<<<grid_for(f, 128, di.sm_count * 4), 128, 0, s>>>(coff, f, rec);
-    twell::col_dw_kernel<0><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+    twell::col_dw_kernel<0><<<f, threads, 0, s>>>(
         coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s);
-    twell::col_dw_kernel<1><<<grid_for(f, 1, di.sm_count * 8), threads, 0, s>>>(
+    twell::col_dw_kernel<1><<<f, threads, 0, s>>>(
         coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr);
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     if (!backup) return TWELL_OK;
