@@ -324,6 +324,31 @@ def test_union_small_ragged(cuda_dev, vals_dtype, N):
     assert_close(y, oracle.twell_walk(vals, idx, cnt, L.T, L.x, L.Wu_s, L.Wd_s), f"union {vals_dtype}")
 
 
+@pytest.mark.parametrize("T", [64, 256])
+def test_union_other_tile_widths(cuda_dev, T):
+    """The union path reads TwELL tiles of 64 and 256 columns (d_ff 1000: a ragged last tile)."""
+    L = synthetic.uniform_layer(200, 512, 1000, T, 0.04, seed=T + 5)
+    t = L.torch_inputs(cuda_dev)
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=T, path="union")
+    assert_close(y.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"union T={T}")
+
+
+def test_streamed_batches_union_path(cuda_dev):
+    """StreamedFFN on the union path returns what ffn_forward(path="union") returns."""
+    L = synthetic.uniform_layer(3 * 128, 512, 1024, 128, 0.05, seed=43)
+    t = L.torch_inputs(cuda_dev)
+    pipe = binding.StreamedFFN(t["Wg_s"], t["Wu_s"], t["Wd_s"], 128, T=L.T, path="union")
+    xs = [t["x"][128 * i:128 * (i + 1)].cpu().pin_memory() for i in range(3)]
+    ys = [torch.empty((128, L.d), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    for xh, yh in zip(xs, ys):
+        pipe.submit(xh, yh)
+    torch.cuda.synchronize()
+    for i in range(3):
+        ref = binding.ffn_forward(t["x"][128 * i:128 * (i + 1)].contiguous(), t["Wg_s"], t["Wu_s"], t["Wd_s"],
+                                  T=L.T, path="union")
+        assert torch.equal(ys[i], ref.cpu()), i
+
+
 @pytest.mark.parametrize("p", [0.01, 0.05, 0.5])
 def test_union_sweep_shapes_end_to_end_sampled(cuda_dev, p):
     """The union path end to end (gate + pack, then the two GEMMs) at the sweep's shapes
