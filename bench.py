@@ -45,6 +45,9 @@ def _args():
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-train", action="store_true", help="skip the hybrid training-step measurement")
     p.add_argument("--train-steps", type=int, default=20)
+    p.add_argument("--config", type=int, choices=[1, 2], default=1,
+                   help="workload of the main line: 1 = the 1.5B-like layer (default), 2 = the 2B-like layer "
+                        "(N=16384, d_model 2560, d_ff 6912, lognormal per-token density; no dead-column step)")
     p.add_argument("--train-only", action="store_true",
                    help="only the hybrid training step against the dense cuBLAS step (one JSON line)")
     p.add_argument("--sweep", action="store_true",
@@ -245,7 +248,8 @@ def run_ours(a, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    L = synthetic.layer_1p5b(seed=1 + rank)  # every rank its own batch (weak scaling)
+    # every rank its own batch (weak scaling)
+    L = synthetic.layer_1p5b(seed=1 + rank) if a.config == 1 else synthetic.layer_2b(seed=2 + rank)
     t = L.torch_inputs(dev)
     x, Wg, Wu, Wd = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"]
     N, d, f, T = L.N, L.d, L.f, L.T
@@ -333,12 +337,14 @@ def run_ours(a, rank, world):
     if mf >= mg:
         ach = fused_bytes / (mf * 1e-3) / 1e9
         roof = {"kernel": "twell_ffn_fused_fwd", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": _traffic("fused"),
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": _traffic("fused") if a.config == 1 else None,
                 "algorithmic_bytes": fused_bytes, "ms_per_launch": mf, "peak_kind": peak_kind + " hbm_gbs"}
     else:
         ach = gate_flops / (mg * 1e-3) / 1e12
         roof = {"kernel": "twell_gate_pack", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": _traffic("gate"),
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                "traffic": _traffic("gate") if a.config == 1 else None,
                 "algorithmic_flops": gate_flops, "ms_per_launch": mg, "peak_kind": peak_kind + " bf16_tflops (burst)"}
 
     # ---- dense cuBLAS bf16 FFN of the same shape (best of two formulations)
@@ -409,45 +415,47 @@ def run_ours(a, rank, world):
     e2e_ms = s0.elapsed_time(s1) / e2e_steps
     binding.check_device_status("e2e", status)
 
-    # ---- dead-column compaction: live units from a separate calibration batch, the same step on
-    # the compacted weights (the bench batch's y must come out bit-identical)
-    x_cal = torch.from_numpy(synthetic.calibration_tokens(L, N, seed=1000 + rank)).to(dev, torch.bfloat16)
-    counts = binding.twell_column_activity(binding.twell_gate_pack(x_cal, Wg, T, status=status), status=status)
-    live = binding.live_columns(counts)
-    Wg_c, Wu_c, Wd_c = binding.compact_weights(Wg, Wu, Wd, live, status=status)
-    f_c = live.numel()
-    packed_c = binding.TwELL.empty(N, f_c, T, torch.float32, dev)
-    y_c = torch.empty_like(y)
-    del x_cal
-    binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
-    binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
-    binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream)
-    binding.twell_ffn_fused_fwd(x, Wu_c, Wd_c, packed_c, y=y_c, status=status, stream=stream)
-    torch.cuda.synchronize()
-    identical = bool(torch.equal(y, y_c))
-    c_steps = max(10, min(a.steps, 200))
-    cg, cf = [], []
-    for _ in range(c_steps):
-        flush.fill_(1)
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        e0.record(stream)
+    # ---- dead-column compaction (the 1.5B-like layer: 30% of its units never fire; the 2B-like layer
+    # has none by construction)
+    compacted = None
+    if a.config == 1:
+        x_cal = torch.from_numpy(synthetic.calibration_tokens(L, N, seed=1000 + rank)).to(dev, torch.bfloat16)
+        counts = binding.twell_column_activity(binding.twell_gate_pack(x_cal, Wg, T, status=status), status=status)
+        live = binding.live_columns(counts)
+        Wg_c, Wu_c, Wd_c = binding.compact_weights(Wg, Wu, Wd, live, status=status)
+        f_c = live.numel()
+        packed_c = binding.TwELL.empty(N, f_c, T, torch.float32, dev)
+        y_c = torch.empty_like(y)
+        del x_cal
+        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
         binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream)
-        e1.record(stream)
         binding.twell_ffn_fused_fwd(x, Wu_c, Wd_c, packed_c, y=y_c, status=status, stream=stream)
-        e2.record(stream)
-        cg.append((e0, e1))
-        cf.append((e1, e2))
-    torch.cuda.synchronize()
-    binding.check_device_status("compacted", status)
-    mcg = statistics.median(u.elapsed_time(v) for u, v in cg)
-    mcf = statistics.median(u.elapsed_time(v) for u, v in cf)
-    compacted = {"live_cols": f_c, "dead_cols": f - f_c, "calibration": f"{N} other tokens (seed {1000 + rank})",
-                 "ms_gate_pack": mcg, "ms_fused": mcf, "ms_per_step": mcg + mcf,
-                 "tokens_per_s": N / ((mcg + mcf) * 1e-3), "y_bit_identical": identical,
-                 "speedup_vs_dense": (dense["ms"] / (mcg + mcf)) if dense else None,
-                 "note": "dead-column compaction (units that never fired in the calibration batch are dropped "
-                         "from Wg_s, Wu_s, Wd_s once); medians over the steps, L2 flushed"}
-    del packed_c, Wg_c, Wu_c, Wd_c
+        torch.cuda.synchronize()
+        identical = bool(torch.equal(y, y_c))
+        c_steps = max(10, min(a.steps, 200))
+        cg, cf = [], []
+        for _ in range(c_steps):
+            flush.fill_(1)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream)
+            e1.record(stream)
+            binding.twell_ffn_fused_fwd(x, Wu_c, Wd_c, packed_c, y=y_c, status=status, stream=stream)
+            e2.record(stream)
+            cg.append((e0, e1))
+            cf.append((e1, e2))
+        torch.cuda.synchronize()
+        binding.check_device_status("compacted", status)
+        mcg = statistics.median(u.elapsed_time(v) for u, v in cg)
+        mcf = statistics.median(u.elapsed_time(v) for u, v in cf)
+        compacted = {"live_cols": f_c, "dead_cols": f - f_c, "calibration": f"{N} other tokens (seed {1000 + rank})",
+                     "ms_gate_pack": mcg, "ms_fused": mcf, "ms_per_step": mcg + mcf,
+                     "tokens_per_s": N / ((mcg + mcf) * 1e-3), "y_bit_identical": identical,
+                     "speedup_vs_dense": (dense["ms"] / (mcg + mcf)) if dense else None,
+                     "note": "dead-column compaction (units that never fired in the calibration batch are dropped "
+                             "from Wg_s, Wu_s, Wd_s once); medians over the steps, L2 flushed"}
+        del packed_c, Wg_c, Wu_c, Wd_c
 
     train = None
     if not a.no_train:
