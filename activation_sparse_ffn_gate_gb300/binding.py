@@ -32,7 +32,8 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_gate_pack", "twell_ffn_fused_fwd", "twell_ffn_union_fwd", "twell_hybrid_fwd", "twell_hybrid_bwd", "twell_unpack",
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
-           "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe")
+           "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe",
+           "twell_ffn_fused_fwd_f16down", "twell_convert_f16")
 
 
 class TwellError(RuntimeError):
@@ -81,6 +82,9 @@ def load(path: str = LIB_PATH):
                 "twell_ffn_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
                                              sz, vp, vp]),
                 "twell_wait_probe": (st, [i32, i32, vp, vp]),
+                "twell_ffn_fused_fwd_f16down": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
+                                                     vp, vp]),
+                "twell_convert_f16": (st, [vp, vp, ctypes.c_int64, vp, vp]),
                 "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
                                           ctypes.POINTER(_Hybrid), vp, vp, sz, vp]),
                 "twell_hybrid_bwd": (st, [vp, vp, vp, vp, ctypes.POINTER(_Hybrid), vp, i32, i32, i32, ctypes.c_float,
@@ -259,6 +263,38 @@ def twell_ffn_fused_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
                                       _ptr(status if status is not None else status_buffer(x.device)),
                                       _stream(stream)),
            "twell_ffn_fused_fwd")
+    return y
+
+
+def twell_convert_f16(src: torch.Tensor, out: Optional[torch.Tensor] = None, status=None,
+                      stream=None) -> torch.Tensor:
+    """A bf16 tensor converted to fp16 by the library (e.g. Wd_s for twell_ffn_fused_fwd_f16down)."""
+    if src.dtype != torch.bfloat16 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous bf16 tensor")
+    out = out if out is not None else torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    _check(load().twell_convert_f16(_ptr(src), _ptr(out), src.numel(),
+                                    _ptr(status if status is not None else status_buffer(src.device)),
+                                    _stream(stream)),
+           "twell_convert_f16")
+    return out
+
+
+def twell_ffn_fused_fwd_f16down(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tensor, a: TwELL,
+                                y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                                stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """twell_ffn_fused_fwd with Wd_s given in fp16 (twell_convert_f16) and the down projection in fp16."""
+    if Wd16_s.dtype != torch.float16:
+        raise ValueError("Wd16_s must be fp16")
+    N, d = x.shape
+    f = Wu_s.shape[0]
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    ws = ws if ws is not None else fused_workspace(N, d, f, x.device, stream)
+    s = a.c_struct()
+    _check(load().twell_ffn_fused_fwd_f16down(_ptr(x), _ptr(Wu_s), _ptr(Wd16_s), ctypes.byref(s), N, d, f,
+                                              _ptr(y), _ptr(ws), ws.numel(),
+                                              _ptr(status if status is not None else status_buffer(x.device)),
+                                              _stream(stream)),
+           "twell_ffn_fused_fwd_f16down")
     return y
 
 

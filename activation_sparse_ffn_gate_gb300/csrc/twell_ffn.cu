@@ -40,6 +40,8 @@
 // in the status word as TWELL_ERR_DEVICE_CHECK and contributes nothing, and every access stays
 // inside the TwELL's own arrays.
 #include "twell_common.cuh"
+#include <cuda_fp16.h>
+
 #include "twell_mma.cuh"
 
 namespace twell {
@@ -79,6 +81,7 @@ struct RowArgs {
     const SplitItem* items = nullptr;  // [item_cap]
     HeavyRow* heavy = nullptr;         // [item_cap], indexed by a split row's first item
     float* part = nullptr;             // [item_cap, d] fp32 partial y_r of each item
+    int f16down = 0;                   // Wd holds fp16 bits (ffn_bulk_kernel only)
 };
 
 // Rows with more than `seg` nonzeros are cut into ceil(nnz / seg) items of near-equal length,
@@ -912,8 +915,10 @@ struct __align__(16) SlotDesc {
 };
 
 
-// NS: 256-column spans of d_model; S: ring slots per warp; WPC: warps per CTA.
-template <int NS, int S, int WPC>
+// NS: 256-column spans of d_model; S: ring slots per warp; WPC: warps per CTA. F16DOWN: Wd_s holds
+// fp16 bits and the down projection is one fp16 product per chunk, with h rounded once to fp16
+// (11 significant bits), instead of two bf16 products with h as a bf16 hi + lo pair.
+template <int NS, int S, int WPC, bool F16DOWN = false>
 __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__nv_bfloat16> a)
 {
     using E = __nv_bfloat16;
@@ -1032,20 +1037,32 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
         u += __shfl_xor_sync(0xffffffffu, u, 4);
         u += __shfl_xor_sync(0xffffffffu, u, 9);
         u += __shfl_xor_sync(0xffffffffu, u, 18);
-        // h = hi + lo, both bf16: the pair carries h to ~16 significant bits
         const float h = D.a * u;
-        const uint32_t hi2 = bf16x2_rn(h, h);
-        const float lo = h - __uint_as_float(hi2 << 16);
-        const uint32_t hd = hi2 & hmask, ld = bf16x2_rn(lo, lo) & hmask;
-        // down projection: y_r += h * Wd_s[j]
+        if constexpr (F16DOWN) {
+            // down projection y_r += h * Wd_s[j], h and the row in fp16
+            const uint32_t hd = f16x2_rn(h, h) & hmask;
 #pragma unroll
-        for (int q = 0; q < NS; ++q) {
-            uint32_t w[4];
-            ldsm_x4_trans(w, su + L::kRow + 512u * q);
-            mma_bf16(yacc[2 * q], hd, 0u, 0u, hd, w[0], w[1]);
-            mma_bf16(yacc[2 * q + 1], hd, 0u, 0u, hd, w[2], w[3]);
-            mma_bf16(yacc[2 * q], ld, 0u, 0u, ld, w[0], w[1]);
-            mma_bf16(yacc[2 * q + 1], ld, 0u, 0u, ld, w[2], w[3]);
+            for (int q = 0; q < NS; ++q) {
+                uint32_t w[4];
+                ldsm_x4_trans(w, su + L::kRow + 512u * q);
+                mma_f16(yacc[2 * q], hd, 0u, 0u, hd, w[0], w[1]);
+                mma_f16(yacc[2 * q + 1], hd, 0u, 0u, hd, w[2], w[3]);
+            }
+        } else {
+            // h = hi + lo, both bf16: the pair carries h to ~16 significant bits
+            const uint32_t hi2 = bf16x2_rn(h, h);
+            const float lo = h - __uint_as_float(hi2 << 16);
+            const uint32_t hd = hi2 & hmask, ld = bf16x2_rn(lo, lo) & hmask;
+            // down projection: y_r += h * Wd_s[j]
+#pragma unroll
+            for (int q = 0; q < NS; ++q) {
+                uint32_t w[4];
+                ldsm_x4_trans(w, su + L::kRow + 512u * q);
+                mma_bf16(yacc[2 * q], hd, 0u, 0u, hd, w[0], w[1]);
+                mma_bf16(yacc[2 * q + 1], hd, 0u, 0u, hd, w[2], w[3]);
+                mma_bf16(yacc[2 * q], ld, 0u, 0u, ld, w[0], w[1]);
+                mma_bf16(yacc[2 * q + 1], ld, 0u, 0u, ld, w[2], w[3]);
+            }
         }
         if (D.flags & kLast) {
             if (D.part == kWholeRow) {
@@ -1203,10 +1220,10 @@ static twell_status launch_mma(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
     return launch_persistent(ffn_mma_kernel<CPLX, R>, a, MmaSmem<CPLX>::cta_bytes(a.nt), kCtaWarps, s);
 }
 
-template <int NS, int S, int WPC>
-static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
+template <int NS, int S, int WPC, bool F16DOWN>
+static twell_status launch_bulk_k(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
 {
-    auto kern = ffn_bulk_kernel<NS, S, WPC>;
+    auto kern = ffn_bulk_kernel<NS, S, WPC, F16DOWN>;
     const size_t smem = static_cast<size_t>(WPC) * BulkLayout<NS>::warp_bytes(S, a.nt);
     twell_host::DevInfo di;
     if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
@@ -1239,6 +1256,12 @@ static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
     return twell_host::launch_status();
 }
 
+template <int NS, int S, int WPC>
+static twell_status launch_bulk(const RowArgs<__nv_bfloat16>& a, cudaStream_t s)
+{
+    return a.f16down ? launch_bulk_k<NS, S, WPC, true>(a, s) : launch_bulk_k<NS, S, WPC, false>(a, s);
+}
+
 // Kernel and layout for d_model = nchunks 16-byte chunks: the tensor-core kernel where it applies,
 // else chunks per lane (CPL) and warps per row (G) of the general kernel.
 template <typename E>
@@ -1266,8 +1289,9 @@ static twell_status run_fused(const RowArgs<E>& a, cudaStream_t s)
             case 12: st = launch_bulk<12, 2, 6>(a, s); break;
             default: break;
             }
-            if (st != TWELL_ERR_UNSUPPORTED) return st;  // else: ring too large for shared memory
+            if (st != TWELL_ERR_UNSUPPORTED || a.f16down) return st;  // else: ring too large for shared memory
         }
+        if (a.f16down) return TWELL_ERR_UNSUPPORTED;  // the other kernels read Wd as bf16
         if (a32 && a.d % 256 == 0) {
             switch (a.d / 256) {
             case 2: return launch_mma<2, 4>(a, s);
@@ -1342,4 +1366,62 @@ extern "C" twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, con
                             static_cast<int*>(ws), dev_status, N, d, f, a->tile, nt, d / twell::Elem<float>::kPer16B, 0};
     p.wait_ns = twell_host::wait_limit_ns();
     return twell::run_fused(p, s);
+}
+
+extern "C" twell_status twell_ffn_fused_fwd_f16down(const void* x, const void* Wu_s, const void* Wd16_s,
+                                                    const twell_packed* a, int32_t N, int32_t d, int32_t f, void* y,
+                                                    void* ws, size_t ws_bytes, int32_t* dev_status, void* stream)
+{
+    if (Wu_s == nullptr || Wd16_s == nullptr || a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if ((x == nullptr || y == nullptr) && N != 0) return TWELL_ERR_INVALID;
+    if (N < 0 || d <= 0 || f <= 0 || d % 8 != 0) return TWELL_ERR_INVALID;
+    if (!dtype_ok(a->dtype)) return TWELL_ERR_UNSUPPORTED;
+    if (d % 256 != 0 || d < 512 || d > 3072) return TWELL_ERR_UNSUPPORTED;
+    twell_status st = check_packed(a, N, f, a->tile, a->dtype);
+    if (st != TWELL_OK) return st;
+    const int nt = (f + a->tile - 1) / a->tile;
+    if (nt > twell::kMaxTiles) return TWELL_ERR_UNSUPPORTED;
+    if (N == 0) return TWELL_OK;
+    if (ws == nullptr || ws_bytes < twell_workspace_bytes(TWELL_OP_FFN_FUSED_FWD, N, d, f, a->tile, 0, 0))
+        return TWELL_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd16_s) || !aligned16(y) || !aligned16(ws))
+        return TWELL_ERR_INVALID;
+    using bf = __nv_bfloat16;
+    twell::RowArgs<bf> p{static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd16_s),
+                         a->vals, a->idx, a->cnt, static_cast<bf*>(y), static_cast<int*>(ws), dev_status,
+                         N, d, f, a->tile, nt, d / twell::Elem<bf>::kPer16B, a->dtype == TWELL_BF16 ? 1 : 0};
+    p.wait_ns = twell_host::wait_limit_ns();
+    p.f16down = 1;
+    set_split_ws(p, ws, N, d, f);
+    return twell::run_fused(p, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// bf16 -> fp16, one element per thread in a grid-stride loop. A finite value that leaves the fp16
+// range (|w| > 65504) is recorded as TWELL_ERR_DEVICE_CHECK; it is stored as the infinity it rounds to.
+__global__ void convert_f16_kernel(const __nv_bfloat16* __restrict__ src, __half* __restrict__ dst, size_t n,
+                                   int32_t* status)
+{
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const float v = __bfloat162float(src[i]);
+        const __half h = __float2half_rn(v);
+        if (isfinite(v) && __hisinf(h)) twell::report(status, TWELL_ERR_DEVICE_CHECK);
+        dst[i] = h;
+    }
+}
+}  // namespace
+
+extern "C" twell_status twell_convert_f16(const void* src, void* dst, int64_t n, int32_t* dev_status, void* stream)
+{
+    if (n < 0 || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (n == 0) return TWELL_OK;
+    if (src == nullptr || dst == nullptr) return TWELL_ERR_INVALID;
+    twell_host::DevInfo di;
+    if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    const long long blocks_needed = (n + 255) / 256;
+    const int grid = static_cast<int>(blocks_needed < 8ll * di.sm_count ? blocks_needed : 8ll * di.sm_count);
+    convert_f16_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(src), static_cast<__half*>(dst), static_cast<size_t>(n), dev_status);
+    return twell_host::launch_status();
 }

@@ -44,6 +44,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-train", action="store_true", help="skip the hybrid training-step measurement")
+    p.add_argument("--no-f16down", action="store_true",
+                   help="skip the sub-entry of the walk with its down projection in fp16")
     p.add_argument("--train-steps", type=int, default=20)
     p.add_argument("--config", type=int, choices=[1, 2], default=1,
                    help="workload of the main line: 1 = the 1.5B-like layer (default), 2 = the 2B-like layer "
@@ -417,7 +419,25 @@ def run_ours(a, rank, world):
 
     # ---- dead-column compaction (the 1.5B-like layer: 30% of its units never fire; the 2B-like layer
     # has none by construction)
+    def medians_gate_walk(gate, walk, n):
+        """Median gate + pack and walk times over n steps, L2 flushed before each."""
+        cg, cf = [], []
+        for _ in range(n):
+            flush.fill_(1)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            gate()
+            e1.record(stream)
+            walk()
+            e2.record(stream)
+            cg.append((e0, e1))
+            cf.append((e1, e2))
+        torch.cuda.synchronize()
+        return (statistics.median(u.elapsed_time(v) for u, v in cg),
+                statistics.median(u.elapsed_time(v) for u, v in cf))
+
     compacted = None
+    Wu_c = Wd_c = Wg_c = packed_c = None
     if a.config == 1:
         x_cal = torch.from_numpy(synthetic.calibration_tokens(L, N, seed=1000 + rank)).to(dev, torch.bfloat16)
         counts = binding.twell_column_activity(binding.twell_gate_pack(x_cal, Wg, T, status=status), status=status)
@@ -434,28 +454,54 @@ def run_ours(a, rank, world):
         torch.cuda.synchronize()
         identical = bool(torch.equal(y, y_c))
         c_steps = max(10, min(a.steps, 200))
-        cg, cf = [], []
-        for _ in range(c_steps):
-            flush.fill_(1)
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            e0.record(stream)
-            binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream)
-            e1.record(stream)
-            binding.twell_ffn_fused_fwd(x, Wu_c, Wd_c, packed_c, y=y_c, status=status, stream=stream)
-            e2.record(stream)
-            cg.append((e0, e1))
-            cf.append((e1, e2))
-        torch.cuda.synchronize()
+        mcg, mcf = medians_gate_walk(
+            lambda: binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream),
+            lambda: binding.twell_ffn_fused_fwd(x, Wu_c, Wd_c, packed_c, y=y_c, status=status, stream=stream),
+            c_steps)
         binding.check_device_status("compacted", status)
-        mcg = statistics.median(u.elapsed_time(v) for u, v in cg)
-        mcf = statistics.median(u.elapsed_time(v) for u, v in cf)
         compacted = {"live_cols": f_c, "dead_cols": f - f_c, "calibration": f"{N} other tokens (seed {1000 + rank})",
                      "ms_gate_pack": mcg, "ms_fused": mcf, "ms_per_step": mcg + mcf,
                      "tokens_per_s": N / ((mcg + mcf) * 1e-3), "y_bit_identical": identical,
                      "speedup_vs_dense": (dense["ms"] / (mcg + mcf)) if dense else None,
                      "note": "dead-column compaction (units that never fired in the calibration batch are dropped "
                              "from Wg_s, Wu_s, Wd_s once); medians over the steps, L2 flushed"}
-        del packed_c, Wg_c, Wu_c, Wd_c
+
+    # ---- the walk with its down projection in fp16 (Wd_s converted once; h rounded once to fp16)
+    f16 = None
+    if not a.no_f16down:
+        n16 = max(10, min(a.steps, 200))
+        Wd16 = binding.twell_convert_f16(Wd, status=status, stream=stream)
+        y16 = torch.empty_like(y)
+        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+        binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y16, status=status, stream=stream)
+        torch.cuda.synchronize()
+        diff = (y16.float() - y.float()).norm().item() / max(y.float().norm().item(), 1e-30)
+        g16, w16 = medians_gate_walk(
+            lambda: binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream),
+            lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y16, status=status, stream=stream),
+            n16)
+        binding.check_device_status("f16down", status)
+        f16 = {"ms_gate_pack": g16, "ms_walk": w16, "ms_per_step": g16 + w16, "tokens_per_s": N / ((g16 + w16) * 1e-3),
+               "walk_roofline_frac": (fused_bytes / (w16 * 1e-3)) / 1e9 / peaks["hbm_gbs"],
+               "speedup_vs_dense": (dense["ms"] / (g16 + w16)) if dense else None,
+               "rel_fro_vs_bf16_walk": diff,
+               "note": "twell_ffn_fused_fwd_f16down: Wd_s converted once to fp16 (exact for these weights), h "
+                       "rounded once to fp16 (11 significant bits) instead of a bf16 hi + lo pair; medians, L2 "
+                       "flushed; not the headline (the headline walk keeps every operand in bf16)"}
+        if Wd_c is not None:
+            Wd16_c = binding.twell_convert_f16(Wd_c, status=status, stream=stream)
+            gc, wc = medians_gate_walk(
+                lambda: binding.twell_gate_pack(x, Wg_c, T, out=packed_c, status=status, stream=stream),
+                lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu_c, Wd16_c, packed_c, y=y_c, status=status,
+                                                            stream=stream),
+                n16)
+            binding.check_device_status("f16down compacted", status)
+            f16["compacted"] = {"ms_per_step": gc + wc, "tokens_per_s": N / ((gc + wc) * 1e-3),
+                                "speedup_vs_dense": (dense["ms"] / (gc + wc)) if dense else None}
+            del Wd16_c
+        del Wd16, y16
+    del packed_c, Wg_c, Wu_c, Wd_c
 
     train = None
     if not a.no_train:
@@ -489,6 +535,7 @@ def run_ours(a, rank, world):
                                          "128-token tile + y) / HBM peak)"},
         "kernels_ms": {"twell_gate_pack": mg, "twell_ffn_fused_fwd": mf},
         "compacted": compacted,
+        "f16down": f16,
         "warm": {"ms_per_step": warm_ms, "tokens_per_s": weak_scaling_rate(N, warm_ms, world),
                  "l2": "not flushed between steps"},
         "vs_dense_cublas": dense,

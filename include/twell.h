@@ -173,6 +173,27 @@ TWELL_API twell_status twell_ffn_fused_fwd(const void* x, const void* Wu_s, cons
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);
 
+/* twell_ffn_fused_fwd with the down projection in fp16: Wd16_s is Wd_s converted once to fp16
+ * (twell_convert_f16; the conversion is exact for every bf16 weight in [2^-17, 65504] in
+ * magnitude, and loses no more than 2^-25 in absolute terms below that), and each h = a * u is
+ * rounded once to fp16 (11 significant bits, against ~16 for the bf16 hi + lo pair of
+ * twell_ffn_fused_fwd), which halves the tensor-core products of the down projection. Products
+ * are accumulated in fp32, as there. bf16 x, Wu_s and y; TwELL values bf16 or fp32; d a multiple
+ * of 256 in [512, 3072] (else TWELL_ERR_UNSUPPORTED). Workspace, determinism and error
+ * reporting as twell_ffn_fused_fwd.
+ */
+TWELL_API twell_status twell_ffn_fused_fwd_f16down(const void* x, const void* Wu_s, const void* Wd16_s,
+                                         const twell_packed* a, int32_t N, int32_t d, int32_t f,
+                                         void* y, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                         void* stream);
+
+/* n bf16 values at src to fp16 at dst (device pointers, no overlap), round to nearest even. A
+ * finite value beyond the fp16 range is stored as infinity and reported as
+ * TWELL_ERR_DEVICE_CHECK in *dev_status.
+ */
+TWELL_API twell_status twell_convert_f16(const void* src, void* dst, int64_t n, int32_t* dev_status,
+                               void* stream);
+
 /* The same y from the same TwELL for a layer too dense for the walk: with more than ~1% of
  * d_ff kept per token the union of the units a tile of 128 tokens keeps is most of d_ff, so the
  * up and down projections are dense contractions over all of it, on the tensor cores ([TC] §3:

@@ -174,6 +174,33 @@ def test_union_rejects_bad_arguments(lib):
     assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
 
 
+def test_fused_f16down_rejects_bad_arguments(lib):
+    p = _packed()
+    need = lib.twell_workspace_bytes(1, 4, 512, 256, 128, 0, 0)  # TWELL_OP_FFN_FUSED_FWD
+    call = lambda **kw: lib.twell_ffn_fused_fwd_f16down(  # noqa: E731
+        ALIGNED, ALIGNED, kw.get("wd", ALIGNED), ctypes.byref(kw.get("p", p)), kw.get("N", 4), kw.get("d", 512),
+        kw.get("f", 256), kw.get("y", ALIGNED), kw.get("ws", ALIGNED), kw.get("ws_bytes", need), STATUS, None)
+    assert call(wd=None) == 1
+    assert call(y=None) == 1
+    assert call(ws=None) == 7
+    assert call(ws_bytes=need - 1) == 7
+    assert call(d=640) == 2  # a multiple of 256 in [512, 3072] only
+    assert call(d=256) == 2
+    assert call(d=3328) == 2
+    assert call(d=12) == 1
+    assert call(N=5) == 1  # the TwELL describes 4 rows
+    assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0
+    assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
+
+
+def test_convert_f16_rejects_bad_arguments(lib):
+    assert lib.twell_convert_f16(ALIGNED, ALIGNED, -1, STATUS, None) == 1
+    assert lib.twell_convert_f16(ALIGNED, ALIGNED, 16, None, None) == 1
+    assert lib.twell_convert_f16(None, ALIGNED, 16, STATUS, None) == 1
+    assert lib.twell_convert_f16(ALIGNED, None, 16, STATUS, None) == 1
+    assert lib.twell_convert_f16(None, None, 0, STATUS, None) == 0
+
+
 def test_wait_probe_rejects_bad_limits(lib):
     assert lib.twell_wait_probe(0, 0, STATUS, None) == 1
     assert lib.twell_wait_probe(0, 10001, STATUS, None) == 1
