@@ -119,6 +119,44 @@ def test_gate_pack_integer_bit_exact(cuda_dev, T, N, d, f, vals_dtype):
 
 
 @pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [64, 128, 256])
+@pytest.mark.parametrize("N,d,f", [(1, 2048, 5632), (2, 64, 300), (7, 512, 1000), (8, 1024, 777), (9, 256, 1024),
+                                   (16, 4096, 520), (17, 512, 1000)])
+def test_gate_pack_small_batch_bit_exact(cuda_dev, T, N, d, f, vals_dtype):
+    """Batches of up to 16 tokens run the cluster-pair GEMV kernel (two CTAs per column tile, the
+    tile's halves exchanged through distributed shared memory); 17 tokens the 128 x T tile GEMM.
+    Bit-exact on integer inputs, with ragged last tiles, and the same bits on a second call."""
+    x, W = _int_layer(N, d, f, seed=3 * T + N)
+    xt, Wt = _to(cuda_dev, x), _to(cuda_dev, W)
+    tw = binding.twell_gate_pack(xt, Wt, T, vals_dtype=vals_dtype)
+    G = oracle.gate(x, W)
+    vals, idx, cnt = oracle.twell_pack(G, T)
+    exact = vals if vals_dtype == torch.float32 else oracle.round_bf16(vals)
+    _compare_packed(tw, vals, idx, cnt, exact_vals=exact)
+    assert cnt.sum() > 0
+    tw2 = binding.twell_gate_pack(xt, Wt, T, vals_dtype=vals_dtype)
+    assert torch.equal(tw.cnt, tw2.cnt) and torch.equal(binding.twell_unpack(tw), binding.twell_unpack(tw2))
+
+
+def test_gate_pack_small_batch_random_matches_oracle(cuda_dev):
+    """Random bf16 decode batch of the 1.5B-like layer: kept set and values against fp64 away from
+    zero, and the fp32 sums equal to the large-batch tile GEMM's within fp32 rounding."""
+    L = synthetic.layer_1p5b(N=12)
+    t = L.torch_inputs(cuda_dev)
+    tw = binding.twell_gate_pack(t["x"], t["Wg_s"], L.T)
+    dense = binding.twell_unpack(tw).double().cpu().numpy()
+    G = oracle.gate(L.x, L.Wg_s)
+    big = np.abs(G) > 1e-3
+    assert np.array_equal(dense[big] > 0, G[big] > 0)
+    np.testing.assert_allclose(dense[big], np.maximum(G[big], 0), rtol=1e-5, atol=2e-5)
+    # the same rows inside a 300-token batch go through the tile GEMM
+    x_big = torch.cat([t["x"], t["x"][:1].expand(288, -1)]).contiguous()
+    dense_big = binding.twell_unpack(binding.twell_gate_pack(x_big, t["Wg_s"], L.T))[:12].double().cpu().numpy()
+    both = big & (dense > 0)
+    np.testing.assert_allclose(dense[both], dense_big[both], rtol=1e-5, atol=2e-5)
+
+
+@pytest.mark.parametrize("vals_dtype", [torch.float32, torch.bfloat16])
 def test_gate_pack_random_matches_oracle_away_from_zero(cuda_dev, vals_dtype):
     """On random bf16 layers the kept set can differ from fp64 only where |g| is at the fp32
     accumulation-error level."""
