@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(_PKG, "libtwell_gb300.so")
 TWELL_OK = 0
 TWELL_BF16 = 0
 TWELL_F32 = 1
-OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD = range(6)
+OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD, OP_FFN_DECODE = range(7)
+DECODE_MAX_N = 16  # twell_ffn_decode takes batches of at most this many tokens
 STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED", 3: "TWELL_ERR_BACKUP_FULL",
                 4: "TWELL_ERR_TIMEOUT", 5: "TWELL_ERR_DEVICE_CHECK", 6: "TWELL_ERR_CUDA",
                 7: "TWELL_ERR_WORKSPACE"}
@@ -33,7 +34,7 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe",
-           "twell_ffn_fused_fwd_f16down", "twell_convert_f16")
+           "twell_ffn_fused_fwd_f16down", "twell_convert_f16", "twell_ffn_decode")
 
 
 class TwellError(RuntimeError):
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
                 "twell_ffn_fused_fwd_f16down": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
                                                      vp, vp]),
                 "twell_convert_f16": (st, [vp, vp, ctypes.c_int64, vp, vp]),
+                "twell_ffn_decode": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.POINTER(_Packed), vp, vp, sz,
+                                          vp, vp]),
                 "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
                                           ctypes.POINTER(_Hybrid), vp, vp, sz, vp]),
                 "twell_hybrid_bwd": (st, [vp, vp, vp, vp, ctypes.POINTER(_Hybrid), vp, i32, i32, i32, ctypes.c_float,
@@ -371,10 +374,44 @@ def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
     return y
 
 
+_decode_ws = {}
+
+
+def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, T: int = 128,
+                     packed: Optional[TwELL] = None, y: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None, ws: Optional[torch.Tensor] = None,
+                     vals_dtype: torch.dtype = torch.float32):
+    """The whole layer for at most DECODE_MAX_N tokens in two launches; returns (y, packed TwELL)."""
+    N, d = x.shape
+    f = Wg_s.shape[0]
+    packed = packed if packed is not None else TwELL.empty(N, f, T, vals_dtype, x.device)
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    if ws is None:
+        n = twell_workspace_bytes(OP_FFN_DECODE, N, d, f, T)
+        key = (x.device.index, _stream(stream).value or 0)
+        ws = _decode_ws.get(key)
+        if ws is None or ws.numel() < n:
+            ws = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
+            _decode_ws[key] = ws
+    s = packed.c_struct()
+    _check(load().twell_ffn_decode(_ptr(x), _ptr(Wg_s), _ptr(Wu_s), _ptr(Wd_s), N, d, f, T, ctypes.byref(s),
+                                   _ptr(y), _ptr(ws), ws.numel(),
+                                   _ptr(status if status is not None else status_buffer(x.device)),
+                                   _stream(stream)),
+           "twell_ffn_decode")
+    return y, packed
+
+
 def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
                 vals_dtype: torch.dtype = torch.float32, path: str = "walk"):
     """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk") or, for a
-    layer too dense for the walk, twell_ffn_union_fwd (path "union")."""
+    layer too dense for the walk, twell_ffn_union_fwd (path "union"); path "decode" runs
+    twell_ffn_decode (at most DECODE_MAX_N tokens), path "auto" decode for such batches, else the walk."""
+    if path == "auto":
+        path = "decode" if x.shape[0] <= DECODE_MAX_N else "walk"
+    if path == "decode":
+        return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
+                                vals_dtype=vals_dtype)[0]
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
     if path == "union":
         return twell_ffn_union_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)

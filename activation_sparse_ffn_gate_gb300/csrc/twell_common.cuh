@@ -463,6 +463,8 @@ twell_status dev_info(DevInfo* out);
 size_t fused_ws_bytes(int N, int d, int f);
 // Bytes of the workspace twell_ffn_union_fwd needs (twell_union.cu).
 size_t union_ws_bytes(int N, int f);
+// Bytes of the workspace twell_ffn_decode needs (twell_decode.cu).
+size_t decode_ws_bytes(int N, int d, int f, int T);
 
 // 2-D tensor map over a row-major matrix of 16-bit elements: `inner` contiguous elements per row,
 // `outer` rows, row pitch `ld` elements; box [box_inner, box_outer]; 128-byte swizzle; zero fill

@@ -811,12 +811,12 @@ twell_status run_route(const twell::HybridWs& L, uint8_t* ws, int N, int f, int 
 extern "C" size_t twell_workspace_bytes(twell_op op, int32_t N, int32_t d, int32_t f, int32_t tile, int32_t K,
                                         int32_t backup_cap)
 {
-    (void)tile;
     if (N < 0 || d <= 0 || f <= 0 || K < 0 || backup_cap < 0) return 0;
     switch (op) {
     case TWELL_OP_GATE_PACK: return 0;
     case TWELL_OP_FFN_FUSED_FWD: return twell_host::fused_ws_bytes(N, d, f);
     case TWELL_OP_FFN_UNION_FWD: return twell_host::union_ws_bytes(N, f);
+    case TWELL_OP_FFN_DECODE: return tile > 0 ? twell_host::decode_ws_bytes(N, d, f, tile) : 0;
     case TWELL_OP_HYBRID_ROUTE: return twell::HybridWs(N, d, f, K, backup_cap).route_total;
     case TWELL_OP_HYBRID_FWD: return twell::HybridWs(N, d, f, K, backup_cap).fwd_total;
     case TWELL_OP_HYBRID_BWD: return twell::HybridWs(N, d, f, K, backup_cap).bwd_total;

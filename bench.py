@@ -720,6 +720,21 @@ def run_sweep(a):
         ms_fused = timed(fused_fn, n_it)
         ms_union = timed(union_fn, max(3, min(n_it, 15)))
         ms_dense = timed(dense_fn, n_it)
+        decode = None
+        if L.N <= binding.DECODE_MAX_N:
+            packed_d = binding.TwELL.empty(L.N, L.f, L.T, torch.float32, dev)
+            y_d = torch.empty_like(y)
+            decode_fn = lambda: binding.twell_ffn_decode(x, Wg, Wu, Wd, L.T, packed=packed_d, y=y_d,  # noqa: E731
+                                                         status=status)
+            decode_fn()
+            fused_fn()
+            torch.cuda.synchronize()
+            rel = ((y_d.float() - y.float()).norm() / y.float().norm().clamp_min(1e-30)).item()
+            ms_d = timed(graphed(decode_fn) if use_graphs else decode_fn, n_it)
+            decode = {"ms": ms_d, "tokens_per_s": L.N / (ms_d * 1e-3), "speedup_vs_dense": ms_dense / ms_d,
+                      "rel_fro_vs_two_call_path": rel,
+                      "how": "twell_ffn_decode: gate + pack + per-tile walk in one cluster kernel, partial rows "
+                             "summed in a fixed order by a second kernel"}
         binding.check_device_status(label, status)
         ms = ms_gate + ms_fused
         ms_u = ms_gate + ms_union
@@ -730,6 +745,7 @@ def run_sweep(a):
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
                           "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
                           "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u),
+                          "decode": decode,
                           "cuda_graphs": use_graphs, "l2": "flushed before every iteration"}), flush=True)
         del t, x, Wg, Wu, Wd, packed, y
         torch.cuda.empty_cache()

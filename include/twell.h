@@ -66,7 +66,8 @@ typedef enum {
     TWELL_OP_HYBRID_FWD = 2,
     TWELL_OP_HYBRID_BWD = 3,
     TWELL_OP_HYBRID_ROUTE = 4,
-    TWELL_OP_FFN_UNION_FWD = 5
+    TWELL_OP_FFN_UNION_FWD = 5,
+    TWELL_OP_FFN_DECODE = 6
 } twell_op;
 
 /* A TwELL matrix of gate activations a = ReLU(G), [n_rows, n_cols] ([TG] "Вот тут и решает TwELL";
@@ -193,6 +194,26 @@ TWELL_API twell_status twell_ffn_fused_fwd_f16down(const void* x, const void* Wu
  */
 TWELL_API twell_status twell_convert_f16(const void* src, void* dst, int64_t n, int32_t* dev_status,
                                void* stream);
+
+/* The whole layer for a batch of at most 16 tokens (decoding) in two launches: the gate + pack of
+ * twell_gate_pack (the same TwELL in *a_out, bit for bit) and, in the same kernel, the walk of each
+ * column tile's kept entries by the CTAs that computed them ([AIM] ¶3; [TG] "Инференс"; [PUL] ¶3;
+ * [TC] §2): the walk is separable by column tile, y_r = sum over tiles of sum over the tile's kept
+ * j of a * (x_r . Wu_s[j]) * Wd_s[j]. Each CTA (half a column tile) forms u and h = a * u for its
+ * units in fp32 (a as stored in the TwELL), adds h * Wd_s[j] in fp32 over its units in ascending
+ * order and stores one fp32 partial row per token; a second kernel adds each token's partial rows
+ * in a fixed order and stores y (bf16). y is the same bit for bit from call to call and does not
+ * depend on scheduling; it agrees with twell_ffn_fused_fwd on the same TwELL to fp32 summation
+ * order. bf16 x, Wg_s, Wu_s, Wd_s, y; 0 <= N <= 16, d_model a multiple of 64 up to 4096, tile 64,
+ * 128 or 256 (else TWELL_ERR_UNSUPPORTED); a_out describes an [N, f] TwELL with tile T, values
+ * bf16 or fp32. ws: twell_workspace_bytes(TWELL_OP_FFN_DECODE, N, d, f, T, 0, 0) bytes (a flag
+ * and an fp32 partial row of d_model per (CTA, token): 2 * ceil(f / T) CTAs), 16-byte aligned,
+ * required when N > 0; its contents need not be initialised, and two calls in flight at the same
+ * time must not share it.
+ */
+TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const void* Wu_s, const void* Wd_s,
+                              int32_t N, int32_t d, int32_t f, int32_t T, const twell_packed* a_out,
+                              void* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* The same y from the same TwELL for a layer too dense for the walk: with more than ~1% of
  * d_ff kept per token the union of the units a tile of 128 tokens keeps is most of d_ff, so the

@@ -193,6 +193,30 @@ def test_fused_f16down_rejects_bad_arguments(lib):
     assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
 
 
+def test_decode_rejects_bad_arguments(lib):
+    p = _packed()
+    need = lib.twell_workspace_bytes(6, 4, 512, 256, 128, 0, 0)  # TWELL_OP_FFN_DECODE
+    assert need >= 4 * 4 * 512 * 4  # a partial row per (CTA, token): 2 * ceil(256 / 128) CTAs
+    assert lib.twell_workspace_bytes(6, 4, 512, 256, 0, 0, 0) == 0  # the tile width sizes it
+    call = lambda **kw: lib.twell_ffn_decode(  # noqa: E731
+        ALIGNED, ALIGNED, kw.get("wu", ALIGNED), ALIGNED, kw.get("N", 4), kw.get("d", 512), kw.get("f", 256),
+        kw.get("T", 128), ctypes.byref(kw.get("p", p)), kw.get("y", ALIGNED), kw.get("ws", ALIGNED),
+        kw.get("ws_bytes", need), STATUS, None)
+    assert call(wu=None) == 1
+    assert call(y=None) == 1
+    assert call(ws=None) == 7
+    assert call(ws_bytes=need - 1) == 7
+    assert call(N=17, p=_packed(N=17)) == 2  # at most 16 tokens
+    assert call(d=72) == 2  # d_model a multiple of 64
+    assert call(d=4160) == 2  # at most 4096
+    assert call(d=100) == 1
+    assert call(T=32, p=_packed(T=32)) == 2
+    assert call(N=5) == 1  # the TwELL describes 4 rows
+    assert call(T=64) == 1  # the TwELL's tile is 128
+    assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0
+    assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
+
+
 def test_convert_f16_rejects_bad_arguments(lib):
     assert lib.twell_convert_f16(ALIGNED, ALIGNED, -1, STATUS, None) == 1
     assert lib.twell_convert_f16(ALIGNED, ALIGNED, 16, None, None) == 1
