@@ -8,6 +8,8 @@
 //     span of d_model; per span each lane loads 32 contiguous bytes of its two units' rows
 //     (16-byte read-only loads that skip L1) -- the k order inside a span is permuted the same way
 //     for both operands, so the fragments come straight from those loads;
+//   * the part of each row past a warp's first batch of spans is prefetched to L2 at the start, so
+//     the later batches' loads hit L2;
 //   * x (padded to 8 or 16 token rows, rows >= N zero) is staged in shared memory once, by
 //     asynchronous copies in flight together with the first weight loads;
 //   * products on mma.sync m16n8k16 (units as the 16 rows, tokens as the 8 columns), fp32
@@ -68,6 +70,15 @@ __device__ __forceinline__ void small_gate_phase(const __nv_bfloat16* __restrict
     float* gs = reinterpret_cast<float*>(smem + L.g);       // [U][NTOK]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 
+    // the spans past the first batch of every warp (columns 4 KS * 64 .. d of the CTA's rows) move
+    // from HBM to L2 while the first batch is loaded and used
+    const int pf0 = 4 * KS * 64;
+    if (pf0 < d) {
+        for (int r = threadIdx.x; r < U; r += blockDim.x) {
+            const int u = tile * T + rank * U + r;
+            if (u < f) bulk_prefetch_l2(Wg + static_cast<size_t>(u) * d + pf0, static_cast<uint32_t>(d - pf0) * 2u);
+        }
+    }
     // x rows (zeros past N) by asynchronous copies, in flight with the first weight loads below
     const int chunks = d / 8;
     for (int i = threadIdx.x; i < NTOK * chunks; i += blockDim.x) {

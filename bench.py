@@ -675,20 +675,42 @@ def run_sweep(a):
             ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
-    def graphed(fn):
-        """fn captured once into a CUDA graph; returns its replay. Small decode batches run for tens
-        of microseconds, less than the host needs to issue the calls, so their GPU time is taken
-        from graph replays (the kernels of one step, launched back to back)."""
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
+    def timed_in_graph(fn, n, rounds=3):
+        """Device time of fn for small decode batches, which run for tens of microseconds: the
+        event clock resolves only ~2 us here, so fn is captured after an L2 flush into one CUDA
+        graph, a flush alone into another, each graph is replayed n times between one pair of
+        events, and the difference per replay is fn's time (L2 still flushed before every call).
+        Median of `rounds` such measurements."""
+        def capture(body):
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                body()
+            torch.cuda.current_stream().wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body()
+            torch.cuda.synchronize()
+            return g
+
+        def body_fn():
+            flush.fill_(1)
             fn()
-        torch.cuda.current_stream().wait_stream(side)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        torch.cuda.synchronize()
-        return g.replay
+
+        g_fn, g_fl = capture(body_fn), capture(lambda: flush.fill_(1))
+
+        def total(g):
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        return statistics.median((total(g_fn) - total(g_fl)) / n for _ in range(rounds))
 
     points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
     layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
@@ -713,13 +735,15 @@ def run_sweep(a):
 
         use_graphs = label.startswith("decode")
         if use_graphs:
-            gate_fn, fused_fn, union_fn, dense_fn = graphed(gate_fn), graphed(fused_fn), graphed(union_fn), \
-                graphed(dense_fn)
-            n_it = max(n_it, 50)
-        ms_gate = timed(gate_fn, n_it)
-        ms_fused = timed(fused_fn, n_it)
-        ms_union = timed(union_fn, max(3, min(n_it, 15)))
-        ms_dense = timed(dense_fn, n_it)
+            ms_gate = timed_in_graph(gate_fn, 50)
+            ms_fused = timed_in_graph(fused_fn, 50)
+            ms_union = timed_in_graph(union_fn, 50)
+            ms_dense = timed_in_graph(dense_fn, 50)
+        else:
+            ms_gate = timed(gate_fn, n_it)
+            ms_fused = timed(fused_fn, n_it)
+            ms_union = timed(union_fn, max(3, min(n_it, 15)))
+            ms_dense = timed(dense_fn, n_it)
         decode = None
         if L.N <= binding.DECODE_MAX_N:
             packed_d = binding.TwELL.empty(L.N, L.f, L.T, torch.float32, dev)
@@ -730,7 +754,7 @@ def run_sweep(a):
             fused_fn()
             torch.cuda.synchronize()
             rel = ((y_d.float() - y.float()).norm() / y.float().norm().clamp_min(1e-30)).item()
-            ms_d = timed(graphed(decode_fn) if use_graphs else decode_fn, n_it)
+            ms_d = timed_in_graph(decode_fn, 50) if use_graphs else timed(decode_fn, n_it)
             decode = {"ms": ms_d, "tokens_per_s": L.N / (ms_d * 1e-3), "speedup_vs_dense": ms_dense / ms_d,
                       "rel_fro_vs_two_call_path": rel,
                       "how": "twell_ffn_decode: gate + pack + per-tile walk in one cluster kernel, partial rows "
@@ -746,7 +770,10 @@ def run_sweep(a):
                           "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
                           "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u),
                           "decode": decode,
-                          "cuda_graphs": use_graphs, "l2": "flushed before every iteration"}), flush=True)
+                          "cuda_graphs": use_graphs, "l2": "flushed before every iteration",
+                          "timing": ("per call: (50 replays of a graph [L2 flush + call] - 50 replays of a graph "
+                                     "[L2 flush]) / 50, median of 3" if use_graphs else
+                                     f"CUDA events around each call, median of {n_it}")}), flush=True)
         del t, x, Wg, Wu, Wd, packed, y
         torch.cuda.empty_cache()
 
