@@ -729,6 +729,8 @@ def run_sweep(a):
         gate_fn = lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)  # noqa: E731
         fused_fn = lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
         union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
+        Wd16 = binding.twell_convert_f16(Wd, status=status)
+        f16_fn = lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
 
         def dense_fn():
             return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
@@ -738,11 +740,13 @@ def run_sweep(a):
             ms_gate = timed_in_graph(gate_fn, 50)
             ms_fused = timed_in_graph(fused_fn, 50)
             ms_union = timed_in_graph(union_fn, 50)
+            ms_f16 = timed_in_graph(f16_fn, 50)
             ms_dense = timed_in_graph(dense_fn, 50)
         else:
             ms_gate = timed(gate_fn, n_it)
             ms_fused = timed(fused_fn, n_it)
             ms_union = timed(union_fn, max(3, min(n_it, 15)))
+            ms_f16 = timed(f16_fn, n_it)
             ms_dense = timed(dense_fn, n_it)
         decode = None
         if L.N <= binding.DECODE_MAX_N:
@@ -769,12 +773,14 @@ def run_sweep(a):
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
                           "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
                           "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u),
+                          "f16down": {"ms_walk": ms_f16, "ms_step": ms_gate + ms_f16,
+                                      "speedup_vs_dense": ms_dense / (ms_gate + ms_f16)},
                           "decode": decode,
                           "cuda_graphs": use_graphs, "l2": "flushed before every iteration",
                           "timing": ("per call: (50 replays of a graph [L2 flush + call] - 50 replays of a graph "
                                      "[L2 flush]) / 50, median of 3" if use_graphs else
                                      f"CUDA events around each call, median of {n_it}")}), flush=True)
-        del t, x, Wg, Wu, Wd, packed, y
+        del t, x, Wg, Wu, Wd, Wd16, packed, y
         torch.cuda.empty_cache()
 
 
