@@ -715,7 +715,7 @@ def run_sweep(a):
     points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
     layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
     layers.append(("layer2b", synthetic.layer_2b))
-    layers += [(f"decode N={n}", lambda n=n: synthetic.layer_1p5b(N=n)) for n in (1, 8, 16, 64, 512)]
+    layers += [(f"decode N={n}", lambda n=n: synthetic.layer_1p5b(N=n)) for n in (1, 8, 16, 32, 64, 512)]
     layers = [(label, make) for label, make in layers if a.sweep_only in label]
     for label, make in layers:
         L = make()
