@@ -20,6 +20,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libtwell_gb300.so")
 
 TWELL_OK = 0
+TWELL_ERR_UNSUPPORTED = 2
 TWELL_BF16 = 0
 TWELL_F32 = 1
 OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD, OP_FFN_DECODE = range(7)
@@ -406,9 +407,17 @@ def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = Non
                 vals_dtype: torch.dtype = torch.float32, path: str = "walk"):
     """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk") or, for a
     layer too dense for the walk, twell_ffn_union_fwd (path "union"); path "decode" runs
-    twell_ffn_decode (at most DECODE_MAX_N tokens), path "auto" decode for such batches, else the walk."""
+    twell_ffn_decode (at most DECODE_MAX_N tokens), path "auto" decode for such batches where the
+    library supports the shape, else the walk."""
     if path == "auto":
-        path = "decode" if x.shape[0] <= DECODE_MAX_N else "walk"
+        if x.shape[0] <= DECODE_MAX_N:
+            try:
+                return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
+                                        vals_dtype=vals_dtype)[0]
+            except TwellError as e:
+                if e.code != TWELL_ERR_UNSUPPORTED:
+                    raise
+        path = "walk"
     if path == "decode":
         return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                 vals_dtype=vals_dtype)[0]

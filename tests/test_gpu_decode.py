@@ -92,6 +92,18 @@ def test_decode_zero_density_and_empty(cuda_dev):
     assert y0.shape == (0, 512)
 
 
+def test_decode_unsupported_shape_falls_back(cuda_dev):
+    """d_model above 4096 is outside the decode kernel's range: the call says so before launching,
+    and the auto path falls back to gate + walk."""
+    L = synthetic.uniform_layer(4, 4608, 1000, 128, 0.02, seed=8)
+    t = L.torch_inputs(cuda_dev)
+    with pytest.raises(binding.TwellError) as e:
+        binding.twell_ffn_decode(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], 128)
+    assert e.value.code == binding.TWELL_ERR_UNSUPPORTED
+    y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128, path="auto")
+    assert_close(y.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), "auto fallback")
+
+
 def test_ffn_forward_auto_path(cuda_dev):
     L = synthetic.layer_1p5b(N=4)
     t = L.torch_inputs(cuda_dev)
