@@ -130,41 +130,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(32 * kSmallWarps, 1)
     // up projection: one warp per listed unit, lanes on 16-byte chunks lane, lane + 32, ... of the
     // row, eight at a time
     const int chunks = d / 8;
-    for (int k = warp; k < nk; k += kSmallWarps) {
-        const int u = list[k];
-        const unsigned m = umask[k];
-        const __nv_bfloat16* wr = Wu + static_cast<size_t>(u_base + u) * d;
-        float s[NTOK];
-#pragma unroll
-        for (int r = 0; r < NTOK; ++r) s[r] = 0.0f;
-        for (int c0 = lane; c0 < chunks; c0 += 32 * kDecodeChunks) {
+    // h = a * u with a as the TwELL stores it (fp32 g, or g rounded to bf16)
+    auto store_h = [&](int u, int r, float dot) {
+        const float g = gs[u * NTOK + r];
+        const float a = vals_f32 ? g : __bfloat162float(__float2bfloat16_rn(g));
+        hs[u * NTOK + r] = a * dot;
+    };
+    if (chunks <= 32 * kDecodeChunks) {
+        // the row fits one batch of chunks: load it once, then one token of the mask at a time
+        for (int k = warp; k < nk; k += kSmallWarps) {
+            const int u = list[k];
+            const __nv_bfloat16* wr = Wu + static_cast<size_t>(u_base + u) * d;
             uint4 w[kDecodeChunks];
 #pragma unroll
             for (int i = 0; i < kDecodeChunks; ++i) {
-                const int c = c0 + 32 * i;
+                const int c = lane + 32 * i;
                 w[i] = c < chunks ? ldg_stream16(wr + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            for (unsigned m = umask[k]; m != 0u; m &= m - 1u) {
+                const int r = __ffs(m) - 1;
+                const uint8_t* xr = xs + r * L.G.x_stride;
+                float v = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kDecodeChunks; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < chunks) v += dot8(w[i], *reinterpret_cast<const uint4*>(xr + c * 16));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) store_h(u, r, v);
+            }
+        }
+    } else {
+        // wider rows: all keeping tokens' dots in one pass per batch of chunks
+        for (int k = warp; k < nk; k += kSmallWarps) {
+            const int u = list[k];
+            const unsigned m = umask[k];
+            const __nv_bfloat16* wr = Wu + static_cast<size_t>(u_base + u) * d;
+            float s[NTOK];
+#pragma unroll
+            for (int r = 0; r < NTOK; ++r) s[r] = 0.0f;
+            for (int c0 = lane; c0 < chunks; c0 += 32 * kDecodeChunks) {
+                uint4 w[kDecodeChunks];
+#pragma unroll
+                for (int i = 0; i < kDecodeChunks; ++i) {
+                    const int c = c0 + 32 * i;
+                    w[i] = c < chunks ? ldg_stream16(wr + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int r = 0; r < NTOK; ++r) {
+                    if (!((m >> r) & 1u)) continue;
+                    const uint8_t* xr = xs + r * L.G.x_stride;
+#pragma unroll
+                    for (int i = 0; i < kDecodeChunks; ++i) {
+                        const int c = c0 + 32 * i;
+                        if (c < chunks) s[r] += dot8(w[i], *reinterpret_cast<const uint4*>(xr + c * 16));
+                    }
+                }
             }
 #pragma unroll
             for (int r = 0; r < NTOK; ++r) {
                 if (!((m >> r) & 1u)) continue;
-                const uint8_t* xr = xs + r * L.G.x_stride;
+                float v = s[r];
 #pragma unroll
-                for (int i = 0; i < kDecodeChunks; ++i) {
-                    const int c = c0 + 32 * i;
-                    if (c < chunks) s[r] += dot8(w[i], *reinterpret_cast<const uint4*>(xr + c * 16));
-                }
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < NTOK; ++r) {
-            if (!((m >> r) & 1u)) continue;
-            float v = s[r];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) {
-                const float g = gs[u * NTOK + r];
-                const float a = vals_f32 ? g : __bfloat162float(__float2bfloat16_rn(g));
-                hs[u * NTOK + r] = a * v;
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0) store_h(u, r, v);
             }
         }
     }
