@@ -565,10 +565,11 @@ class Hybrid:
         return self.col.to(torch.int32) & 0xFFFF
 
     def c_struct(self) -> _Hybrid:
-        return _Hybrid(self.n_rows, self.n_cols, self.K, self.backup_cap, TWELL_BF16, self.a.data_ptr(),
-                       self.u.data_ptr(), self.col.data_ptr(), self.cnt.data_ptr(), self.backup_rows.data_ptr(),
-                       self.n_backup.data_ptr(), self.A_b.data_ptr(), self.U_b.data_ptr(), self.l1.data_ptr(),
-                       self.status.data_ptr())
+        def ptr(t):
+            return t.data_ptr() if t is not None else None
+        return _Hybrid(self.n_rows, self.n_cols, self.K, self.backup_cap, TWELL_BF16, ptr(self.a), ptr(self.u),
+                       ptr(self.col), ptr(self.cnt), ptr(self.backup_rows), ptr(self.n_backup), ptr(self.A_b),
+                       ptr(self.U_b), ptr(self.l1), ptr(self.status))
 
 
 def _workspace(op, N, d, f, K, cap, device, ws=None):

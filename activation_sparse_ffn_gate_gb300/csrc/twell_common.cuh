@@ -207,8 +207,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
         : "memory");
 }
 
-// The same 2D tile load with cluster multicast: the box lands at the same shared-memory offset
-// in every CTA of `cta_mask` and counts its bytes on the mbarrier at the same offset in each.
 // The same copy for a CTA pair (tcgen05 cta_group::2): the completion is counted on the
 // mbarrier at shared::cluster address `bar_cluster`, which may be in the peer CTA.
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* tm, int32_t c0, int32_t c1,

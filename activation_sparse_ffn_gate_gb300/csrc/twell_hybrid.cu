@@ -780,6 +780,24 @@ twell_status check_hybrid(const twell_hybrid* c, int N, int f, int K)
     return TWELL_OK;
 }
 
+// The fields the routing kernels write (cnt, col, a, backup_rows, n_backup, A_b) and the status
+// word; u, U_b and l1 are not touched by routing and may be null.
+twell_status check_route_ctx(const twell_hybrid* c, int N, int f, int K)
+{
+    if (c == nullptr) return TWELL_ERR_INVALID;
+    if (c->n_rows != N || c->n_cols != f || c->K != K || c->backup_cap < 0) return TWELL_ERR_INVALID;
+    if (c->dtype != TWELL_BF16) return TWELL_ERR_UNSUPPORTED;
+    if (N == 0) return TWELL_OK;
+    if (c->cnt == nullptr || c->n_backup == nullptr || c->dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (K > 0 && (c->a == nullptr || c->col == nullptr)) return TWELL_ERR_INVALID;
+    if (c->backup_cap > 0 && (c->backup_rows == nullptr || c->A_b == nullptr)) return TWELL_ERR_INVALID;
+    const void* ps[] = {c->a, c->col, c->cnt, c->backup_rows, c->n_backup, c->A_b, c->dev_status};
+    for (const void* p : ps)
+        if (p != nullptr && !aligned16(p)) return TWELL_ERR_INVALID;
+    if (c->backup_cap > 0 && (static_cast<size_t>(f) * 4) % 16 != 0) return TWELL_ERR_UNSUPPORTED;
+    return TWELL_OK;
+}
+
 inline unsigned grid_for(long long work, int threads, int cap_blocks)
 {
     long long g = (work + threads - 1) / threads;
@@ -1088,12 +1106,14 @@ extern "C" twell_status twell_gemm_test(const void* A, const void* B, int32_t M,
 // Routing without any allocation or workspace.
 //
 // Some callers cannot hand the library a workspace or let anything allocate device memory: code
-// that runs while a CUDA graph is being captured (cudaMalloc is not allowed during capture), code
-// living inside a framework whose allocator owns all device memory, and latency-critical loops
-// where a cudaMalloc / cudaFree would synchronise the device. For them the routing of an already
-// packed TwELL matrix keeps its only scratch -- the number of overflow rows of each 128-row block
-// -- in the fixed array below. The array lives in every GPU that loads the library until the
-// process exits, and holds the previous call's counts (every call rewrites the entries it uses).
+// living inside a framework whose caching allocator owns all device memory (a second allocator
+// would fight it for the same HBM), plug-in hosts that pass only inputs and outputs across their
+// interface, and latency-critical loops where a cudaMalloc / cudaFree would synchronise the
+// device. For them the routing of an already packed TwELL matrix keeps its only scratch -- the
+// number of overflow rows of each 128-row block -- in the fixed array below. The array lives in
+// every GPU that loads the library until the process exits, and holds the previous call's counts;
+// nothing in it has to start at zero, because the first kernel of every call rewrites each entry
+// the second kernel reads. Calls that overlap on the GPU share the array and race.
 
 namespace {
 
@@ -1129,7 +1149,7 @@ extern "C" twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_
     if (a->dtype != TWELL_F32 || a->tile != twell::kHybTile) return TWELL_ERR_UNSUPPORTED;
     twell_status st = check_packed(a, N, f, twell::kHybTile, TWELL_F32);
     if (st != TWELL_OK) return st;
-    st = check_hybrid(ctx, N, f, K);
+    st = check_route_ctx(ctx, N, f, K);
     if (st != TWELL_OK) return st;
     const int nblk = (N + twell::kRouteRows - 1) / twell::kRouteRows;
     if (nblk > kNoAllocBlocks) return TWELL_ERR_UNSUPPORTED;  // more rows than the fixed scratch covers

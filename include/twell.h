@@ -321,9 +321,11 @@ TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t 
  * the routing inside twell_hybrid_fwd / twell_hybrid_route_from_gate (ctx->cnt, col, a,
  * backup_rows, n_backup, A_b; not u, U_b, l1) -- without any workspace and without allocating.
  * The pages have no counterpart: this call exists for callers that cannot allocate device memory
- * or pass a workspace (code recorded into a CUDA graph, where cudaMalloc is not allowed during
- * capture; code inside a framework whose allocator owns all device memory; latency-critical
- * loops where an allocation would synchronise the device).
+ * or pass a workspace (code inside a framework whose caching allocator owns all device memory;
+ * plug-in hosts whose interface carries only inputs and outputs; latency-critical loops where an
+ * allocation would synchronise the device). ctx->u, ctx->U_b and ctx->l1 are not used and may be
+ * null; cnt, n_backup, dev_status, and col and a (K > 0), backup_rows and A_b (backup_cap > 0)
+ * are required.
  * Its only scratch, the overflow-row count of each 128-row block, is a fixed array of 8192 int32
  * inside the library: every GPU that loads the library keeps it (32 KB) until the process exits.
  * Limit: a->n_rows <= 1,048,576; larger inputs return TWELL_ERR_UNSUPPORTED before any launch.

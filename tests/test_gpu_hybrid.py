@@ -173,23 +173,71 @@ def test_hybrid_all_rows_backup(cuda_dev):
         assert_close(got.double().cpu().numpy()[live], ref[live], name)
 
 
-def test_hybrid_full_size_training_layer_sampled(cuda_dev):
-    """The 2B-like training step (N=16384, d=2560, f=6912, K=64) on sampled rows and hidden units."""
-    L = synthetic.train_2b()
-    y, ctx, dx, dWg, dWu, dWd = _run_hybrid(cuda_dev, L, cap=2048)
+def _heaviest_units(dev, L, n):
+    """The n hidden units kept by the most tokens (from the library's own gate pack and column
+    counts: a choice of what to check, not an expected value)."""
+    t = L.torch_inputs(dev)
+    counts = binding.twell_column_activity(binding.twell_gate_pack(t["x"], t["Wg_s"], 128))
+    return torch.argsort(counts, descending=True)[:n].cpu().numpy()
+
+
+def _check_sampled(cuda_dev, L, cap, overflow_lo, overflow_hi, n_rows, n_cols, seed):
+    """y, dx on sampled rows (backup rows forced in) and dWg, dWu, dWd on sampled and on the
+    heaviest hidden units, against the oracle."""
+    y, ctx, dx, dWg, dWu, dWd = _run_hybrid(cuda_dev, L, cap=cap)
     assert binding.twell_read_status(ctx.status) == 0
     nb = int(ctx.n_backup.item())
-    assert 0.01 * L.N <= nb <= 0.04 * L.N
-    rng = np.random.default_rng(3)
+    assert overflow_lo * L.N <= nb <= overflow_hi * L.N, nb / L.N
+    rng = np.random.default_rng(seed)
     brows = ctx.backup_rows[:nb].cpu().numpy()
-    rows = np.unique(np.concatenate([[0, 1, L.N - 1], rng.choice(L.N, 12, replace=False), brows[:6]]))
+    rows = np.unique(np.concatenate([[0, 1, L.N - 1], rng.choice(L.N, n_rows, replace=False), brows[:6]]))
     y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
     sel = torch.from_numpy(rows).to(cuda_dev)
     assert_close(y[sel].double().cpu().numpy(), y_ref, "y (sampled rows)")
     dx_ref = oracle.ffn_bwd_rows(L.x, L.Wg_s, L.Wu_s, L.Wd_s, L.dy, L.l1_coef, rows=rows)
     assert_close(dx[sel].double().cpu().numpy(), dx_ref, "dx (sampled rows)")
-    cols = rng.choice(L.f, 8, replace=False)
+    heavy = _heaviest_units(cuda_dev, L, n_cols)
+    cols = np.unique(np.concatenate([rng.choice(L.f, n_cols, replace=False), heavy]))
     rg, ru, rd = oracle.ffn_bwd_cols(L.x, L.Wg_s, L.Wu_s, L.Wd_s, L.dy, L.l1_coef, cols=cols)
     csel = torch.from_numpy(cols).to(cuda_dev)
     for name, got, ref in (("dWg", dWg, rg), ("dWu", dWu, ru), ("dWd", dWd, rd)):
-        assert_close(got[csel].double().cpu().numpy(), ref, name + " (sampled hidden units)")
+        assert_close(got[csel].double().cpu().numpy(), ref, name + " (sampled and heaviest hidden units)")
+    return ctx, nb
+
+
+def test_hybrid_full_size_training_layer_sampled(cuda_dev):
+    """The 2B-like training step (N=16384, d=2560, f=6912, K=64) on sampled rows and hidden units
+    (8 random, 8 kept by the most tokens)."""
+    _check_sampled(cuda_dev, synthetic.train_2b(), 2048, 0.01, 0.04, 12, 8, seed=3)
+
+
+def test_hybrid_full_size_literal_density_sampled(cuda_dev):
+    """The training step on the 2B-like layer's own generator (mean density 0.5%, lognormal per
+    token, 10x on the first four positions of each sequence): ~13% of rows overflow K = 64, so the
+    dense backup carries the heavy case. Sampled rows (backup rows forced in) and hidden units."""
+    _check_sampled(cuda_dev, synthetic.train_2b(literal=True), 16384 // 4, 0.08, 0.2, 10, 8, seed=4)
+
+
+def test_hybrid_training_layer_full_width_l1_and_all_rows(cuda_dev):
+    """The 2B-like training layer's widths (d=2560, f=6912, K=64) on N = 2048 tokens: the L1 term
+    against the oracle's (reduced over all N*f hidden activations), y and dx on sampled rows
+    (backup rows forced in), and the weight gradients of the 8 heaviest units."""
+    L = synthetic.train_2b(N=2048)
+    y, ctx, dx, dWg, dWu, dWd = _run_hybrid(cuda_dev, L, cap=2048 // 4)
+    assert binding.twell_read_status(ctx.status) == 0
+    nb = int(ctx.n_backup.item())
+    assert nb > 0
+    l1_ref = oracle.l1(L.x, L.Wg_s, L.Wu_s, L.l1_coef)
+    assert abs(ctx.l1.item() - l1_ref) <= 5e-3 * abs(l1_ref), (ctx.l1.item(), l1_ref)
+    rng = np.random.default_rng(8)
+    brows = ctx.backup_rows[:nb].cpu().numpy()
+    rows = np.unique(np.concatenate([rng.choice(L.N, 64, replace=False), brows[:16]]))
+    sel = torch.from_numpy(rows).to(cuda_dev)
+    assert_close(y[sel].double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows), "y (sampled rows)")
+    dx_ref = oracle.ffn_bwd_rows(L.x, L.Wg_s, L.Wu_s, L.Wd_s, L.dy, L.l1_coef, rows=rows)
+    assert_close(dx[sel].double().cpu().numpy(), dx_ref, "dx (sampled rows)")
+    cols = _heaviest_units(cuda_dev, L, 8)
+    rg, ru, rd = oracle.ffn_bwd_cols(L.x, L.Wg_s, L.Wu_s, L.Wd_s, L.dy, L.l1_coef, cols=cols)
+    csel = torch.from_numpy(cols).to(cuda_dev)
+    for name, got, ref in (("dWg", dWg, rg), ("dWu", dWu, ru), ("dWd", dWd, rd)):
+        assert_close(got[csel].double().cpu().numpy(), ref, name + " (heaviest hidden units)")

@@ -477,7 +477,9 @@ def test_gather_rows_copies_and_checks(cuda_dev):
 
 def test_compacted_layer_gives_the_same_y(cuda_dev):
     """Live columns from a calibration batch, weights gathered to them: y is bit-identical to the
-    uncompacted layer on a different batch (1.5B-like shapes, 30% dead columns, N = 1024)."""
+    uncompacted layer on a different batch (1.5B-like shapes, 30% dead columns, N = 1024), and
+    matches the fp64 oracle's dense layer over all d_ff units (the dropped ones included) on every
+    row."""
     L = synthetic.layer_1p5b(N=1024)
     t = L.torch_inputs(cuda_dev)
     x_cal = torch.from_numpy(synthetic.calibration_tokens(L, 2048, seed=77)).to(cuda_dev, torch.bfloat16)
@@ -492,6 +494,7 @@ def test_compacted_layer_gives_the_same_y(cuda_dev):
     assert not (active & (counts.cpu().numpy() == 0)).any()
     y_c = binding.ffn_forward(t["x"], Wg_c, Wu_c, Wd_c, T=L.T)
     assert torch.equal(y_c, y)
+    assert_close(y_c.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), "compacted layer vs oracle")
 
 
 # ------------------------------------------------------------------------------------------ end to end
