@@ -23,7 +23,8 @@ TWELL_OK = 0
 TWELL_ERR_UNSUPPORTED = 2
 TWELL_BF16 = 0
 TWELL_F32 = 1
-OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD, OP_FFN_DECODE = range(7)
+(OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD, OP_FFN_DECODE,
+ OP_FFN_TILE_UNION_FWD) = range(8)
 DECODE_MAX_N = 16  # twell_ffn_decode takes batches of at most this many tokens
 STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED", 3: "TWELL_ERR_BACKUP_FULL",
                 4: "TWELL_ERR_TIMEOUT", 5: "TWELL_ERR_DEVICE_CHECK", 6: "TWELL_ERR_CUDA",
@@ -35,7 +36,8 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_pack_from_gate", "twell_hybrid_route_from_gate", "twell_hybrid_route_noalloc",
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe",
-           "twell_ffn_fused_fwd_f16down", "twell_convert_f16", "twell_ffn_decode")
+           "twell_ffn_fused_fwd_f16down", "twell_convert_f16", "twell_ffn_decode", "twell_ffn_tile_union_fwd",
+           "twell_count_nonzeros")
 
 
 class TwellError(RuntimeError):
@@ -83,6 +85,8 @@ def load(path: str = LIB_PATH):
                                              sz, vp, vp]),
                 "twell_ffn_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
                                              sz, vp, vp]),
+                "twell_ffn_tile_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
+                                                  vp, vp]),
                 "twell_wait_probe": (st, [i32, i32, vp, vp]),
                 "twell_ffn_fused_fwd_f16down": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
                                                      vp, vp]),
@@ -100,6 +104,7 @@ def load(path: str = LIB_PATH):
                 "twell_hybrid_route_noalloc": (st, [ctypes.POINTER(_Packed), i32, ctypes.POINTER(_Hybrid), vp]),
                 "twell_gate_gemm": (st, [vp, vp, i32, i32, i32, vp, vp, vp]),
                 "twell_column_activity": (st, [ctypes.POINTER(_Packed), vp, vp, vp]),
+                "twell_count_nonzeros": (st, [ctypes.POINTER(_Packed), vp, vp, vp]),
                 "twell_gather_rows": (st, [vp, i32, vp, i32, i32, ctypes.c_int, vp, vp, vp]),
                 "twell_gemm_test": (st, [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
                 "twell_read_status": (st, [vp, vp]),
@@ -375,6 +380,35 @@ def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
     return y
 
 
+_tile_union_ws = {}
+
+
+def twell_ffn_tile_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tensor, a: TwELL,
+                             y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                             stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The same y as twell_ffn_fused_fwd, as tensor-core GEMMs over each 128-token tile's union of kept
+    units (gathered weight rows); Wd16_s is Wd_s converted by twell_convert_f16."""
+    N, d = x.shape
+    f = Wu_s.shape[0]
+    if Wd16_s.dtype != torch.float16:
+        raise ValueError("Wd16_s must be fp16 (twell_convert_f16 of Wd_s)")
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    if ws is None:
+        n = twell_workspace_bytes(OP_FFN_TILE_UNION_FWD, N, d, f)
+        key = (x.device.index, _stream(stream).value or 0)
+        ws = _tile_union_ws.get(key)
+        if ws is None or ws.numel() < n:
+            ws = torch.empty(n, dtype=torch.uint8, device=x.device)
+            _tile_union_ws[key] = ws
+    s = a.c_struct()
+    _check(load().twell_ffn_tile_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd16_s), ctypes.byref(s), N, d, f, _ptr(y),
+                                           _ptr(ws), ws.numel(),
+                                           _ptr(status if status is not None else status_buffer(x.device)),
+                                           _stream(stream)),
+           "twell_ffn_tile_union_fwd")
+    return y
+
+
 _decode_ws = {}
 
 
@@ -403,27 +437,57 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
     return y, packed
 
 
+# Densities (kept fraction of d_ff per token) where the faster path changes, measured with gate +
+# path on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
+#   density         0.5%    1%      2%      5%      10%     50%
+#   walk            0.325   0.471   0.787   1.721   3.347   15.31
+#   tile union      0.378   0.481   0.584   0.686   0.789   1.627
+#   union (dense)   0.664   0.675   0.682   0.690   0.708   1.012
+TILE_UNION_MIN_DENSITY = 0.011
+TILE_UNION_MAX_DENSITY = 0.08
+
+
+def choose_path(n_tokens: int, density: Optional[float]) -> str:
+    """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the walk below
+    TILE_UNION_MIN_DENSITY (or without a density estimate); the tile-union GEMMs up to
+    TILE_UNION_MAX_DENSITY; above it the union GEMMs over all of d_ff."""
+    if n_tokens <= DECODE_MAX_N:
+        return "decode"
+    if density is None or density < TILE_UNION_MIN_DENSITY:
+        return "walk"
+    return "tile_union" if density < TILE_UNION_MAX_DENSITY else "union"
+
+
 def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
-                vals_dtype: torch.dtype = torch.float32, path: str = "walk"):
-    """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk") or, for a
-    layer too dense for the walk, twell_ffn_union_fwd (path "union"); path "decode" runs
-    twell_ffn_decode (at most DECODE_MAX_N tokens), path "auto" decode for such batches where the
-    library supports the shape, else the walk."""
+                vals_dtype: torch.dtype = torch.float32, path: str = "walk", Wd16_s: Optional[torch.Tensor] = None,
+                density: Optional[float] = None):
+    """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk"),
+    twell_ffn_tile_union_fwd (path "tile_union": needs Wd16_s = twell_convert_f16(Wd_s)) or
+    twell_ffn_union_fwd (path "union"); path "decode" runs twell_ffn_decode (at most DECODE_MAX_N
+    tokens). Path "auto" follows choose_path with `density`, the kept fraction of the previous batch
+    (twell_count_nonzeros / (N * d_ff)); without Wd16_s it stays on the walk."""
     if path == "auto":
-        if x.shape[0] <= DECODE_MAX_N:
+        path = choose_path(x.shape[0], density)
+        if path == "tile_union" and Wd16_s is None:
+            path = "walk"
+        if path == "decode":
             try:
                 return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                         vals_dtype=vals_dtype)[0]
             except TwellError as e:
                 if e.code != TWELL_ERR_UNSUPPORTED:
                     raise
-        path = "walk"
+            path = "walk"
     if path == "decode":
         return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                 vals_dtype=vals_dtype)[0]
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
     if path == "union":
         return twell_ffn_union_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
+    if path == "tile_union":
+        if Wd16_s is None:
+            raise ValueError('path "tile_union" needs Wd16_s (twell_convert_f16(Wd_s))')
+        return twell_ffn_tile_union_fwd(x, Wu_s, Wd16_s, a, y=y, status=status, stream=stream)
     if path != "walk":
         raise ValueError(f"unknown path {path!r}")
     return twell_ffn_fused_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
@@ -447,6 +511,17 @@ def twell_column_activity(a: TwELL, counts: Optional[torch.Tensor] = None, statu
                                         _stream(stream)),
            "twell_column_activity")
     return counts
+
+
+def twell_count_nonzeros(a: TwELL, total: Optional[torch.Tensor] = None, status=None, stream=None) -> torch.Tensor:
+    """Device int64 [1]: the number of kept entries of `a` (added to `total`, zeros if None)."""
+    total = total if total is not None else torch.zeros(1, dtype=torch.int64, device=a.vals.device)
+    s = a.c_struct()
+    _check(load().twell_count_nonzeros(ctypes.byref(s), _ptr(total),
+                                       _ptr(status if status is not None else status_buffer(total.device)),
+                                       _stream(stream)),
+           "twell_count_nonzeros")
+    return total
 
 
 def twell_gather_rows(src: torch.Tensor, rows: torch.Tensor, out: Optional[torch.Tensor] = None, status=None,

@@ -92,6 +92,23 @@ __global__ void column_activity_kernel(const uint8_t* __restrict__ idx, const ui
     }
 }
 
+// total += the sum of the TwELL counts (its kept entries); a count above the tile width is
+// recorded and counted as 0. Grid-stride over the counts, a warp sum, one atomic per warp.
+__global__ void count_nonzeros_kernel(const uint16_t* __restrict__ cnt, long long n, int T,
+                                      unsigned long long* __restrict__ total, int32_t* status)
+{
+    unsigned long long s = 0;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int c = cnt[i];
+        if (c > T) report(status, TWELL_ERR_DEVICE_CHECK);
+        else s += static_cast<unsigned long long>(c);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0 && s != 0) atomicAdd(total, s);
+}
+
 // dst[i, :] = src[rows[i], :] in 16-byte chunks; a row index outside [0, n_src) is recorded and
 // its output row is zero.
 __global__ void gather_rows_checked_kernel(const uint4* __restrict__ src, int n_src, const int32_t* __restrict__ rows,
@@ -195,6 +212,25 @@ extern "C" twell_status twell_column_activity(const twell_packed* a, int32_t* co
     if (warps / 8 + 1 > 0x7fffffffLL) return TWELL_ERR_UNSUPPORTED;
     twell::column_activity_kernel<<<warp_blocks(warps, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         a->idx, a->cnt, N, f, T, nt, col_counts, dev_status);
+    return launch_status();
+}
+
+extern "C" twell_status twell_count_nonzeros(const twell_packed* a, unsigned long long* total, int32_t* dev_status,
+                                             void* stream)
+{
+    if (a == nullptr || dev_status == nullptr || total == nullptr) return TWELL_ERR_INVALID;
+    if (!dtype_ok(a->dtype)) return TWELL_ERR_UNSUPPORTED;
+    const int N = a->n_rows, f = a->n_cols, T = a->tile;
+    if (N < 0 || f <= 0) return TWELL_ERR_INVALID;
+    twell_status st = check_packed(a, N, f, T, a->dtype);
+    if (st != TWELL_OK) return st;
+    if (N == 0) return TWELL_OK;
+    DevInfo di;
+    if (dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    const long long n = static_cast<long long>(N) * ((f + T - 1) / T);
+    const long long need = (n + 255) / 256;
+    const int grid = static_cast<int>(need < 4ll * di.sm_count ? need : 4ll * di.sm_count);
+    twell::count_nonzeros_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(a->cnt, n, T, total, dev_status);
     return launch_status();
 }
 

@@ -743,6 +743,7 @@ def run_sweep(a):
         union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
         Wd16 = binding.twell_convert_f16(Wd, status=status)
         f16_fn = lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
+        tu_fn = lambda: binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
 
         def dense_fn():
             return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
@@ -753,12 +754,14 @@ def run_sweep(a):
             ms_fused = timed_in_graph(fused_fn, 50)
             ms_union = timed_in_graph(union_fn, 50)
             ms_f16 = timed_in_graph(f16_fn, 50)
+            ms_tu = timed_in_graph(tu_fn, 50)
             ms_dense = timed_in_graph(dense_fn, 50)
         else:
             ms_gate = timed(gate_fn, n_it)
             ms_fused = timed(fused_fn, n_it)
             ms_union = timed(union_fn, max(3, min(n_it, 15)))
             ms_f16 = timed(f16_fn, n_it)
+            ms_tu = timed(tu_fn, n_it)
             ms_dense = timed(dense_fn, n_it)
         decode = None
         if L.N <= binding.DECODE_MAX_N:
@@ -778,13 +781,21 @@ def run_sweep(a):
         binding.check_device_status(label, status)
         ms = ms_gate + ms_fused
         ms_u = ms_gate + ms_union
-        best = "walk" if ms <= ms_u else "union"
+        ms_t = ms_gate + ms_tu
+        best = min((("walk", ms), ("union", ms_u), ("tile_union", ms_t)), key=lambda kv: kv[1])[0]
+        auto = binding.choose_path(L.N, nnz / (L.N * L.f))
+        ms_auto = {"decode": None, "walk": ms, "tile_union": ms_t, "union": ms_u}[auto]
+        if ms_auto is None:
+            ms_auto = decode["ms"] if decode else ms
         print(json.dumps({"sweep": label, "workload": L.name, "N": L.N, "d_model": L.d, "d_ff": L.f, "T": L.T,
                           "density": nnz / (L.N * L.f), "nnz_per_token": nnz / L.N, "ms_gate_pack": ms_gate,
                           "ms_fused": ms_fused, "ms_sparse": ms, "tokens_per_s": L.N / (ms * 1e-3),
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
                           "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
-                          "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u),
+                          "ms_tile_union": ms_tu, "ms_sparse_tile_union": ms_t,
+                          "speedup_tile_union_vs_dense": ms_dense / ms_t,
+                          "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u, ms_t),
+                          "auto_path": auto, "speedup_auto_vs_dense": ms_dense / ms_auto,
                           "f16down": {"ms_walk": ms_f16, "ms_step": ms_gate + ms_f16,
                                       "speedup_vs_dense": ms_dense / (ms_gate + ms_f16)},
                           "decode": decode,
@@ -793,6 +804,7 @@ def run_sweep(a):
                                      "[L2 flush]) / 50, median of 3" if use_graphs else
                                      f"CUDA events around each call, median of {n_it}")}), flush=True)
         del t, x, Wg, Wu, Wd, Wd16, packed, y
+        binding._tile_union_ws.clear()
         torch.cuda.empty_cache()
 
 

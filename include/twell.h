@@ -67,7 +67,8 @@ typedef enum {
     TWELL_OP_HYBRID_BWD = 3,
     TWELL_OP_HYBRID_ROUTE = 4,
     TWELL_OP_FFN_UNION_FWD = 5,
-    TWELL_OP_FFN_DECODE = 6
+    TWELL_OP_FFN_DECODE = 6,
+    TWELL_OP_FFN_TILE_UNION_FWD = 7
 } twell_op;
 
 /* A TwELL matrix of gate activations a = ReLU(G), [n_rows, n_cols] ([TG] "Вот тут и решает TwELL";
@@ -221,9 +222,9 @@ TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const v
  * tensor cores for the heavy work). Steps: a = the TwELL expanded to dense bf16 [N, f_pad]
  * (f_pad = f rounded up to 64); H = (x Wu_s^T) * a (tcgen05 GEMM, product in its epilogue) kept
  * as two bf16 terms hi + lo (~16 significant bits, as in the walk); y = [hi | lo] [Wd_s ; Wd_s]
- * (tcgen05 GEMM over 2 f_pad). Which of
- * the two to call is the caller's policy, e.g. from the density of the previous batch
- * (twell_column_activity); the walk wins below ~0.6% of d_ff per token on the 1.5B-like shapes.
+ * (tcgen05 GEMM over 2 f_pad). twell_ffn_tile_union_fwd below computes the same y over each
+ * tile's union only, with h in fp16 (one down product over |U_m| instead of two over f_pad), and is
+ * faster at every density measured; this call is kept for layers without an fp16 copy of Wd_s.
  * bf16 only; d and f multiples of 8; x [N, d], Wu_s / Wd_s [f, d], y [N, d], device, 16-byte
  * aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (dense a and
  * [hi | lo] of H, 6*N*f_pad bytes), required when N > 0. A corrupt TwELL (count above the tile width, column >= f) is
@@ -233,6 +234,28 @@ TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, cons
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);
+
+/* y = (a * (x Wu_s^T)) Wd_s from the TwELL a, as tensor-core GEMMs over the units each tile of
+ * 128 tokens keeps -- the tile's union U_m -- with the union's weight rows gathered ([TG] "Инференс":
+ * the kernel gathers only the needed rows of Wu and Wd; [TC] §3: tensor cores take the heavy work).
+ * Per tile m: H_m[r, p] = a[r, U_m[p]] * (x_r . Wu_s[U_m[p]]) over p < |U_m| (tcgen05, B = gathered
+ * Wu_s rows, the product in the epilogue, h stored once as fp16), then y_m = H_m Wd16_s[U_m]
+ * (tcgen05 over K = |U_m|, B = gathered rows of Wd16_s). Each weight row is read once per tile of
+ * 128 tokens instead of once per token that keeps it. Wd16_s is Wd_s converted to fp16 once
+ * (twell_convert_f16: the same values for weights of magnitude 2^-14 .. 65504; smaller ones move by
+ * at most 2^-25); h carries 11 significant bits.
+ * x [N, d] bf16, Wu_s [f, d] bf16, Wd16_s [f, d] fp16, y [N, d] bf16, all device, 32-byte aligned;
+ * d a multiple of 64 (else TWELL_ERR_UNSUPPORTED); f <= 65535; a: any tile width, fp32 or bf16
+ * values. ws: twell_workspace_bytes(TWELL_OP_FFN_TILE_UNION_FWD, N, d, f, ...) bytes, 32-byte
+ * aligned, required when N > 0 (per tile: the union list and bitmap; H as fp16 [N, f rounded up to
+ * 256]); its contents need not be initialised; two calls in flight at the same time must not share
+ * it. A corrupt TwELL entry (count above the tile width, in-tile index >= T, column >= f) is
+ * recorded as TWELL_ERR_DEVICE_CHECK and contributes nothing; so is an h beyond the fp16 range
+ * (|h| >= 65520, stored as infinity).
+ */
+TWELL_API twell_status twell_ffn_tile_union_fwd(const void* x, const void* Wu_s, const void* Wd16_s,
+                                                const twell_packed* a, int32_t N, int32_t d, int32_t f, void* y,
+                                                void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Hybrid-format training forward ([TG] "Обучение"; [TC] §3), bf16 only (d_ff a multiple of
  * 64, d_model at most 4096, d_ff at most 65535): gate GEMM + TwELL pack,
@@ -277,6 +300,13 @@ TWELL_API twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const v
  * the same y, bit for bit, on any batch whose active units are among them. The pages state the
  * observation, not this procedure.
  */
+
+/* *total += the number of kept entries of `a` (the sum of its counts; device uint64, the caller
+ * clears it): the batch's density is *total / (n_rows * n_cols), which is what a caller needs to
+ * choose between twell_ffn_fused_fwd and twell_ffn_tile_union_fwd for the next batch. A count above
+ * the tile width is reported as TWELL_ERR_DEVICE_CHECK and counts as 0. Asynchronous on `stream`. */
+TWELL_API twell_status twell_count_nonzeros(const twell_packed* a, unsigned long long* total, int32_t* dev_status,
+                                            void* stream);
 
 /* col_counts[j] += the number of rows of `a` that keep column j (device int32 [a->n_cols]; the
  * call adds to what is there, the caller clears it). A bad entry (count above the tile width,

@@ -1,0 +1,18 @@
+"""Host-side path policy of binding.ffn_forward(path="auto") (no GPU)."""
+from activation_sparse_ffn_gate_gb300 import binding
+
+
+def test_small_batches_take_the_decode_path():
+    for n in (1, 8, binding.DECODE_MAX_N):
+        assert binding.choose_path(n, None) == "decode"
+        assert binding.choose_path(n, 0.05) == "decode"
+
+
+def test_density_chooses_walk_or_tile_union():
+    n = binding.DECODE_MAX_N + 1
+    assert binding.choose_path(n, None) == "walk"  # no estimate yet: the walk
+    assert binding.choose_path(n, 0.005) == "walk"
+    assert binding.choose_path(n, binding.TILE_UNION_MIN_DENSITY) == "tile_union"
+    assert binding.choose_path(8192, 0.02) == "tile_union"
+    assert binding.choose_path(8192, binding.TILE_UNION_MAX_DENSITY) == "union"
+    assert binding.choose_path(8192, 0.5) == "union"
