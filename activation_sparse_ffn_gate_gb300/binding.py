@@ -316,10 +316,12 @@ class StreamedFFN:
     kernels and their results are those of ffn_forward."""
 
     def __init__(self, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, N: int, T: int = 128,
-                 path: str = "walk", vals_dtype: torch.dtype = torch.float32, status: Optional[torch.Tensor] = None):
+                 path: str = "walk", vals_dtype: torch.dtype = torch.float32, status: Optional[torch.Tensor] = None,
+                 Wd16_s: Optional[torch.Tensor] = None):
         dev = Wg_s.device
         f, d = Wg_s.shape
         self.W, self.T, self.path, self.status, self.N, self.d = (Wg_s, Wu_s, Wd_s), T, path, status, N, d
+        self.Wd16 = Wd16_s
         self.copy_in, self.compute, self.copy_out = (torch.cuda.Stream(dev) for _ in range(3))
         self.x = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
         self.y = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
@@ -345,7 +347,7 @@ class StreamedFFN:
             if later:
                 self.compute.wait_event(self.y_out[b])  # y[b] of batch count-2 is on the host
             ffn_forward(self.x[b], *self.W, T=self.T, packed=self.packed, y=self.y[b], status=self.status,
-                        stream=self.compute, path=self.path)
+                        stream=self.compute, path=self.path, Wd16_s=self.Wd16)
             self.done[b].record(self.compute)
         with torch.cuda.stream(self.copy_out):
             self.copy_out.wait_event(self.done[b])

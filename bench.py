@@ -57,6 +57,12 @@ def _args():
     p.add_argument("--config", type=int, choices=[1, 2], default=1,
                    help="workload of the main line: 1 = the 1.5B-like layer (default), 2 = the 2B-like layer "
                         "(N=16384, d_model 2560, d_ff 6912, lognormal per-token density; no dead-column step)")
+    p.add_argument("--path", choices=["walk", "tile_union"], default="walk",
+                   help="second call of the step: the fused walk (default) or the tile-union GEMMs "
+                        "(twell_ffn_tile_union_fwd, Wd_s converted to fp16 once outside the timed region)")
+    p.add_argument("--density", type=float, default=None,
+                   help="run the main line on the sweep's uniform-density layer (N=8192, d_model 2048, d_ff 5632, "
+                        "T=128) with this kept fraction instead of the --config layer")
     p.add_argument("--train-only", action="store_true",
                    help="only the hybrid training step against the dense cuBLAS step (one JSON line)")
     p.add_argument("--sweep", action="store_true",
@@ -258,7 +264,11 @@ def run_ours(a, rank, world):
         dist.init_process_group("nccl", device_id=dev)
 
     # every rank its own batch (weak scaling)
-    L = synthetic.layer_1p5b(seed=1 + rank) if a.config == 1 else synthetic.layer_2b(seed=2 + rank)
+    if a.density is not None:
+        L = synthetic.sweep_point(a.density, 128, seed=3 + rank)
+    else:
+        L = synthetic.layer_1p5b(seed=1 + rank) if a.config == 1 else synthetic.layer_2b(seed=2 + rank)
+    main_cfg1 = a.density is None and a.config == 1
     t = L.torch_inputs(dev)
     x, Wg, Wu, Wd = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"]
     N, d, f, T = L.N, L.d, L.f, L.T
@@ -270,9 +280,17 @@ def run_ours(a, rank, world):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
+    Wd16 = binding.twell_convert_f16(Wd, status=status, stream=stream) if a.path == "tile_union" else None
+
+    def second():
+        if a.path == "tile_union":
+            binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status, stream=stream)
+        else:
+            binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+
     def step():
         binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
-        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+        second()
 
     for _ in range(a.warmup):
         flush.fill_(1)
@@ -295,7 +313,7 @@ def run_ours(a, rank, world):
         e0.record(stream)
         binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
         e1.record(stream)
-        binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
+        second()
         e2.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -348,7 +366,17 @@ def run_ours(a, rank, world):
     # per-kernel algorithmic work
     fused_bytes = (N * d * 2) + union * 2 * d * 2 + (N * d * 2) + twell_bytes
     mg, mf = sum(t_gate) / a.steps, sum(t_fused) / a.steps
-    if mf >= mg:
+    second_name = "twell_ffn_tile_union_fwd" if a.path == "tile_union" else "twell_ffn_fused_fwd"
+    if a.path == "tile_union" and mf >= mg:
+        # the up and down GEMMs over each 128-token tile's union: 2 * 128 * |U_m| * d FLOPs each per tile
+        tu_flops = 4.0 * 128 * union * d
+        ach = tu_flops / (mf * 1e-3) / 1e12
+        roof = {"kernel": second_name, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                "algorithmic_flops": tu_flops, "ms_per_launch": mf,
+                "peak_kind": peak_kind + " bf16_tflops (burst; the down GEMM runs fp16, the same rate)",
+                "note": "whole call (union, expand, up and down GEMMs) against the union GEMMs' FLOPs"}
+    elif mf >= mg:
         # The walk moves, per kept entry, the unit's rows of Wu_s and Wd_s (2 * d * 2 B) from L2 into
         # shared memory, plus x_r once per row: these gathers, not HBM, bound it (ncu: DRAM ~9% busy).
         gathered = nnz * 2 * d * 2 + N * d * 2
@@ -356,7 +384,7 @@ def run_ours(a, rank, world):
         ach = fused_bytes / (mf * 1e-3) / 1e9
         roof = {"kernel": "twell_ffn_fused_fwd", "bound": "l2", "achieved": ach_l2, "peak": L2_GATHER_GBS,
                 "unit": "GB/s", "frac": ach_l2 / L2_GATHER_GBS,
-                "traffic": _traffic("fused") if a.config == 1 else None,
+                "traffic": _traffic("fused") if main_cfg1 else None,
                 "algorithmic_bytes": gathered, "ms_per_launch": mf,
                 "peak_kind": L2_GATHER_KIND,
                 "limiter": "L2 -> SM gathers of weight rows and the per-nonzero instruction chain (latency; "
@@ -371,7 +399,7 @@ def run_ours(a, rank, world):
         ach = gate_flops / (mg * 1e-3) / 1e12
         roof = {"kernel": "twell_gate_pack", "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                "traffic": _traffic("gate") if a.config == 1 else None,
+                "traffic": _traffic("gate") if main_cfg1 else None,
                 "algorithmic_flops": gate_flops, "ms_per_launch": mg, "peak_kind": peak_kind + " bf16_tflops (burst)"}
 
     # ---- dense cuBLAS bf16 FFN of the same shape (best of two formulations)
@@ -417,19 +445,21 @@ def run_ours(a, rank, world):
     e2e_steps = max(10, min(a.steps, 200))
     for _ in range(3):
         xd.copy_(xh, non_blocking=True)
-        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream)
+        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream, path=a.path,
+                            Wd16_s=Wd16)
         yh.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record(stream)
     for _ in range(e2e_steps):
         xd.copy_(xh, non_blocking=True)
-        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream)
+        binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream, path=a.path,
+                            Wd16_s=Wd16)
         yh.copy_(y, non_blocking=True)
     s1.record(stream)
     torch.cuda.synchronize()
     e2e_serial_ms = s0.elapsed_time(s1) / e2e_steps
-    pipe = binding.StreamedFFN(Wg, Wu, Wd, N, T=T, status=status)
+    pipe = binding.StreamedFFN(Wg, Wu, Wd, N, T=T, status=status, path=a.path, Wd16_s=Wd16)
     for _ in range(3):
         pipe.submit(xh, yh)
     torch.cuda.synchronize()
@@ -463,7 +493,7 @@ def run_ours(a, rank, world):
 
     compacted = None
     Wu_c = Wd_c = Wg_c = packed_c = None
-    if a.config == 1:
+    if main_cfg1 and a.path == "walk":
         x_cal = torch.from_numpy(synthetic.calibration_tokens(L, N, seed=1000 + rank)).to(dev, torch.bfloat16)
         counts = binding.twell_column_activity(binding.twell_gate_pack(x_cal, Wg, T, status=status), status=status)
         live = binding.live_columns(counts)
@@ -493,7 +523,7 @@ def run_ours(a, rank, world):
 
     # ---- the walk with its down projection in fp16 (Wd_s converted once; h rounded once to fp16)
     f16 = None
-    if not a.no_f16down:
+    if not a.no_f16down and a.path == "walk":
         n16 = max(10, min(a.steps, 200))
         Wd16 = binding.twell_convert_f16(Wd, status=status, stream=stream)
         y16 = torch.empty_like(y)
@@ -569,7 +599,7 @@ def run_ours(a, rank, world):
                            "distinct_active_units": distinct,
                            "definition_strict": "every active weight row read once per layer: max(gate FLOPs / bf16 "
                                                 "peak, (x + Wg + distinct active Wu/Wd rows + y) / HBM peak)"},
-        "kernels_ms": {"twell_gate_pack": mg, "twell_ffn_fused_fwd": mf},
+        "kernels_ms": {"twell_gate_pack": mg, second_name: mf},
         "compacted": compacted,
         "f16down": f16,
         "warm": {"ms_per_step": warm_ms, "tokens_per_s": weak_scaling_rate(N, warm_ms, world),
@@ -583,7 +613,10 @@ def run_ours(a, rank, world):
                        "steps' gate + walk (three streams, double-buffered device x and y)",
                 "serial": {"value": N / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
                            "how": "copy in, gate + walk, copy out one after the other on one stream"}},
-        "gpu_launches": 3 * a.steps,  # per step: gate + pack, the walk's plan, the walk
+        # per step: gate + pack, then the walk's plan and the walk, or the tile-union path's union bits,
+        # prefix, work list, expand, up GEMM and down GEMM (plus a memset of the union bitmaps)
+        "gpu_launches": (3 if a.path == "walk" else 7) * a.steps,
+        "path": a.path,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
