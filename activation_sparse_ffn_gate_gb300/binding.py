@@ -359,12 +359,15 @@ class StreamedFFN:
 _union_ws = {}
 
 
-def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, a: TwELL,
+def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tensor, a: TwELL,
                         y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                         stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """The same y as twell_ffn_fused_fwd, as two tensor-core GEMMs over all of d_ff (for dense layers)."""
+    """The same y as twell_ffn_fused_fwd, as two tensor-core GEMMs over all of d_ff (for dense layers);
+    Wd16_s is Wd_s converted by twell_convert_f16."""
     N, d = x.shape
     f = Wu_s.shape[0]
+    if Wd16_s.dtype != torch.float16:
+        raise ValueError("Wd16_s must be fp16 (twell_convert_f16 of Wd_s)")
     y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
     if ws is None:
         n = twell_workspace_bytes(OP_FFN_UNION_FWD, N, d, f)
@@ -374,7 +377,7 @@ def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor,
             ws = torch.empty(n, dtype=torch.uint8, device=x.device)
             _union_ws[key] = ws
     s = a.c_struct()
-    _check(load().twell_ffn_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd_s), ctypes.byref(s), N, d, f,
+    _check(load().twell_ffn_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd16_s), ctypes.byref(s), N, d, f,
                                       _dtype_code(x.dtype), _ptr(y), _ptr(ws), ws.numel(),
                                       _ptr(status if status is not None else status_buffer(x.device)),
                                       _stream(stream)),
@@ -439,38 +442,38 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
     return y, packed
 
 
-# Densities (kept fraction of d_ff per token) where the faster path changes, measured with gate +
-# path on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
-#   density         0.5%    1%      2%      5%      10%     50%
-#   walk            0.325   0.471   0.787   1.721   3.347   15.31
-#   tile union      0.378   0.481   0.584   0.686   0.789   1.627
-#   union (dense)   0.664   0.675   0.682   0.690   0.708   1.012
-TILE_UNION_MIN_DENSITY = 0.011
-TILE_UNION_MAX_DENSITY = 0.08
+# Density (kept fraction of d_ff per token) above which the union GEMMs beat the walk, measured with
+# gate + path on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
+#   density                0.1%    0.5%    1%      2%      5%      10%     50%
+#   walk                   0.191   0.328   0.471   0.787   1.723   3.336   15.34
+#   union (all of d_ff)    0.399   0.412   0.423   0.445   0.493   0.561   1.095
+#   tile union (gathered)  0.236   0.376   0.484   0.589   0.689   0.793   1.627
+# The gathered tile-union path is never the fastest under these uniform densities (nor on the
+# lognormal 2B-like layer, where the walk wins); it stays available as path "tile_union".
+UNION_MIN_DENSITY = 0.008
 
 
 def choose_path(n_tokens: int, density: Optional[float]) -> str:
     """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the walk below
-    TILE_UNION_MIN_DENSITY (or without a density estimate); the tile-union GEMMs up to
-    TILE_UNION_MAX_DENSITY; above it the union GEMMs over all of d_ff."""
+    UNION_MIN_DENSITY (or without a density estimate); the union GEMMs over all of d_ff above it."""
     if n_tokens <= DECODE_MAX_N:
         return "decode"
-    if density is None or density < TILE_UNION_MIN_DENSITY:
+    if density is None or density < UNION_MIN_DENSITY:
         return "walk"
-    return "tile_union" if density < TILE_UNION_MAX_DENSITY else "union"
+    return "union"
 
 
 def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
                 vals_dtype: torch.dtype = torch.float32, path: str = "walk", Wd16_s: Optional[torch.Tensor] = None,
                 density: Optional[float] = None):
     """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk"),
-    twell_ffn_tile_union_fwd (path "tile_union": needs Wd16_s = twell_convert_f16(Wd_s)) or
-    twell_ffn_union_fwd (path "union"); path "decode" runs twell_ffn_decode (at most DECODE_MAX_N
+    twell_ffn_tile_union_fwd (path "tile_union") or twell_ffn_union_fwd (path "union"), the latter two
+    with Wd16_s = twell_convert_f16(Wd_s); path "decode" runs twell_ffn_decode (at most DECODE_MAX_N
     tokens). Path "auto" follows choose_path with `density`, the kept fraction of the previous batch
     (twell_count_nonzeros / (N * d_ff)); without Wd16_s it stays on the walk."""
     if path == "auto":
         path = choose_path(x.shape[0], density)
-        if path == "tile_union" and Wd16_s is None:
+        if path in ("tile_union", "union") and Wd16_s is None:
             path = "walk"
         if path == "decode":
             try:
@@ -484,12 +487,11 @@ def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = Non
         return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                 vals_dtype=vals_dtype)[0]
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
-    if path == "union":
-        return twell_ffn_union_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)
-    if path == "tile_union":
+    if path in ("union", "tile_union"):
         if Wd16_s is None:
-            raise ValueError('path "tile_union" needs Wd16_s (twell_convert_f16(Wd_s))')
-        return twell_ffn_tile_union_fwd(x, Wu_s, Wd16_s, a, y=y, status=status, stream=stream)
+            raise ValueError(f'path "{path}" needs Wd16_s (twell_convert_f16(Wd_s))')
+        fn = twell_ffn_union_fwd if path == "union" else twell_ffn_tile_union_fwd
+        return fn(x, Wu_s, Wd16_s, a, y=y, status=status, stream=stream)
     if path != "walk":
         raise ValueError(f"unknown path {path!r}")
     return twell_ffn_fused_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)

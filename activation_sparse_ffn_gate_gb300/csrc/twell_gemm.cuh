@@ -1,6 +1,7 @@
 // twell_gemm.cuh -- persistent warp-specialised tcgen05 GEMM for sm_103a with pluggable epilogues.
 //
-//   C[M, N] = A[M, K] * B[K, N]     bf16 operands, fp32 accumulation in tensor memory (TMEM)
+//   C[M, N] = A[M, K] * B[K, N]     bf16 (or, with F16, fp16) operands, fp32 accumulation in
+//                                     tensor memory (TMEM)
 //
 // A is K-major ([M, K] row-major) or MN-major ([K, M] row-major); B is K-major ([N, K] row-major,
 // i.e. the "rows of W" layout) or MN-major ([K, N] row-major). Tiles are 128 x BN x 64; TMA
@@ -38,6 +39,8 @@
 // the MMA thread waits (bounded) for its last tcgen05 operations, and TMEM is freed before exit.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "twell_common.cuh"
 
 namespace twell {
@@ -51,6 +54,8 @@ enum class Epi : int {
     ScatterF32 = 5,  // out[rowmap[m], n] = acc (fp32)
     MulBF16 = 6,     // out[m, n] = bf16(acc * aux[m, n]), aux bf16
     MulHiLoBF16 = 7, // v = acc * aux[m, n]: out[m, n] = hi = bf16(v), out[m, n + lo_offset] = bf16(v - hi)
+    MulMaskF16 = 8,  // out[m, n] = fp16(acc * aux[m, n]) where bit n of mask row m is set, else 0; aux
+                     // fp16 (may be out itself: each element is read before it is written, by one thread)
 };
 
 struct GemmArgs {
@@ -69,6 +74,8 @@ struct GemmArgs {
     const void* aux;         // MulBF16, MulHiLoBF16: bf16 factor matrix [M, ldaux]
     int64_t ldaux;
     int64_t lo_offset;       // MulHiLoBF16: columns between a value's hi and lo parts
+    const uint32_t* mask;    // MulMaskF16: bit n of word mask[m * ldmask + n / 32] selects column n of row m
+    int64_t ldmask;
     // PackTwell
     int vals_f32;  // packed values stored as fp32 (else bf16, rounded to nearest even)
     void* vals;
@@ -94,7 +101,7 @@ struct GemmCfg {
     static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 };
 
-template <int BN, bool A_MN, bool B_MN, Epi EPI, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, Epi EPI, bool PAIR, bool F16 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs g)
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     using C = GemmCfg<BN, PAIR>;
     constexpr int CG = PAIR ? 2 : 1;
     constexpr int STAGES = C::STAGES;
-    constexpr uint32_t IDESC = idesc_bf16_f32(CG * kBM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = F16 ? idesc_f16_f32(CG * kBM, BN, A_MN, B_MN) : idesc_bf16_f32(CG * kBM, BN, A_MN, B_MN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -355,6 +362,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 }
                             }
                         }
+                    } else if constexpr (EPI == Epi::MulMaskF16) {
+                        const uint32_t km = g.mask[static_cast<size_t>(row) * g.ldmask + col0 / 32];
+                        const uint4* ax = reinterpret_cast<const uint4*>(static_cast<const __half*>(g.aux) +
+                                                                         static_cast<size_t>(row) * g.ldaux + col0);
+                        uint4* o = reinterpret_cast<uint4*>(static_cast<__half*>(g.out) + static_cast<size_t>(row) * g.ldo +
+                                                            col0);
+                        uint4 av[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) av[i] = ax[i];  // col0 + 32 <= N: the columns are whole chunks
+                        bool over = false;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t aw[4] = {av[i].x, av[i].y, av[i].z, av[i].w};
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = 8 * i + 2 * e;
+                                const float2 af = __half22float2(*reinterpret_cast<const __half2*>(&aw[e]));
+                                const float h0 = ((km >> c) & 1u) ? af.x * v[c] : 0.0f;
+                                const float h1 = ((km >> (c + 1)) & 1u) ? af.y * v[c + 1] : 0.0f;
+                                over |= !(fabsf(h0) < 65520.0f) || !(fabsf(h1) < 65520.0f);
+                                const __half2 hh = __floats2half2_rn(h0, h1);
+                                ow[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                            }
+                            o[i] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                        if (over) report(g.status, TWELL_ERR_DEVICE_CHECK);
                     } else {
                         const int orow = (EPI == Epi::ScatterBF16) ? g.rowmap[row] : row;
                         __nv_bfloat16* o = static_cast<__nv_bfloat16*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0;
@@ -440,14 +474,14 @@ namespace twell_host {
 
 // Operand description for the host launcher.
 struct GemmOperand {
-    const void* ptr;  // bf16 row-major matrix
+    const void* ptr;  // row-major matrix of 16-bit elements (bf16, or fp16 with F16)
     int64_t rows, cols, ld;
 };
 
 // Launch C = A * B with the tcgen05 kernel. A: [M, K] (a_mn = false) or [K, M] (a_mn = true);
 // B: [N, K] (b_mn = false) or [K, N] (b_mn = true); B2 (optional) continues B along K from
 // k-block kb_split on. Returns TWELL_ERR_CUDA on a tensor-map or launch failure.
-template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR = false>
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR = false, bool F16 = false>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
                          cudaStream_t stream);
 
@@ -455,7 +489,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
 
 namespace twell_host {
 
-template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR, bool F16>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
                          cudaStream_t stream)
 {
@@ -487,7 +521,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         tb2 = tb;
         g.kb_split = 1 << 30;
     }
-    auto kern = twell::tc_gemm_kernel<BN, A_MN, B_MN, EPI, PAIR>;
+    auto kern = twell::tc_gemm_kernel<BN, A_MN, B_MN, EPI, PAIR, F16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM_BYTES)) !=
         cudaSuccess)
         return TWELL_ERR_CUDA;

@@ -258,12 +258,6 @@ __device__ __forceinline__ void cp_async_wait_group()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Instruction descriptor of kind::f16 with fp16 A and B (fp32 D).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn)
-{
-    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
 
 // The up GEMM (UP: work units (tile, 256 union positions), K = d_model) and the down GEMM (work
 // units (tile, 256 columns of y), K = |U_m|): one persistent launch each, one CTA per SM.

@@ -817,8 +817,8 @@ def run_sweep(a):
         n_it = a.sweep_iters if nnz / L.N < 400 else max(3, a.sweep_iters // 3)
         gate_fn = lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)  # noqa: E731
         fused_fn = lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
-        union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
         Wd16 = binding.twell_convert_f16(Wd, status=status)
+        union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
         f16_fn = lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
         tu_fn = lambda: binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
 

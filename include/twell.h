@@ -216,21 +216,21 @@ TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const v
                               int32_t N, int32_t d, int32_t f, int32_t T, const twell_packed* a_out,
                               void* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
-/* The same y from the same TwELL for a layer too dense for the walk: with more than ~1% of
- * d_ff kept per token the union of the units a tile of 128 tokens keeps is most of d_ff, so the
- * up and down projections are dense contractions over all of it, on the tensor cores ([TC] §3:
- * tensor cores for the heavy work). Steps: a = the TwELL expanded to dense bf16 [N, f_pad]
- * (f_pad = f rounded up to 64); H = (x Wu_s^T) * a (tcgen05 GEMM, product in its epilogue) kept
- * as two bf16 terms hi + lo (~16 significant bits, as in the walk); y = [hi | lo] [Wd_s ; Wd_s]
- * (tcgen05 GEMM over 2 f_pad). twell_ffn_tile_union_fwd below computes the same y over each
- * tile's union only, with h in fp16 (one down product over |U_m| instead of two over f_pad), and is
- * faster at every density measured; this call is kept for layers without an fp16 copy of Wd_s.
- * bf16 only; d and f multiples of 8; x [N, d], Wu_s / Wd_s [f, d], y [N, d], device, 16-byte
- * aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (dense a and
- * [hi | lo] of H, 6*N*f_pad bytes), required when N > 0. A corrupt TwELL (count above the tile width, column >= f) is
- * reported as TWELL_ERR_DEVICE_CHECK in *dev_status; such entries contribute nothing.
+/* The same y from the same TwELL for a layer too dense for the walk: with more than a few percent
+ * of d_ff kept per token the union of the units a tile of 128 tokens keeps is nearly all of d_ff,
+ * so the up and down projections are dense contractions over all of it, on the tensor cores ([TC]
+ * §3: tensor cores for the heavy work). Steps: a is written into H [N, f_pad] (fp16, f_pad = f
+ * rounded up to 64) at each row's kept columns, with a per-row keep mask; H = (x Wu_s^T) * a
+ * (tcgen05 GEMM on SM pairs, the product formed in its epilogue where the mask is set, h stored in
+ * place as fp16: 11 significant bits); y = H Wd16_s (tcgen05 GEMM over f_pad, fp16 operands, bf16 y).
+ * Wd16_s is Wd_s converted once to fp16 (twell_convert_f16).
+ * bf16 x, Wu_s, y; d and f multiples of 8; x [N, d], Wu_s / Wd16_s [f, d], y [N, d], device,
+ * 16-byte aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (H and the
+ * masks, 2.125 * N * f_pad bytes), required when N > 0. A corrupt TwELL entry (count above the tile
+ * width, column >= f) is reported as TWELL_ERR_DEVICE_CHECK in *dev_status and contributes nothing;
+ * so is an a or h beyond the fp16 range.
  */
-TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd_s,
+TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16_s,
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);

@@ -123,20 +123,25 @@ def test_count_nonzeros_matches_the_counts(cuda_dev):
 
 
 def test_auto_path_follows_the_density(cuda_dev):
-    """ffn_forward(path="auto"): with a density above the crossover and an fp16 Wd_s the tile-union
-    path runs (same y as calling it directly), below it the walk; without Wd16_s the walk."""
+    """ffn_forward(path="auto"): with a density above the crossover and an fp16 Wd_s the union path
+    runs (same y as calling it directly), below it the walk; without Wd16_s the walk. The tile-union
+    path is called by name."""
     L = synthetic.uniform_layer(400, 512, 1280, 128, 0.03, seed=23)
     t = L.torch_inputs(cuda_dev)
     Wd16 = binding.twell_convert_f16(t["Wd_s"])
     args = (t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"])
+    y_union = binding.ffn_forward(*args, T=128, path="union", Wd16_s=Wd16)
     y_tu = binding.ffn_forward(*args, T=128, path="tile_union", Wd16_s=Wd16)
     y_walk = binding.ffn_forward(*args, T=128, path="walk")
     y_auto_hi = binding.ffn_forward(*args, T=128, path="auto", Wd16_s=Wd16, density=0.03)
     y_auto_lo = binding.ffn_forward(*args, T=128, path="auto", Wd16_s=Wd16, density=0.001)
     y_auto_no16 = binding.ffn_forward(*args, T=128, path="auto", density=0.03)
-    assert torch.equal(y_auto_hi, y_tu)
+    assert torch.equal(y_auto_hi, y_union)
     assert torch.equal(y_auto_lo, y_walk)
     assert torch.equal(y_auto_no16, y_walk)
-    assert_close(y_tu.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), "auto tile union")
-    with pytest.raises(ValueError):
-        binding.ffn_forward(*args, T=128, path="tile_union")
+    ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s)
+    assert_close(y_tu.double().cpu().numpy(), ref, "tile union")
+    assert_close(y_union.double().cpu().numpy(), ref, "union")
+    for path in ("tile_union", "union"):
+        with pytest.raises(ValueError):
+            binding.ffn_forward(*args, T=128, path=path)

@@ -8,11 +8,10 @@ def test_small_batches_take_the_decode_path():
         assert binding.choose_path(n, 0.05) == "decode"
 
 
-def test_density_chooses_walk_or_tile_union():
+def test_density_chooses_walk_or_union():
     n = binding.DECODE_MAX_N + 1
     assert binding.choose_path(n, None) == "walk"  # no estimate yet: the walk
     assert binding.choose_path(n, 0.005) == "walk"
-    assert binding.choose_path(n, binding.TILE_UNION_MIN_DENSITY) == "tile_union"
-    assert binding.choose_path(8192, 0.02) == "tile_union"
-    assert binding.choose_path(8192, binding.TILE_UNION_MAX_DENSITY) == "union"
+    assert binding.choose_path(n, binding.UNION_MIN_DENSITY) == "union"
+    assert binding.choose_path(8192, 0.02) == "union"
     assert binding.choose_path(8192, 0.5) == "union"
