@@ -37,7 +37,7 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe",
            "twell_ffn_fused_fwd_f16down", "twell_convert_f16", "twell_ffn_decode", "twell_ffn_tile_union_fwd",
-           "twell_count_nonzeros")
+           "twell_count_nonzeros", "twell_convert_f16_transposed")
 
 
 class TwellError(RuntimeError):
@@ -91,6 +91,7 @@ def load(path: str = LIB_PATH):
                 "twell_ffn_fused_fwd_f16down": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
                                                      vp, vp]),
                 "twell_convert_f16": (st, [vp, vp, ctypes.c_int64, vp, vp]),
+                "twell_convert_f16_transposed": (st, [vp, vp, i32, i32, vp, vp]),
                 "twell_ffn_decode": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.POINTER(_Packed), vp, vp, sz,
                                           vp, vp]),
                 "twell_hybrid_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
@@ -288,6 +289,21 @@ def twell_convert_f16(src: torch.Tensor, out: Optional[torch.Tensor] = None, sta
     return out
 
 
+def twell_convert_f16_transposed(src: torch.Tensor, out: Optional[torch.Tensor] = None, status=None,
+                                 stream=None) -> torch.Tensor:
+    """The transpose of a 2-D bf16 tensor converted to fp16 by the library (e.g. Wd_s [f, d] -> Wd16t_s
+    [d, f] for twell_ffn_union_fwd)."""
+    if src.dtype != torch.bfloat16 or src.dim() != 2 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous 2-D bf16 tensor")
+    rows, cols = src.shape
+    out = out if out is not None else torch.empty((cols, rows), dtype=torch.float16, device=src.device)
+    _check(load().twell_convert_f16_transposed(_ptr(src), _ptr(out), rows, cols,
+                                               _ptr(status if status is not None else status_buffer(src.device)),
+                                               _stream(stream)),
+           "twell_convert_f16_transposed")
+    return out
+
+
 def twell_ffn_fused_fwd_f16down(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tensor, a: TwELL,
                                 y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                                 stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -317,11 +333,11 @@ class StreamedFFN:
 
     def __init__(self, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd_s: torch.Tensor, N: int, T: int = 128,
                  path: str = "walk", vals_dtype: torch.dtype = torch.float32, status: Optional[torch.Tensor] = None,
-                 Wd16_s: Optional[torch.Tensor] = None):
+                 Wd16_s: Optional[torch.Tensor] = None, Wd16t_s: Optional[torch.Tensor] = None):
         dev = Wg_s.device
         f, d = Wg_s.shape
         self.W, self.T, self.path, self.status, self.N, self.d = (Wg_s, Wu_s, Wd_s), T, path, status, N, d
-        self.Wd16 = Wd16_s
+        self.Wd16, self.Wd16t = Wd16_s, Wd16t_s
         self.copy_in, self.compute, self.copy_out = (torch.cuda.Stream(dev) for _ in range(3))
         self.x = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
         self.y = [torch.empty((N, d), dtype=Wg_s.dtype, device=dev) for _ in range(2)]
@@ -347,7 +363,7 @@ class StreamedFFN:
             if later:
                 self.compute.wait_event(self.y_out[b])  # y[b] of batch count-2 is on the host
             ffn_forward(self.x[b], *self.W, T=self.T, packed=self.packed, y=self.y[b], status=self.status,
-                        stream=self.compute, path=self.path, Wd16_s=self.Wd16)
+                        stream=self.compute, path=self.path, Wd16_s=self.Wd16, Wd16t_s=self.Wd16t)
             self.done[b].record(self.compute)
         with torch.cuda.stream(self.copy_out):
             self.copy_out.wait_event(self.done[b])
@@ -359,15 +375,16 @@ class StreamedFFN:
 _union_ws = {}
 
 
-def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tensor, a: TwELL,
+def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16t_s: torch.Tensor, a: TwELL,
                         y: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                         stream=None, ws: Optional[torch.Tensor] = None) -> torch.Tensor:
     """The same y as twell_ffn_fused_fwd, as two tensor-core GEMMs over all of d_ff (for dense layers);
-    Wd16_s is Wd_s converted by twell_convert_f16."""
+    Wd16t_s [d, f] is Wd_s transposed and converted by twell_convert_f16_transposed."""
     N, d = x.shape
     f = Wu_s.shape[0]
-    if Wd16_s.dtype != torch.float16:
-        raise ValueError("Wd16_s must be fp16 (twell_convert_f16 of Wd_s)")
+    if Wd16t_s.dtype != torch.float16 or tuple(Wd16t_s.shape) != (d, f) or not Wd16t_s.is_contiguous():
+        raise ValueError("Wd16t_s must be a contiguous fp16 [d_model, d_ff] tensor "
+                         "(twell_convert_f16_transposed of Wd_s)")
     y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
     if ws is None:
         n = twell_workspace_bytes(OP_FFN_UNION_FWD, N, d, f)
@@ -377,7 +394,7 @@ def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16_s: torch.Tenso
             ws = torch.empty(n, dtype=torch.uint8, device=x.device)
             _union_ws[key] = ws
     s = a.c_struct()
-    _check(load().twell_ffn_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd16_s), ctypes.byref(s), N, d, f,
+    _check(load().twell_ffn_union_fwd(_ptr(x), _ptr(Wu_s), _ptr(Wd16t_s), ctypes.byref(s), N, d, f,
                                       _dtype_code(x.dtype), _ptr(y), _ptr(ws), ws.numel(),
                                       _ptr(status if status is not None else status_buffer(x.device)),
                                       _stream(stream)),
@@ -465,15 +482,16 @@ def choose_path(n_tokens: int, density: Optional[float]) -> str:
 
 def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = None, y=None, status=None, stream=None,
                 vals_dtype: torch.dtype = torch.float32, path: str = "walk", Wd16_s: Optional[torch.Tensor] = None,
-                density: Optional[float] = None):
+                density: Optional[float] = None, Wd16t_s: Optional[torch.Tensor] = None):
     """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk"),
-    twell_ffn_tile_union_fwd (path "tile_union") or twell_ffn_union_fwd (path "union"), the latter two
-    with Wd16_s = twell_convert_f16(Wd_s); path "decode" runs twell_ffn_decode (at most DECODE_MAX_N
-    tokens). Path "auto" follows choose_path with `density`, the kept fraction of the previous batch
-    (twell_count_nonzeros / (N * d_ff)); without Wd16_s it stays on the walk."""
+    twell_ffn_union_fwd (path "union", with Wd16t_s = twell_convert_f16_transposed(Wd_s)) or
+    twell_ffn_tile_union_fwd (path "tile_union", with Wd16_s = twell_convert_f16(Wd_s)); path
+    "decode" runs twell_ffn_decode (at most DECODE_MAX_N tokens). Path "auto" follows choose_path
+    with `density`, the kept fraction of the previous batch (twell_count_nonzeros / (N * d_ff));
+    without Wd16t_s it stays on the walk."""
     if path == "auto":
         path = choose_path(x.shape[0], density)
-        if path in ("tile_union", "union") and Wd16_s is None:
+        if path == "union" and Wd16t_s is None:
             path = "walk"
         if path == "decode":
             try:
@@ -487,11 +505,14 @@ def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = Non
         return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                 vals_dtype=vals_dtype)[0]
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
-    if path in ("union", "tile_union"):
+    if path == "union":
+        if Wd16t_s is None:
+            raise ValueError('path "union" needs Wd16t_s (twell_convert_f16_transposed(Wd_s))')
+        return twell_ffn_union_fwd(x, Wu_s, Wd16t_s, a, y=y, status=status, stream=stream)
+    if path == "tile_union":
         if Wd16_s is None:
-            raise ValueError(f'path "{path}" needs Wd16_s (twell_convert_f16(Wd_s))')
-        fn = twell_ffn_union_fwd if path == "union" else twell_ffn_tile_union_fwd
-        return fn(x, Wu_s, Wd16_s, a, y=y, status=status, stream=stream)
+            raise ValueError('path "tile_union" needs Wd16_s (twell_convert_f16(Wd_s))')
+        return twell_ffn_tile_union_fwd(x, Wu_s, Wd16_s, a, y=y, status=status, stream=stream)
     if path != "walk":
         raise ValueError(f"unknown path {path!r}")
     return twell_ffn_fused_fwd(x, Wu_s, Wd_s, a, y=y, status=status, stream=stream)

@@ -1410,7 +1410,43 @@ __global__ void convert_f16_kernel(const __nv_bfloat16* __restrict__ src, __half
         dst[i] = h;
     }
 }
+// src [rows, cols] bf16 -> dst [cols, rows] fp16 through 32 x 32 shared-memory tiles (reads and writes
+// coalesced); an overflow of the fp16 range is recorded as in convert_f16_kernel.
+__global__ void __launch_bounds__(256) convert_f16_t_kernel(const __nv_bfloat16* __restrict__ src,
+                                                            __half* __restrict__ dst, int rows, int cols,
+                                                            int32_t* status)
+{
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int j = threadIdx.y; j < 32; j += 8) {
+        const int r = r0 + j, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[j][threadIdx.x] = __bfloat162float(src[static_cast<size_t>(r) * cols + c]);
+    }
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += 8) {
+        const int c = c0 + j, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) {
+            const float v = tile[threadIdx.x][j];
+            const __half h = __float2half_rn(v);
+            if (isfinite(v) && __hisinf(h)) twell::report(status, TWELL_ERR_DEVICE_CHECK);
+            dst[static_cast<size_t>(c) * rows + r] = h;
+        }
+    }
+}
 }  // namespace
+
+extern "C" twell_status twell_convert_f16_transposed(const void* src, void* dst, int32_t rows, int32_t cols,
+                                                     int32_t* dev_status, void* stream)
+{
+    if (rows < 0 || cols < 0 || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (rows == 0 || cols == 0) return TWELL_OK;
+    if (src == nullptr || dst == nullptr) return TWELL_ERR_INVALID;
+    if ((rows + 31) / 32 > 65535) return TWELL_ERR_UNSUPPORTED;
+    const dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+    convert_f16_t_kernel<<<grid, dim3(32, 8), 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(src), static_cast<__half*>(dst), rows, cols, dev_status);
+    return twell_host::launch_status();
+}
 
 extern "C" twell_status twell_convert_f16(const void* src, void* dst, int64_t n, int32_t* dev_status, void* stream)
 {

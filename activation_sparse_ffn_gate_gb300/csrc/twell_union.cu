@@ -10,8 +10,8 @@
 //      (one bit per column, f_pad = d_ff rounded up to 64); H is not cleared;
 //   2. H = (x Wu_s^T) * a: tcgen05 GEMM on SM pairs whose epilogue forms h = a * acc where the mask
 //      bit is set (0 elsewhere) and stores it in place as fp16;
-//   3. y = H Wd16_s: tcgen05 GEMM over K = f_pad with fp16 operands (Wd16_s: Wd_s converted once to
-//      fp16, the same values), bf16 y.
+//   3. y = H Wd16_s: tcgen05 GEMM on SM pairs over K = f_pad with fp16 operands, B read K-major from
+//      Wd16t_s = Wd_s^T converted once to fp16 ([d_model, d_ff], the same values), bf16 y.
 // h and a carry 11 significant bits (fp16); an a or h beyond the fp16 range is recorded as
 // TWELL_ERR_DEVICE_CHECK. (The earlier form of this path carried h as a bf16 hi + lo pair, which
 // doubled K of the down GEMM.)
@@ -83,11 +83,11 @@ size_t twell_host::union_ws_bytes(int N, int f) { return twell::UnionWs(N, f).to
 
 using namespace twell_host;
 
-extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16_s, const twell_packed* a,
+extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16t_s, const twell_packed* a,
                                             int32_t N, int32_t d, int32_t f, twell_dtype dtype, void* y, void* ws,
                                             size_t ws_bytes, int32_t* dev_status, void* stream)
 {
-    if (Wu_s == nullptr || Wd16_s == nullptr || a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
+    if (Wu_s == nullptr || Wd16t_s == nullptr || a == nullptr || dev_status == nullptr) return TWELL_ERR_INVALID;
     if ((x == nullptr || y == nullptr) && N != 0) return TWELL_ERR_INVALID;
     if (N < 0 || d <= 0 || f <= 0 || d % 8 != 0 || f % 8 != 0) return TWELL_ERR_INVALID;
     if (dtype != TWELL_BF16 || !dtype_ok(a->dtype)) return TWELL_ERR_UNSUPPORTED;
@@ -96,7 +96,7 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
     if (N == 0) return TWELL_OK;
     const twell::UnionWs L(N, f);
     if (ws == nullptr || ws_bytes < L.total) return TWELL_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd16_s) || !aligned16(y) || !aligned16(ws))
+    if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd16t_s) || !aligned16(y) || !aligned16(ws))
         return TWELL_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t* M = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + L.mask);
@@ -127,7 +127,7 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
     st = launch_gemm<256, false, false, twell::Epi::MulMaskF16, true>(GemmOperand{x, N, d, d},
                                                                       GemmOperand{Wu_s, f, d, d}, nullptr, g, s);
     if (st != TWELL_OK) return st;
-    // 3. y = H Wd16_s over K = f_pad (rows f .. f_pad of Wd16_s read as zeros)
+    // 3. y = H Wd16_s over K = f_pad: B = Wd16t_s [d, f] K-major (columns f .. f_pad read as zeros)
     twell::GemmArgs g2{};
     g2.M = N;
     g2.N = d;
@@ -135,6 +135,7 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
     g2.out = y;
     g2.ldo = d;
     g2.status = dev_status;
-    return launch_gemm<256, false, true, twell::Epi::StoreBF16, false, true>(GemmOperand{H, N, fp, fp},
-                                                                             GemmOperand{Wd16_s, f, d, d}, nullptr, g2, s);
+    return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(GemmOperand{H, N, fp, fp},
+                                                                             GemmOperand{Wd16t_s, d, f, f}, nullptr, g2,
+                                                                             s);
 }

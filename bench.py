@@ -57,9 +57,10 @@ def _args():
     p.add_argument("--config", type=int, choices=[1, 2], default=1,
                    help="workload of the main line: 1 = the 1.5B-like layer (default), 2 = the 2B-like layer "
                         "(N=16384, d_model 2560, d_ff 6912, lognormal per-token density; no dead-column step)")
-    p.add_argument("--path", choices=["walk", "tile_union"], default="walk",
-                   help="second call of the step: the fused walk (default) or the tile-union GEMMs "
-                        "(twell_ffn_tile_union_fwd, Wd_s converted to fp16 once outside the timed region)")
+    p.add_argument("--path", choices=["walk", "union", "tile_union"], default="walk",
+                   help="second call of the step: the fused walk (default), the union GEMMs over all of d_ff "
+                        "(twell_ffn_union_fwd) or the tile-union GEMMs (twell_ffn_tile_union_fwd); the last two "
+                        "with Wd_s converted to fp16 once outside the timed region")
     p.add_argument("--density", type=float, default=None,
                    help="run the main line on the sweep's uniform-density layer (N=8192, d_model 2048, d_ff 5632, "
                         "T=128) with this kept fraction instead of the --config layer")
@@ -281,10 +282,13 @@ def run_ours(a, rank, world):
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
     Wd16 = binding.twell_convert_f16(Wd, status=status, stream=stream) if a.path == "tile_union" else None
+    Wd16t = binding.twell_convert_f16_transposed(Wd, status=status, stream=stream) if a.path == "union" else None
 
     def second():
         if a.path == "tile_union":
             binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status, stream=stream)
+        elif a.path == "union":
+            binding.twell_ffn_union_fwd(x, Wu, Wd16t, packed, y=y, status=status, stream=stream)
         else:
             binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
 
@@ -366,16 +370,19 @@ def run_ours(a, rank, world):
     # per-kernel algorithmic work
     fused_bytes = (N * d * 2) + union * 2 * d * 2 + (N * d * 2) + twell_bytes
     mg, mf = sum(t_gate) / a.steps, sum(t_fused) / a.steps
-    second_name = "twell_ffn_tile_union_fwd" if a.path == "tile_union" else "twell_ffn_fused_fwd"
-    if a.path == "tile_union" and mf >= mg:
-        # the up and down GEMMs over each 128-token tile's union: 2 * 128 * |U_m| * d FLOPs each per tile
-        tu_flops = 4.0 * 128 * union * d
+    second_name = {"walk": "twell_ffn_fused_fwd", "union": "twell_ffn_union_fwd",
+                   "tile_union": "twell_ffn_tile_union_fwd"}[a.path]
+    if a.path != "walk" and mf >= mg:
+        # the up and down GEMMs: over each 128-token tile's union (2 * 128 * |U_m| * d FLOPs each per
+        # tile), or over all of d_ff rounded up to 64 for the union path
+        tu_flops = 4.0 * 128 * union * d if a.path == "tile_union" else 4.0 * N * ((f + 63) // 64 * 64) * d
         ach = tu_flops / (mf * 1e-3) / 1e12
         roof = {"kernel": second_name, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
                 "algorithmic_flops": tu_flops, "ms_per_launch": mf,
                 "peak_kind": peak_kind + " bf16_tflops (burst; the down GEMM runs fp16, the same rate)",
-                "note": "whole call (union, expand, up and down GEMMs) against the union GEMMs' FLOPs"}
+                "note": "whole call (expand, up and down GEMMs; the tile unions first on the tile-union path) "
+                        "against the two GEMMs' FLOPs"}
     elif mf >= mg:
         # The walk moves, per kept entry, the unit's rows of Wu_s and Wd_s (2 * d * 2 B) from L2 into
         # shared memory, plus x_r once per row: these gathers, not HBM, bound it (ncu: DRAM ~9% busy).
@@ -446,7 +453,7 @@ def run_ours(a, rank, world):
     for _ in range(3):
         xd.copy_(xh, non_blocking=True)
         binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream, path=a.path,
-                            Wd16_s=Wd16)
+                            Wd16_s=Wd16, Wd16t_s=Wd16t)
         yh.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -454,12 +461,12 @@ def run_ours(a, rank, world):
     for _ in range(e2e_steps):
         xd.copy_(xh, non_blocking=True)
         binding.ffn_forward(xd, Wg, Wu, Wd, T, packed=packed, y=y, status=status, stream=stream, path=a.path,
-                            Wd16_s=Wd16)
+                            Wd16_s=Wd16, Wd16t_s=Wd16t)
         yh.copy_(y, non_blocking=True)
     s1.record(stream)
     torch.cuda.synchronize()
     e2e_serial_ms = s0.elapsed_time(s1) / e2e_steps
-    pipe = binding.StreamedFFN(Wg, Wu, Wd, N, T=T, status=status, path=a.path, Wd16_s=Wd16)
+    pipe = binding.StreamedFFN(Wg, Wu, Wd, N, T=T, status=status, path=a.path, Wd16_s=Wd16, Wd16t_s=Wd16t)
     for _ in range(3):
         pipe.submit(xh, yh)
     torch.cuda.synchronize()
@@ -613,9 +620,9 @@ def run_ours(a, rank, world):
                        "steps' gate + walk (three streams, double-buffered device x and y)",
                 "serial": {"value": N / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
                            "how": "copy in, gate + walk, copy out one after the other on one stream"}},
-        # per step: gate + pack, then the walk's plan and the walk, or the tile-union path's union bits,
-        # prefix, work list, expand, up GEMM and down GEMM (plus a memset of the union bitmaps)
-        "gpu_launches": (3 if a.path == "walk" else 7) * a.steps,
+        # per step: gate + pack, then the walk's plan and the walk; or the union path's expand, up and
+        # down GEMMs; or the tile-union path's union bits, prefix, work list, expand, up and down GEMMs
+        "gpu_launches": {"walk": 3, "union": 4, "tile_union": 7}[a.path] * a.steps,
         "path": a.path,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
@@ -818,7 +825,8 @@ def run_sweep(a):
         gate_fn = lambda: binding.twell_gate_pack(x, Wg, L.T, out=packed, status=status)  # noqa: E731
         fused_fn = lambda: binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status)  # noqa: E731
         Wd16 = binding.twell_convert_f16(Wd, status=status)
-        union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
+        Wd16t = binding.twell_convert_f16_transposed(Wd, status=status)
+        union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd16t, packed, y=y, status=status)  # noqa: E731
         f16_fn = lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
         tu_fn = lambda: binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
 
@@ -880,7 +888,7 @@ def run_sweep(a):
                           "timing": ("per call: (50 replays of a graph [L2 flush + call] - 50 replays of a graph "
                                      "[L2 flush]) / 50, median of 3" if use_graphs else
                                      f"CUDA events around each call, median of {n_it}")}), flush=True)
-        del t, x, Wg, Wu, Wd, Wd16, packed, y
+        del t, x, Wg, Wu, Wd, Wd16, Wd16t, packed, y
         binding._tile_union_ws.clear()
         torch.cuda.empty_cache()
 

@@ -196,6 +196,13 @@ TWELL_API twell_status twell_ffn_fused_fwd_f16down(const void* x, const void* Wu
 TWELL_API twell_status twell_convert_f16(const void* src, void* dst, int64_t n, int32_t* dev_status,
                                void* stream);
 
+/* dst [cols, rows] (fp16) = the transpose of src [rows, cols] (bf16, row-major) converted to fp16 with
+ * the same rounding and overflow reporting as twell_convert_f16 (e.g. Wd_s [d_ff, d_model] ->
+ * Wd16t_s [d_model, d_ff] for twell_ffn_union_fwd). rows <= 2,097,120 (else TWELL_ERR_UNSUPPORTED).
+ * Device pointers; asynchronous on `stream`. */
+TWELL_API twell_status twell_convert_f16_transposed(const void* src, void* dst, int32_t rows, int32_t cols,
+                                                    int32_t* dev_status, void* stream);
+
 /* The whole layer for a batch of at most 16 tokens (decoding) in two launches: the gate + pack of
  * twell_gate_pack (the same TwELL in *a_out, bit for bit) and, in the same kernel, the walk of each
  * column tile's kept entries by the CTAs that computed them ([AIM] ¶3; [TG] "Инференс"; [PUL] ¶3;
@@ -222,15 +229,16 @@ TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const v
  * §3: tensor cores for the heavy work). Steps: a is written into H [N, f_pad] (fp16, f_pad = f
  * rounded up to 64) at each row's kept columns, with a per-row keep mask; H = (x Wu_s^T) * a
  * (tcgen05 GEMM on SM pairs, the product formed in its epilogue where the mask is set, h stored in
- * place as fp16: 11 significant bits); y = H Wd16_s (tcgen05 GEMM over f_pad, fp16 operands, bf16 y).
- * Wd16_s is Wd_s converted once to fp16 (twell_convert_f16).
- * bf16 x, Wu_s, y; d and f multiples of 8; x [N, d], Wu_s / Wd16_s [f, d], y [N, d], device,
+ * place as fp16: 11 significant bits); y = H Wd16_s (tcgen05 GEMM on SM pairs over f_pad, fp16
+ * operands, bf16 y). Wd16t_s is the transpose of Wd_s converted once to fp16 ([d, f]:
+ * twell_convert_f16_transposed), so that the down GEMM reads both operands K-major.
+ * bf16 x, Wu_s, y; d and f multiples of 8; x [N, d], Wu_s [f, d], Wd16t_s [d, f], y [N, d], device,
  * 16-byte aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (H and the
  * masks, 2.125 * N * f_pad bytes), required when N > 0. A corrupt TwELL entry (count above the tile
  * width, column >= f) is reported as TWELL_ERR_DEVICE_CHECK in *dev_status and contributes nothing;
  * so is an a or h beyond the fp16 range.
  */
-TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16_s,
+TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16t_s,
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);

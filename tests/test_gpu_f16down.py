@@ -58,6 +58,27 @@ def test_convert_f16_round_to_nearest_even(cuda_dev):
     assert binding.twell_read_status() == 0
 
 
+@pytest.mark.parametrize("shape", [(1000, 576), (37, 45), (1, 8), (5632, 2048)])
+def test_convert_f16_transposed_is_the_transpose(cuda_dev, shape):
+    """twell_convert_f16_transposed gives, bit for bit, the transpose of numpy's round-to-nearest-even
+    fp16 conversion, for shapes that are and are not multiples of its 32 x 32 tile."""
+    rng = np.random.default_rng(shape[0])
+    src = torch.from_numpy(rng.normal(0, 0.02, shape).astype(np.float32)).to(torch.bfloat16)
+    src[0, 0] = 2.0 ** -20  # an fp16 subnormal
+    want = np.ascontiguousarray(src.float().numpy().astype(np.float16).T)
+    got = binding.twell_convert_f16_transposed(src.to(cuda_dev)).cpu().numpy()
+    assert got.shape == (shape[1], shape[0])
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+    assert binding.twell_read_status() == 0
+
+
+def test_convert_f16_transposed_reports_overflow(cuda_dev):
+    src = torch.tensor([[1.0, 65536.0], [-1e6, 3.0]], dtype=torch.bfloat16, device=cuda_dev)
+    got = binding.twell_convert_f16_transposed(src).cpu().float().numpy()
+    assert binding.twell_read_status(reset=True) == 5  # TWELL_ERR_DEVICE_CHECK
+    assert got[0, 0] == 1.0 and got[1, 1] == 3.0 and np.isposinf(got[1, 0]) and np.isneginf(got[0, 1])
+
+
 def test_convert_f16_reports_overflow(cuda_dev):
     src = torch.tensor([1.0, 65536.0, -1e6, 3.0], dtype=torch.bfloat16, device=cuda_dev)
     got = binding.twell_convert_f16(src).cpu().float().numpy()

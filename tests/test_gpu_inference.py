@@ -357,7 +357,8 @@ def test_union_small_ragged(cuda_dev, vals_dtype, N):
     Gs = synthetic.round_bf16_np(Ga.astype(np.float32)) if vals_dtype == torch.bfloat16 else Ga.astype(np.float32)
     tw = binding.twell_pack_from_gate(_to(cuda_dev, Gs, vals_dtype), L.T)
     t = L.torch_inputs(cuda_dev)
-    y = binding.twell_ffn_union_fwd(t["x"], t["Wu_s"], binding.twell_convert_f16(t["Wd_s"]), tw).double().cpu().numpy()
+    Wd16t = binding.twell_convert_f16_transposed(t["Wd_s"])
+    y = binding.twell_ffn_union_fwd(t["x"], t["Wu_s"], Wd16t, tw).double().cpu().numpy()
     vals, idx, cnt = oracle.twell_pack(Gs.astype(np.float64), L.T)
     assert_close(y, oracle.twell_walk(vals, idx, cnt, L.T, L.x, L.Wu_s, L.Wd_s), f"union {vals_dtype}")
 
@@ -368,7 +369,7 @@ def test_union_other_tile_widths(cuda_dev, T):
     L = synthetic.uniform_layer(200, 512, 1000, T, 0.04, seed=T + 5)
     t = L.torch_inputs(cuda_dev)
     y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=T, path="union",
-                            Wd16_s=binding.twell_convert_f16(t["Wd_s"]))
+                            Wd16t_s=binding.twell_convert_f16_transposed(t["Wd_s"]))
     assert_close(y.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"union T={T}")
 
 
@@ -405,8 +406,8 @@ def test_streamed_batches_union_path(cuda_dev):
     """StreamedFFN on the union path returns what ffn_forward(path="union") returns."""
     L = synthetic.uniform_layer(3 * 128, 512, 1024, 128, 0.05, seed=43)
     t = L.torch_inputs(cuda_dev)
-    Wd16 = binding.twell_convert_f16(t["Wd_s"])
-    pipe = binding.StreamedFFN(t["Wg_s"], t["Wu_s"], t["Wd_s"], 128, T=L.T, path="union", Wd16_s=Wd16)
+    Wd16t = binding.twell_convert_f16_transposed(t["Wd_s"])
+    pipe = binding.StreamedFFN(t["Wg_s"], t["Wu_s"], t["Wd_s"], 128, T=L.T, path="union", Wd16t_s=Wd16t)
     xs = [t["x"][128 * i:128 * (i + 1)].cpu().pin_memory() for i in range(3)]
     ys = [torch.empty((128, L.d), dtype=torch.bfloat16).pin_memory() for _ in range(3)]
     for xh, yh in zip(xs, ys):
@@ -414,7 +415,7 @@ def test_streamed_batches_union_path(cuda_dev):
     torch.cuda.synchronize()
     for i in range(3):
         ref = binding.ffn_forward(t["x"][128 * i:128 * (i + 1)].contiguous(), t["Wg_s"], t["Wu_s"], t["Wd_s"],
-                                  T=L.T, path="union", Wd16_s=Wd16)
+                                  T=L.T, path="union", Wd16t_s=Wd16t)
         assert torch.equal(ys[i], ref.cpu()), i
 
 
@@ -425,7 +426,7 @@ def test_union_sweep_shapes_end_to_end_sampled(cuda_dev, p):
     L = synthetic.sweep_point(p, 128, N=1024)
     t = L.torch_inputs(cuda_dev)
     y = binding.ffn_forward(t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"], T=128, path="union",
-                            Wd16_s=binding.twell_convert_f16(t["Wd_s"]))
+                            Wd16t_s=binding.twell_convert_f16_transposed(t["Wd_s"]))
     rows = _sampled_rows(L.N, 12, seed=3)
     y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
     assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"union p={p}")

@@ -123,19 +123,20 @@ def test_count_nonzeros_matches_the_counts(cuda_dev):
 
 
 def test_auto_path_follows_the_density(cuda_dev):
-    """ffn_forward(path="auto"): with a density above the crossover and an fp16 Wd_s the union path
-    runs (same y as calling it directly), below it the walk; without Wd16_s the walk. The tile-union
-    path is called by name."""
+    """ffn_forward(path="auto"): with a density above the crossover and the transposed fp16 Wd_s the
+    union path runs (same y as calling it directly), below it the walk; without Wd16t_s the walk.
+    The tile-union path is called by name."""
     L = synthetic.uniform_layer(400, 512, 1280, 128, 0.03, seed=23)
     t = L.torch_inputs(cuda_dev)
     Wd16 = binding.twell_convert_f16(t["Wd_s"])
+    Wd16t = binding.twell_convert_f16_transposed(t["Wd_s"])
     args = (t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"])
-    y_union = binding.ffn_forward(*args, T=128, path="union", Wd16_s=Wd16)
+    y_union = binding.ffn_forward(*args, T=128, path="union", Wd16t_s=Wd16t)
     y_tu = binding.ffn_forward(*args, T=128, path="tile_union", Wd16_s=Wd16)
     y_walk = binding.ffn_forward(*args, T=128, path="walk")
-    y_auto_hi = binding.ffn_forward(*args, T=128, path="auto", Wd16_s=Wd16, density=0.03)
-    y_auto_lo = binding.ffn_forward(*args, T=128, path="auto", Wd16_s=Wd16, density=0.001)
-    y_auto_no16 = binding.ffn_forward(*args, T=128, path="auto", density=0.03)
+    y_auto_hi = binding.ffn_forward(*args, T=128, path="auto", Wd16t_s=Wd16t, density=0.03)
+    y_auto_lo = binding.ffn_forward(*args, T=128, path="auto", Wd16t_s=Wd16t, density=0.001)
+    y_auto_no16 = binding.ffn_forward(*args, T=128, path="auto", Wd16_s=Wd16, density=0.03)
     assert torch.equal(y_auto_hi, y_union)
     assert torch.equal(y_auto_lo, y_walk)
     assert torch.equal(y_auto_no16, y_walk)
