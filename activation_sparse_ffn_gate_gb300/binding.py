@@ -24,7 +24,7 @@ TWELL_ERR_UNSUPPORTED = 2
 TWELL_BF16 = 0
 TWELL_F32 = 1
 (OP_GATE_PACK, OP_FFN_FUSED_FWD, OP_HYBRID_FWD, OP_HYBRID_BWD, OP_HYBRID_ROUTE, OP_FFN_UNION_FWD, OP_FFN_DECODE,
- OP_FFN_TILE_UNION_FWD) = range(8)
+ OP_FFN_TILE_UNION_FWD, OP_FFN_GATE_UNION_FWD) = range(9)
 DECODE_MAX_N = 16  # twell_ffn_decode takes batches of at most this many tokens
 STATUS_NAMES = {0: "TWELL_OK", 1: "TWELL_ERR_INVALID", 2: "TWELL_ERR_UNSUPPORTED", 3: "TWELL_ERR_BACKUP_FULL",
                 4: "TWELL_ERR_TIMEOUT", 5: "TWELL_ERR_DEVICE_CHECK", 6: "TWELL_ERR_CUDA",
@@ -37,7 +37,7 @@ EXPORTS = ("twell_packed_vals_bytes", "twell_packed_idx_bytes", "twell_packed_cn
            "twell_gate_gemm", "twell_gemm_test", "twell_column_activity", "twell_gather_rows",
            "twell_read_status", "twell_status_string", "twell_device_info", "twell_wait_probe",
            "twell_ffn_fused_fwd_f16down", "twell_convert_f16", "twell_ffn_decode", "twell_ffn_tile_union_fwd",
-           "twell_count_nonzeros", "twell_convert_f16_transposed")
+           "twell_count_nonzeros", "twell_convert_f16_transposed", "twell_ffn_gate_union_fwd")
 
 
 class TwellError(RuntimeError):
@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH):
                                              sz, vp, vp]),
                 "twell_ffn_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, ctypes.c_int, vp, vp,
                                              sz, vp, vp]),
+                "twell_ffn_gate_union_fwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int,
+                                                  ctypes.POINTER(_Packed), vp, vp, sz, vp, vp]),
                 "twell_ffn_tile_union_fwd": (st, [vp, vp, vp, ctypes.POINTER(_Packed), i32, i32, i32, vp, vp, sz,
                                                   vp, vp]),
                 "twell_wait_probe": (st, [i32, i32, vp, vp]),
@@ -402,6 +404,35 @@ def twell_ffn_union_fwd(x: torch.Tensor, Wu_s: torch.Tensor, Wd16t_s: torch.Tens
     return y
 
 
+def twell_ffn_gate_union_fwd(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd16t_s: torch.Tensor,
+                             T: int = 128, out: Optional[TwELL] = None, y: Optional[torch.Tensor] = None,
+                             status: Optional[torch.Tensor] = None, stream=None, ws: Optional[torch.Tensor] = None,
+                             vals_dtype: torch.dtype = torch.float32):
+    """twell_gate_pack and twell_ffn_union_fwd with the gate and up projections in one tensor-core
+    GEMM: returns (y, the TwELL of ReLU(x Wg_s^T)). T = 64 or 128."""
+    N, d = x.shape
+    f = Wu_s.shape[0]
+    if Wd16t_s.dtype != torch.float16 or tuple(Wd16t_s.shape) != (d, f) or not Wd16t_s.is_contiguous():
+        raise ValueError("Wd16t_s must be a contiguous fp16 [d_model, d_ff] tensor "
+                         "(twell_convert_f16_transposed of Wd_s)")
+    out = out if out is not None else TwELL.empty(N, f, T, vals_dtype, x.device)
+    y = y if y is not None else torch.empty((N, d), dtype=x.dtype, device=x.device)
+    if ws is None:
+        n = twell_workspace_bytes(OP_FFN_GATE_UNION_FWD, N, d, f)
+        key = (x.device.index, _stream(stream).value or 0)
+        ws = _union_ws.get(key)
+        if ws is None or ws.numel() < n:
+            ws = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
+            _union_ws[key] = ws
+    s = out.c_struct()
+    _check(load().twell_ffn_gate_union_fwd(_ptr(x), _ptr(Wg_s), _ptr(Wu_s), _ptr(Wd16t_s), N, d, f, T,
+                                           _dtype_code(x.dtype), ctypes.byref(s), _ptr(y), _ptr(ws), ws.numel(),
+                                           _ptr(status if status is not None else status_buffer(x.device)),
+                                           _stream(stream)),
+           "twell_ffn_gate_union_fwd")
+    return y, out
+
+
 _tile_union_ws = {}
 
 
@@ -459,15 +490,16 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
     return y, packed
 
 
-# Density (kept fraction of d_ff per token) above which the union GEMMs beat the walk, measured with
-# gate + path on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
-#   density                0.1%    0.5%    1%      2%      5%      10%     50%
-#   walk                   0.191   0.328   0.471   0.787   1.723   3.336   15.34
-#   union (all of d_ff)    0.399   0.412   0.423   0.445   0.493   0.561   1.095
-#   tile union (gathered)  0.236   0.376   0.484   0.589   0.689   0.793   1.627
-# The gathered tile-union path is never the fastest under these uniform densities (nor on the
-# lognormal 2B-like layer, where the walk wins); it stays available as path "tile_union".
-UNION_MIN_DENSITY = 0.008
+# Density (kept fraction of d_ff per token) above which the union path beats the walk, measured with
+# the whole layer on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
+#   density                               0.1%    0.5%    1%      2%      5%      10%     50%
+#   walk (gate + pack, then the walk)     0.193   0.327   0.473   0.791   1.739   3.333   15.33
+#   union (gate + up in one GEMM, down)   0.322   0.324   0.326   0.330   0.336   0.347   0.572
+#   tile union (gate, then gathered)      0.238   0.378   0.481   0.589   0.692   0.787   1.613
+#   dense cuBLAS FFN                      0.368   0.368   0.370   0.371   0.370   0.370   0.378
+# The two cross between 0.5% and 1% (within 1% of each other at 0.5%). The gathered tile-union path
+# is never the fastest under these uniform densities; it stays available as path "tile_union".
+UNION_MIN_DENSITY = 0.006
 
 
 def choose_path(n_tokens: int, density: Optional[float]) -> str:
@@ -484,7 +516,8 @@ def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = Non
                 vals_dtype: torch.dtype = torch.float32, path: str = "walk", Wd16_s: Optional[torch.Tensor] = None,
                 density: Optional[float] = None, Wd16t_s: Optional[torch.Tensor] = None):
     """The sparse inference FFN: twell_gate_pack, then twell_ffn_fused_fwd (path "walk"),
-    twell_ffn_union_fwd (path "union", with Wd16t_s = twell_convert_f16_transposed(Wd_s)) or
+    twell_ffn_union_fwd (path "union", with Wd16t_s = twell_convert_f16_transposed(Wd_s); for
+    T = 64 or 128 as twell_ffn_gate_union_fwd, gate and up projection in one GEMM) or
     twell_ffn_tile_union_fwd (path "tile_union", with Wd16_s = twell_convert_f16(Wd_s)); path
     "decode" runs twell_ffn_decode (at most DECODE_MAX_N tokens). Path "auto" follows choose_path
     with `density`, the kept fraction of the previous batch (twell_count_nonzeros / (N * d_ff));
@@ -504,10 +537,13 @@ def ffn_forward(x, Wg_s, Wu_s, Wd_s, T: int = 128, packed: Optional[TwELL] = Non
     if path == "decode":
         return twell_ffn_decode(x, Wg_s, Wu_s, Wd_s, T, packed=packed, y=y, status=status, stream=stream,
                                 vals_dtype=vals_dtype)[0]
+    if path == "union" and Wd16t_s is None:
+        raise ValueError('path "union" needs Wd16t_s (twell_convert_f16_transposed(Wd_s))')
+    if path == "union" and T in (64, 128):
+        return twell_ffn_gate_union_fwd(x, Wg_s, Wu_s, Wd16t_s, T, out=packed, y=y, status=status, stream=stream,
+                                        vals_dtype=vals_dtype)[0]
     a = twell_gate_pack(x, Wg_s, T, out=packed, status=status, stream=stream, vals_dtype=vals_dtype)
     if path == "union":
-        if Wd16t_s is None:
-            raise ValueError('path "union" needs Wd16t_s (twell_convert_f16_transposed(Wd_s))')
         return twell_ffn_union_fwd(x, Wu_s, Wd16t_s, a, y=y, status=status, stream=stream)
     if path == "tile_union":
         if Wd16_s is None:

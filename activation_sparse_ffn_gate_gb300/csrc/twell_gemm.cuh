@@ -56,6 +56,10 @@ enum class Epi : int {
     MulHiLoBF16 = 7, // v = acc * aux[m, n]: out[m, n] = hi = bf16(v), out[m, n + lo_offset] = bf16(v - hi)
     MulMaskF16 = 8,  // out[m, n] = fp16(acc * aux[m, n]) where bit n of mask row m is set, else 0; aux
                      // fp16 (may be out itself: each element is read before it is written, by one thread)
+    GateUpF16 = 9,   // PAIR only: the even CTA's B rows come from B (Wg_s), the odd CTA's from B2 (Wu_s),
+                     // for the same BN / 2 units, so a tile holds g and u of 256 rows x BN / 2 units;
+                     // the epilogue packs ReLU(g) into the TwELL as PackTwell does (T = 64 or 128) and
+                     // stores out[m, n] = fp16(a * u) (a = the packed value) where g > 0, else 0
 };
 
 struct GemmArgs {
@@ -107,6 +111,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs g)
 {
     static_assert(!PAIR || (!A_MN && !B_MN && BN == 256), "the CTA-pair tile is 256 x 256 with K-major operands");
+    static_assert(EPI != Epi::GateUpF16 || PAIR, "the gate + up tile takes its two B operands from a CTA pair");
+    // N extent of one tile: BN columns of C, or BN / 2 units (their g and u) with GateUpF16
+    constexpr int TN = EPI == Epi::GateUpF16 ? BN / 2 : BN;
     using C = GemmCfg<BN, PAIR>;
     constexpr int CG = PAIR ? 2 : 1;
     constexpr int STAGES = C::STAGES;
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int K = g.K;
     if (g.K_dyn != nullptr) K = min(K, *g.K_dyn);
     const int m_tiles = M > 0 ? (M + kBM - 1) / kBM : 0;
-    const int n_tiles = (g.N + BN - 1) / BN;
+    const int n_tiles = (g.N + TN - 1) / TN;
     const int kbs = K > 0 ? (K + kBK - 1) / kBK : 0;
     // k-block ranges per tile: ks of them, each non-empty
     const int ks = (PAIR || EPI != Epi::StoreF32 || g.k_splits <= 1) ? 1 : min(g.k_splits, max(kbs, 1));
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int units = kbs > 0 ? (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles * ks : 0;
     // unit u: tile u / ks, k-block range u % ks
     auto tile_m0 = [&](int u) { return (PAIR ? 2 * (u / ks / n_tiles) + crank : u / ks / n_tiles) * kBM; };
-    auto tile_n0 = [&](int u) { return (u / ks % n_tiles) * BN; };
+    auto tile_n0 = [&](int u) { return (u / ks % n_tiles) * TN; };
     auto kb_begin = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks) * kbs / ks); };
     auto kb_end = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks + 1) * kbs / ks); };
 
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (g.kb_split < kbs) tma_prefetch_desc(&tmB2);
+        if (EPI == Epi::GateUpF16 || g.kb_split < kbs) tma_prefetch_desc(&tmB2);
     }
     if (warp == 1) {
         tmem_alloc<CG>(tmem_slot, C::TMEM_COLS);
@@ -204,7 +211,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
                         const uint32_t fb = full_lead + stage * 8u;
                         tma_load_2d_pair(a, &tmA, k0, m0, fb);
-                        tma_load_2d_pair(b, &tmB, k0, n0 + crank * (BN / 2), fb);
+                        if constexpr (EPI == Epi::GateUpF16)
+                            tma_load_2d_pair(b, crank ? &tmB2 : &tmB, k0, n0, fb);
+                        else
+                            tma_load_2d_pair(b, &tmB, k0, n0 + crank * (BN / 2), fb);
                     } else {
                         mbar_arrive_expect_tx(&full[stage], g.a_box_rows > 0 && !A_MN
                                                                 ? static_cast<uint32_t>(g.a_box_rows) * kBK * 2 + C::B_BYTES
@@ -302,7 +312,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const bool row_ok = row < M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
-            if constexpr (EPI == Epi::PackTwell) {
+            if constexpr (EPI == Epi::GateUpF16) {
+                // columns [0, TN) of the accumulator hold g of units n0 .. n0 + TN, columns [TN, 2 TN)
+                // u of the same units. Per T-wide column tile: ReLU + TwELL pack of g as below, and
+                // h = a * u (a = the value as packed) stored as fp16 for every unit below ldo.
+                const int T = g.T;
+                __nv_bfloat16* vals16 = static_cast<__nv_bfloat16*>(g.vals);
+                float* vals32 = static_cast<float*>(g.vals);
+                __half* H = static_cast<__half*>(g.out);
+                bool over = false;
+                for (int tt = 0; tt < TN / T; ++tt) {
+                    const int tile = n0 / T + tt;
+                    const bool valid = row_ok && tile < g.nt;
+                    const size_t slot = (static_cast<size_t>(row) * g.nt + tile) * static_cast<size_t>(T);
+                    int c = 0;
+                    for (int ch = 0; ch < T / 32; ++ch) {
+                        float gv[32], uv[32];
+                        tmem_ld_32x32b_x32(taddr + tt * T + ch * 32, gv);
+                        tmem_ld_32x32b_x32(taddr + TN + tt * T + ch * 32, uv);
+                        const int col0 = n0 + tt * T + ch * 32;
+                        if (valid) {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                if (gv[k] > 0.0f) {
+                                    if (g.vals_f32) {
+                                        vals32[slot + c] = gv[k];
+                                    } else {
+                                        const __nv_bfloat16 b = __float2bfloat16_rn(gv[k]);
+                                        vals16[slot + c] = b;
+                                        gv[k] = __bfloat162float(b);
+                                    }
+                                    g.idx[slot + c] = static_cast<uint8_t>(ch * 32 + k);
+                                    ++c;
+                                }
+                            }
+                        }
+                        if (row_ok && col0 < g.ldo) {  // ldo is a multiple of 32: whole chunks
+                            uint4* o = reinterpret_cast<uint4*>(H + static_cast<size_t>(row) * g.ldo + col0);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t ow[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int k = 8 * i + 2 * e;
+                                    const float h0 = gv[k] > 0.0f ? gv[k] * uv[k] : 0.0f;
+                                    const float h1 = gv[k + 1] > 0.0f ? gv[k + 1] * uv[k + 1] : 0.0f;
+                                    over |= !(fabsf(h0) < 65520.0f) || !(fabsf(h1) < 65520.0f);
+                                    const __half2 hh = __floats2half2_rn(h0, h1);
+                                    ow[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                                }
+                                o[i] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                            }
+                        }
+                    }
+                    if (valid) g.cnt[static_cast<size_t>(row) * g.nt + tile] = static_cast<uint16_t>(c);
+                }
+                if (over) report(g.status, TWELL_ERR_DEVICE_CHECK);
+            } else if constexpr (EPI == Epi::PackTwell) {
                 // ReLU + TwELL: per (row, T-wide column tile) keep g > 0 in ascending column order.
                 const int T = g.T;
                 __nv_bfloat16* vals16 = static_cast<__nv_bfloat16*>(g.vals);
@@ -495,7 +561,9 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
 {
     static_assert(!PAIR || (!A_MN && !B_MN), "the CTA-pair GEMM takes K-major operands");
     using Cfg = twell::GemmCfg<BN, PAIR>;
-    if (PAIR && B2 != nullptr) return TWELL_ERR_UNSUPPORTED;
+    constexpr bool DUAL = EPI == twell::Epi::GateUpF16;
+    constexpr int TN = DUAL ? BN / 2 : BN;
+    if (PAIR && (B2 != nullptr) != DUAL) return TWELL_ERR_UNSUPPORTED;
     DevInfo di;
     if (dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
     if (di.max_smem_optin < Cfg::SMEM_BYTES) return TWELL_ERR_UNSUPPORTED;
@@ -515,8 +583,9 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
     if (st != TWELL_OK) return st;
     if (B2 != nullptr) {
         st = B_MN ? make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, 64)
-                  : make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, BN);
+                  : make_tmap_bf16(&tb2, B2->ptr, B2->cols, B2->rows, B2->ld, 64, PAIR ? BN / 2 : BN);
         if (st != TWELL_OK) return st;
+        if (DUAL) g.kb_split = 1 << 30;
     } else {
         tb2 = tb;
         g.kb_split = 1 << 30;
@@ -526,7 +595,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         cudaSuccess)
         return TWELL_ERR_CUDA;
     g.wait_limit_ns = wait_limit_ns();
-    const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + BN - 1) / BN;
+    const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + TN - 1) / TN;
     if (g.k_splits > 1 && (PAIR || EPI != twell::Epi::StoreF32)) return TWELL_ERR_UNSUPPORTED;
     if constexpr (!PAIR) {
         const long long tiles = m_tiles * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);

@@ -15,6 +15,12 @@
 // h and a carry 11 significant bits (fp16); an a or h beyond the fp16 range is recorded as
 // TWELL_ERR_DEVICE_CHECK. (The earlier form of this path carried h as a bf16 hi + lo pair, which
 // doubled K of the down GEMM.)
+//
+// twell_ffn_gate_union_fwd starts from x instead of a TwELL: one tcgen05 GEMM on SM pairs computes
+// the gate and the up projection of the same 128 units in one tile (the even CTA of the pair loads
+// Wg_s rows, the odd CTA Wu_s rows; A = x is shared), and its epilogue packs ReLU(g) into the
+// TwELL exactly as twell_gate_pack does and stores h = a * u (fp16, 0 where g <= 0) -- no expansion
+// pass, no second read of x, no mask. Step 3 follows as above.
 #include "twell_gemm.cuh"
 
 namespace twell {
@@ -81,7 +87,33 @@ struct UnionWs {
 
 size_t twell_host::union_ws_bytes(int N, int f) { return twell::UnionWs(N, f).total; }
 
+size_t twell_host::gate_union_ws_bytes(int N, int f)
+{
+    return (static_cast<size_t>(N) * ((f + 63) / 64 * 64) * 2 + 255) & ~size_t(255);
+}
+
 using namespace twell_host;
+
+namespace {
+
+// y = H Wd16t_s^T over K = f_pad: A = H [N, f_pad] fp16, B = Wd16t_s [d, f] fp16 K-major (columns
+// f .. f_pad read as zeros by TMA), bf16 y, on SM pairs.
+twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
+                        int32_t* dev_status, cudaStream_t s)
+{
+    twell::GemmArgs g2{};
+    g2.M = N;
+    g2.N = d;
+    g2.K = fp;
+    g2.out = y;
+    g2.ldo = d;
+    g2.status = dev_status;
+    return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(GemmOperand{H, N, fp, fp},
+                                                                             GemmOperand{Wd16t_s, d, f, f}, nullptr, g2,
+                                                                             s);
+}
+
+}  // namespace
 
 extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, const void* Wd16t_s, const twell_packed* a,
                                             int32_t N, int32_t d, int32_t f, twell_dtype dtype, void* y, void* ws,
@@ -127,15 +159,48 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
     st = launch_gemm<256, false, false, twell::Epi::MulMaskF16, true>(GemmOperand{x, N, d, d},
                                                                       GemmOperand{Wu_s, f, d, d}, nullptr, g, s);
     if (st != TWELL_OK) return st;
-    // 3. y = H Wd16_s over K = f_pad: B = Wd16t_s [d, f] K-major (columns f .. f_pad read as zeros)
-    twell::GemmArgs g2{};
-    g2.M = N;
-    g2.N = d;
-    g2.K = fp;
-    g2.out = y;
-    g2.ldo = d;
-    g2.status = dev_status;
-    return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(GemmOperand{H, N, fp, fp},
-                                                                             GemmOperand{Wd16t_s, d, f, f}, nullptr, g2,
-                                                                             s);
+    // 3. y = H Wd16_s over K = f_pad
+    return union_down(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+}
+
+extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s, const void* Wu_s,
+                                                 const void* Wd16t_s, int32_t N, int32_t d, int32_t f, int32_t T,
+                                                 twell_dtype dtype, const twell_packed* out, void* y, void* ws,
+                                                 size_t ws_bytes, int32_t* dev_status, void* stream)
+{
+    if (Wg_s == nullptr || Wu_s == nullptr || Wd16t_s == nullptr || out == nullptr || dev_status == nullptr)
+        return TWELL_ERR_INVALID;
+    if ((x == nullptr || y == nullptr) && N != 0) return TWELL_ERR_INVALID;
+    if (N < 0 || d <= 0 || f <= 0 || d % 8 != 0 || f % 8 != 0) return TWELL_ERR_INVALID;
+    if (dtype != TWELL_BF16 || !dtype_ok(out->dtype) || (T != 64 && T != 128)) return TWELL_ERR_UNSUPPORTED;
+    twell_status st = check_packed(out, N, f, T, out->dtype);
+    if (st != TWELL_OK) return st;
+    if (N == 0) return TWELL_OK;
+    if (ws == nullptr || ws_bytes < gate_union_ws_bytes(N, f)) return TWELL_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(Wg_s) || !aligned16(Wu_s) || !aligned16(Wd16t_s) || !aligned16(y) ||
+        !aligned16(ws))
+        return TWELL_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    __half* H = static_cast<__half*>(ws);
+    const int fp = (f + 63) / 64 * 64;
+    // 1 + 2. g and u of each 128-unit block in one tile: TwELL of ReLU(g), h = a * u into H
+    twell::GemmArgs g{};
+    g.M = N;
+    g.N = f;
+    g.K = d;
+    g.out = H;
+    g.ldo = fp;
+    g.vals_f32 = out->dtype == TWELL_F32 ? 1 : 0;
+    g.vals = out->vals;
+    g.idx = out->idx;
+    g.cnt = out->cnt;
+    g.T = T;
+    g.nt = (f + T - 1) / T;
+    g.status = dev_status;
+    const GemmOperand Bu{Wu_s, f, d, d};
+    st = launch_gemm<256, false, false, twell::Epi::GateUpF16, true>(GemmOperand{x, N, d, d},
+                                                                     GemmOperand{Wg_s, f, d, d}, &Bu, g, s);
+    if (st != TWELL_OK) return st;
+    // 3. y = H Wd16_s over K = f_pad
+    return union_down(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
 }

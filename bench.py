@@ -284,7 +284,18 @@ def run_ours(a, rank, world):
     Wd16 = binding.twell_convert_f16(Wd, status=status, stream=stream) if a.path == "tile_union" else None
     Wd16t = binding.twell_convert_f16_transposed(Wd, status=status, stream=stream) if a.path == "union" else None
 
+    # the union path with T = 64 or 128 is one call: gate and up projection in one GEMM, then the down GEMM
+    gate_union = a.path == "union" and T in (64, 128)
+
+    def first():
+        if gate_union:
+            binding.twell_ffn_gate_union_fwd(x, Wg, Wu, Wd16t, T, out=packed, y=y, status=status, stream=stream)
+        else:
+            binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+
     def second():
+        if gate_union:
+            return
         if a.path == "tile_union":
             binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status, stream=stream)
         elif a.path == "union":
@@ -293,7 +304,7 @@ def run_ours(a, rank, world):
             binding.twell_ffn_fused_fwd(x, Wu, Wd, packed, y=y, status=status, stream=stream)
 
     def step():
-        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        first()
         second()
 
     for _ in range(a.warmup):
@@ -315,7 +326,7 @@ def run_ours(a, rank, world):
         flush.fill_(1)
         e0, e1, e2 = ev[i]
         e0.record(stream)
-        binding.twell_gate_pack(x, Wg, T, out=packed, status=status, stream=stream)
+        first()
         e1.record(stream)
         second()
         e2.record(stream)
@@ -372,7 +383,19 @@ def run_ours(a, rank, world):
     mg, mf = sum(t_gate) / a.steps, sum(t_fused) / a.steps
     second_name = {"walk": "twell_ffn_fused_fwd", "union": "twell_ffn_union_fwd",
                    "tile_union": "twell_ffn_tile_union_fwd"}[a.path]
-    if a.path != "walk" and mf >= mg:
+    first_name = "twell_ffn_gate_union_fwd" if gate_union else "twell_gate_pack"
+    if gate_union:
+        # one call: the gate + up GEMM (2 * N * d * 2 f FLOPs, the TwELL packed in its epilogue) and
+        # the down GEMM over f rounded up to 64 (2 * N * f_pad * d)
+        gu_flops = 4.0 * N * d * f + 2.0 * N * ((f + 63) // 64 * 64) * d
+        ach = gu_flops / (mg * 1e-3) / 1e12
+        roof = {"kernel": first_name, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                "algorithmic_flops": gu_flops, "ms_per_launch": mg,
+                "peak_kind": peak_kind + " bf16_tflops (burst; the down GEMM runs fp16, the same rate)",
+                "note": "whole call (gate + up GEMM with the pack and h = a * u in its epilogue, then the "
+                        "down GEMM) against the three products' FLOPs: all of d_ff, the dense regime"}
+    elif a.path != "walk" and mf >= mg:
         # the up and down GEMMs: over each 128-token tile's union (2 * 128 * |U_m| * d FLOPs each per
         # tile), or over all of d_ff rounded up to 64 for the union path
         tu_flops = 4.0 * 128 * union * d if a.path == "tile_union" else 4.0 * N * ((f + 63) // 64 * 64) * d
@@ -606,7 +629,7 @@ def run_ours(a, rank, world):
                            "distinct_active_units": distinct,
                            "definition_strict": "every active weight row read once per layer: max(gate FLOPs / bf16 "
                                                 "peak, (x + Wg + distinct active Wu/Wd rows + y) / HBM peak)"},
-        "kernels_ms": {"twell_gate_pack": mg, second_name: mf},
+        "kernels_ms": {first_name: mg} if gate_union else {"twell_gate_pack": mg, second_name: mf},
         "compacted": compacted,
         "f16down": f16,
         "warm": {"ms_per_step": warm_ms, "tokens_per_s": weak_scaling_rate(N, warm_ms, world),
@@ -617,12 +640,12 @@ def run_ours(a, rank, world):
         "e2e": {"value": N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": N * d * 2,
                 "d2h_bytes_per_step": N * d * 2, "ms_per_step": e2e_ms,
                 "how": "binding.StreamedFFN: each step's pinned H2D copy and D2H copy overlap the neighbouring "
-                       "steps' gate + walk (three streams, double-buffered device x and y)",
+                       "steps' layer calls (three streams, double-buffered device x and y)",
                 "serial": {"value": N / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
-                           "how": "copy in, gate + walk, copy out one after the other on one stream"}},
+                           "how": "copy in, the layer, copy out one after the other on one stream"}},
         # per step: gate + pack, then the walk's plan and the walk; or the union path's expand, up and
         # down GEMMs; or the tile-union path's union bits, prefix, work list, expand, up and down GEMMs
-        "gpu_launches": {"walk": 3, "union": 4, "tile_union": 7}[a.path] * a.steps,
+        "gpu_launches": (2 if gate_union else {"walk": 3, "union": 4, "tile_union": 7}[a.path]) * a.steps,
         "path": a.path,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
@@ -827,6 +850,8 @@ def run_sweep(a):
         Wd16 = binding.twell_convert_f16(Wd, status=status)
         Wd16t = binding.twell_convert_f16_transposed(Wd, status=status)
         union_fn = lambda: binding.twell_ffn_union_fwd(x, Wu, Wd16t, packed, y=y, status=status)  # noqa: E731
+        gu_fn = (lambda: binding.twell_ffn_gate_union_fwd(x, Wg, Wu, Wd16t, L.T, out=packed, y=y,  # noqa: E731
+                                                          status=status)) if L.T in (64, 128) else None
         f16_fn = lambda: binding.twell_ffn_fused_fwd_f16down(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
         tu_fn = lambda: binding.twell_ffn_tile_union_fwd(x, Wu, Wd16, packed, y=y, status=status)  # noqa: E731
 
@@ -838,6 +863,7 @@ def run_sweep(a):
             ms_gate = timed_in_graph(gate_fn, 50)
             ms_fused = timed_in_graph(fused_fn, 50)
             ms_union = timed_in_graph(union_fn, 50)
+            ms_gu = timed_in_graph(gu_fn, 50) if gu_fn else None
             ms_f16 = timed_in_graph(f16_fn, 50)
             ms_tu = timed_in_graph(tu_fn, 50)
             ms_dense = timed_in_graph(dense_fn, 50)
@@ -845,6 +871,7 @@ def run_sweep(a):
             ms_gate = timed(gate_fn, n_it)
             ms_fused = timed(fused_fn, n_it)
             ms_union = timed(union_fn, max(3, min(n_it, 15)))
+            ms_gu = timed(gu_fn, max(3, min(n_it, 15))) if gu_fn else None
             ms_f16 = timed(f16_fn, n_it)
             ms_tu = timed(tu_fn, n_it)
             ms_dense = timed(dense_fn, n_it)
@@ -865,7 +892,8 @@ def run_sweep(a):
                              "summed in a fixed order by a second kernel"}
         binding.check_device_status(label, status)
         ms = ms_gate + ms_fused
-        ms_u = ms_gate + ms_union
+        ms_u2 = ms_gate + ms_union
+        ms_u = ms_gu if ms_gu is not None else ms_u2  # the union path as ffn_forward runs it
         ms_t = ms_gate + ms_tu
         best = min((("walk", ms), ("union", ms_u), ("tile_union", ms_t)), key=lambda kv: kv[1])[0]
         auto = binding.choose_path(L.N, nnz / (L.N * L.f))
@@ -876,7 +904,8 @@ def run_sweep(a):
                           "density": nnz / (L.N * L.f), "nnz_per_token": nnz / L.N, "ms_gate_pack": ms_gate,
                           "ms_fused": ms_fused, "ms_sparse": ms, "tokens_per_s": L.N / (ms * 1e-3),
                           "ms_dense_cublas": ms_dense, "speedup_vs_dense": ms_dense / ms,
-                          "ms_union": ms_union, "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
+                          "ms_union": ms_union, "ms_sparse_union_two_call": ms_u2, "ms_gate_union": ms_gu,
+                          "ms_sparse_union": ms_u, "speedup_union_vs_dense": ms_dense / ms_u,
                           "ms_tile_union": ms_tu, "ms_sparse_tile_union": ms_t,
                           "speedup_tile_union_vs_dense": ms_dense / ms_t,
                           "faster_path": best, "speedup_faster_path_vs_dense": ms_dense / min(ms, ms_u, ms_t),

@@ -68,7 +68,8 @@ typedef enum {
     TWELL_OP_HYBRID_ROUTE = 4,
     TWELL_OP_FFN_UNION_FWD = 5,
     TWELL_OP_FFN_DECODE = 6,
-    TWELL_OP_FFN_TILE_UNION_FWD = 7
+    TWELL_OP_FFN_TILE_UNION_FWD = 7,
+    TWELL_OP_FFN_GATE_UNION_FWD = 8
 } twell_op;
 
 /* A TwELL matrix of gate activations a = ReLU(G), [n_rows, n_cols] ([TG] "Вот тут и решает TwELL";
@@ -242,6 +243,26 @@ TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, cons
                                  const twell_packed* a, int32_t N, int32_t d, int32_t f,
                                  twell_dtype dtype, void* y, void* ws, size_t ws_bytes,
                                  int32_t* dev_status, void* stream);
+
+/* twell_gate_pack followed by twell_ffn_union_fwd, with the gate and the up projection in one
+ * tensor-core GEMM: each tile of an SM pair computes g = x Wg_s^T and u = x Wu_s^T for the same 128
+ * units (the pair's two CTAs load Wg_s and Wu_s rows respectively, x is shared), and its epilogue
+ * packs ReLU(g) into *out -- the TwELL twell_gate_pack writes, bit for bit ([AIM] ¶3, [TC] §2:
+ * the pack in the gate GEMM's epilogue) -- and stores h = a * u (a = the packed value; fp16, 11
+ * significant bits; 0 where g <= 0) into the workspace; then y = H Wd16_s as in twell_ffn_union_fwd.
+ * For layers whose density the walk no longer serves: the union of the units a tile of 128 tokens
+ * keeps is then most of d_ff ([TC] §3: tensor cores for the heavy work).
+ * bf16 x, Wg_s, Wu_s, y (dtype must be TWELL_BF16); d and f multiples of 8; T = 64 or 128 (else
+ * TWELL_ERR_UNSUPPORTED); x [N, d], Wg_s / Wu_s [f, d], Wd16t_s [d, f] (twell_convert_f16_transposed
+ * of Wd_s), y [N, d]; *out a TwELL of N rows, f columns, tile T, fp32 or bf16 values. Device
+ * pointers, 16-byte aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_GATE_UNION_FWD, N, d, f, ...)
+ * bytes (H [N, f_pad] fp16, f_pad = f rounded up to 64), required when N > 0. An h beyond the fp16
+ * range is recorded as TWELL_ERR_DEVICE_CHECK in *dev_status.
+ */
+TWELL_API twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s, const void* Wu_s,
+                                      const void* Wd16t_s, int32_t N, int32_t d, int32_t f, int32_t T,
+                                      twell_dtype dtype, const twell_packed* out, void* y, void* ws,
+                                      size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* y = (a * (x Wu_s^T)) Wd_s from the TwELL a, as tensor-core GEMMs over the units each tile of
  * 128 tokens keeps -- the tile's union U_m -- with the union's weight rows gathered ([TG] "Инференс":

@@ -174,6 +174,30 @@ def test_union_rejects_bad_arguments(lib):
     assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
 
 
+def test_gate_union_rejects_bad_arguments(lib):
+    p = _packed()
+    need = lib.twell_workspace_bytes(8, 4, 64, 256, 128, 0, 0)  # TWELL_OP_FFN_GATE_UNION_FWD
+    assert need >= 4 * 256 * 2  # H [N, f_pad] fp16
+    assert lib.twell_workspace_bytes(8, 3, 64, 1000, 128, 0, 0) >= 3 * 1024 * 2  # f_pad = 1024
+    call = lambda **kw: lib.twell_ffn_gate_union_fwd(  # noqa: E731
+        ALIGNED, kw.get("wg", ALIGNED), ALIGNED, kw.get("wd", ALIGNED), kw.get("N", 4), kw.get("d", 64),
+        kw.get("f", 256), kw.get("T", 128), kw.get("dt", 0), ctypes.byref(kw.get("p", p)), kw.get("y", ALIGNED),
+        kw.get("ws", ALIGNED), kw.get("ws_bytes", need), STATUS, None)
+    assert call(wg=None) == 1
+    assert call(wd=None) == 1
+    assert call(y=None) == 1
+    assert call(ws=None) == 7
+    assert call(ws_bytes=need - 1) == 7
+    assert call(dt=1) == 2  # bf16 only
+    assert call(T=256, p=_packed(T=256)) == 2  # the tile holds 128 units: T = 64 or 128
+    assert call(T=64) == 1  # the TwELL's tile is 128
+    assert call(d=12) == 1
+    assert call(f=252, p=_packed(f=252)) == 1  # f a multiple of 8
+    assert call(N=5) == 1  # the TwELL describes 4 rows
+    assert call(N=0, p=_packed(N=0), ws=None, ws_bytes=0) == 0
+    assert call(y=ctypes.c_void_p((1 << 20) + 8)) == 1
+
+
 def test_fused_f16down_rejects_bad_arguments(lib):
     p = _packed()
     need = lib.twell_workspace_bytes(1, 4, 512, 256, 128, 0, 0)  # TWELL_OP_FFN_FUSED_FWD

@@ -12,6 +12,7 @@ def test_density_chooses_walk_or_union():
     n = binding.DECODE_MAX_N + 1
     assert binding.choose_path(n, None) == "walk"  # no estimate yet: the walk
     assert binding.choose_path(n, 0.005) == "walk"
+    assert binding.choose_path(n, 0.01) == "union"
     assert binding.choose_path(n, binding.UNION_MIN_DENSITY) == "union"
     assert binding.choose_path(8192, 0.02) == "union"
     assert binding.choose_path(8192, 0.5) == "union"
