@@ -466,8 +466,8 @@ twell_status dev_info(DevInfo* out);
 // Bytes of the workspace twell_ffn_fused_fwd needs for N token rows, d_model d, d_ff f (twell_ffn.cu).
 size_t fused_ws_bytes(int N, int d, int f);
 // Bytes of the workspace twell_ffn_union_fwd needs (twell_union.cu).
-size_t union_ws_bytes(int N, int f);
-size_t gate_union_ws_bytes(int N, int f);
+size_t union_ws_bytes(int N, int d, int f);
+size_t gate_union_ws_bytes(int N, int d, int f);
 // Bytes of the workspace twell_ffn_tile_union_fwd needs (twell_tile_union.cu).
 size_t tile_union_ws_bytes(int N, int f);
 // Bytes of the workspace twell_ffn_decode needs (twell_decode.cu).

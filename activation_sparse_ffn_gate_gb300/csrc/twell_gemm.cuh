@@ -15,7 +15,7 @@
 // M and K may be read from device memory (rows of a device-side list, e.g. the hybrid backup
 // rows), so a launch sized for an upper bound does only the work that exists.
 //
-// Split K (k_splits > 1, StoreF32, one CTA per tile): the k-blocks of each tile are cut into
+// Split K (k_splits > 1, StoreF32; one CTA or one CTA pair per tile): the k-blocks of each tile are cut into
 // k_splits near-equal ranges, each a work unit of its own, and split s stores its partial sum at
 // out + s * split_stride; the caller adds the partials in split order (a fixed order, so the
 // result does not depend on scheduling). For products with few rows and a long K (the hybrid
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int n_tiles = (g.N + TN - 1) / TN;
     const int kbs = K > 0 ? (K + kBK - 1) / kBK : 0;
     // k-block ranges per tile: ks of them, each non-empty
-    const int ks = (PAIR || EPI != Epi::StoreF32 || g.k_splits <= 1) ? 1 : min(g.k_splits, max(kbs, 1));
+    const int ks = (EPI != Epi::StoreF32 || g.k_splits <= 1) ? 1 : min(g.k_splits, max(kbs, 1));
     // work units: one 128 x BN tile per CTA, or with PAIR one 256 x BN tile per cluster, of which
     // this CTA holds the 128 rows of its rank (past M its loads read zeros and its epilogue
     // writes nothing)
@@ -596,7 +596,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         return TWELL_ERR_CUDA;
     g.wait_limit_ns = wait_limit_ns();
     const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + TN - 1) / TN;
-    if (g.k_splits > 1 && (PAIR || EPI != twell::Epi::StoreF32)) return TWELL_ERR_UNSUPPORTED;
+    if (g.k_splits > 1 && EPI != twell::Epi::StoreF32) return TWELL_ERR_UNSUPPORTED;
     if constexpr (!PAIR) {
         const long long tiles = m_tiles * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
         const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
@@ -617,7 +617,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         cfg.gridDim = dim3(2 * static_cast<unsigned>(di.sm_count / 2));
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return TWELL_ERR_CUDA;
-        const long long units = ((m_tiles + 1) / 2) * n_tiles;
+        const long long units = ((m_tiles + 1) / 2) * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
         if (clusters > units) clusters = static_cast<int>(units);
         cfg.gridDim = dim3(2 * static_cast<unsigned>(clusters));
         if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g) != cudaSuccess) return TWELL_ERR_CUDA;

@@ -833,9 +833,9 @@ extern "C" size_t twell_workspace_bytes(twell_op op, int32_t N, int32_t d, int32
     switch (op) {
     case TWELL_OP_GATE_PACK: return 0;
     case TWELL_OP_FFN_FUSED_FWD: return twell_host::fused_ws_bytes(N, d, f);
-    case TWELL_OP_FFN_UNION_FWD: return twell_host::union_ws_bytes(N, f);
+    case TWELL_OP_FFN_UNION_FWD: return twell_host::union_ws_bytes(N, d, f);
     case TWELL_OP_FFN_TILE_UNION_FWD: return twell_host::tile_union_ws_bytes(N, f);
-    case TWELL_OP_FFN_GATE_UNION_FWD: return twell_host::gate_union_ws_bytes(N, f);
+    case TWELL_OP_FFN_GATE_UNION_FWD: return twell_host::gate_union_ws_bytes(N, d, f);
     case TWELL_OP_FFN_DECODE: return tile > 0 ? twell_host::decode_ws_bytes(N, d, f, tile) : 0;
     case TWELL_OP_HYBRID_ROUTE: return twell::HybridWs(N, d, f, K, backup_cap).route_total;
     case TWELL_OP_HYBRID_FWD: return twell::HybridWs(N, d, f, K, backup_cap).fwd_total;

@@ -21,6 +21,14 @@
 // Wg_s rows, the odd CTA Wu_s rows; A = x is shared), and its epilogue packs ReLU(g) into the
 // TwELL exactly as twell_gate_pack does and stores h = a * u (fp16, 0 where g <= 0) -- no expansion
 // pass, no second read of x, no mask. Step 3 follows as above.
+//
+// Small batches: with at most 1024 tokens the down GEMM has too few 256 x 256 tiles to occupy the SM
+// pairs (8 at 64 tokens and d_model 2048), and each pair would stream a whole 256-row block of
+// Wd16t_s. There K = f_pad is split into ks ranges (ks * ceil(N / 256) <= 8), each range a work
+// unit that stores an fp32 partial product, and a second kernel adds the partials in range order
+// (a fixed order: y does not depend on scheduling) and rounds to bf16.
+#include <algorithm>
+
 #include "twell_gemm.cuh"
 
 namespace twell {
@@ -69,48 +77,111 @@ __global__ void __launch_bounds__(256) expand_f16_mask_kernel(const Ein* __restr
     if (bad) report(status, TWELL_ERR_DEVICE_CHECK);
 }
 
+// Most rows whose split partial products the down GEMM stores: ks * ceil(N / 256) <= 8 pairs of
+// 128-row tiles, i.e. ks * N <= 2048, and splitting only for N <= 1024.
+constexpr int kSplitMaxRows = 2048;
+constexpr int kSplitMaxN = 1024;
+
+// y[i] = bf16(part[0][i] + part[1][i] + ... + part[ks - 1][i]) for four elements per thread.
+__global__ void __launch_bounds__(256) reduce_splits_bf16_kernel(const float* __restrict__ part, int ks, size_t n,
+                                                                 __nv_bfloat16* __restrict__ y)
+{
+    const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+    if (i >= n) return;
+    float4 a = *reinterpret_cast<const float4*>(part + i);
+    for (int sp = 1; sp < ks; ++sp) {
+        const float4 b = *reinterpret_cast<const float4*>(part + static_cast<size_t>(sp) * n + i);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + i) = w;
+}
+
+inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// bytes of the split partials a call may need (0 above kSplitMaxN tokens)
+inline size_t split_bytes(int N, int d)
+{
+    return N <= kSplitMaxN ? up256(static_cast<size_t>(kSplitMaxRows) * d * 4) : 0;
+}
+
 struct UnionWs {
     int f_pad = 0;
-    size_t mask = 0, h = 0, total = 0;
-    static size_t up(size_t v) { return (v + 255) & ~size_t(255); }
-    UnionWs(int N, int f)
+    size_t mask = 0, h = 0, part = 0, total = 0;
+    UnionWs(int N, int d, int f)
     {
         f_pad = (f + 63) / 64 * 64;
         mask = 0;
-        h = up(static_cast<size_t>(N) * (f_pad / 32) * 4);
-        total = h + up(static_cast<size_t>(N) * f_pad * 2);
+        h = up256(static_cast<size_t>(N) * (f_pad / 32) * 4);
+        part = h + up256(static_cast<size_t>(N) * f_pad * 2);
+        total = part + split_bytes(N, d);
     }
 };
 
 }  // namespace
 }  // namespace twell
 
-size_t twell_host::union_ws_bytes(int N, int f) { return twell::UnionWs(N, f).total; }
+size_t twell_host::union_ws_bytes(int N, int d, int f) { return twell::UnionWs(N, d, f).total; }
 
-size_t twell_host::gate_union_ws_bytes(int N, int f)
+size_t twell_host::gate_union_ws_bytes(int N, int d, int f)
 {
-    return (static_cast<size_t>(N) * ((f + 63) / 64 * 64) * 2 + 255) & ~size_t(255);
+    return twell::up256(static_cast<size_t>(N) * ((f + 63) / 64 * 64) * 2) + twell::split_bytes(N, d);
 }
 
 using namespace twell_host;
 
 namespace {
 
+// Ranges K is split into for the down GEMM: enough work units for half the SM pairs or more, at
+// least four k-blocks per range, ks * ceil(N / 256) <= 8; 1 above kSplitMaxN tokens.
+int union_down_splits(int N, int d, int fp)
+{
+    if (N > twell::kSplitMaxN) return 1;
+    DevInfo di;
+    if (dev_info(&di) != TWELL_OK) return 1;
+    const int pairs = di.sm_count / 2;
+    const int m_pairs = (N + 255) / 256, n_tiles = (d + 255) / 256;
+    const int units = m_pairs * n_tiles;
+    if (2 * units >= pairs) return 1;
+    int ks = (pairs + units - 1) / units;
+    ks = std::min(ks, twell::kSplitMaxRows / 256 / m_pairs);
+    ks = std::min(ks, fp / twell::kBK / 4);
+    return std::max(ks, 1);
+}
+
 // y = H Wd16t_s^T over K = f_pad: A = H [N, f_pad] fp16, B = Wd16t_s [d, f] fp16 K-major (columns
-// f .. f_pad read as zeros by TMA), bf16 y, on SM pairs.
-twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
+// f .. f_pad read as zeros by TMA), bf16 y, on SM pairs; for small batches split along K into fp32
+// partials at `part` (split_bytes(N, d) bytes), added in order by reduce_splits_bf16_kernel.
+twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
                         int32_t* dev_status, cudaStream_t s)
 {
+    const int ks = union_down_splits(N, d, fp);
     twell::GemmArgs g2{};
     g2.M = N;
     g2.N = d;
     g2.K = fp;
-    g2.out = y;
     g2.ldo = d;
     g2.status = dev_status;
-    return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(GemmOperand{H, N, fp, fp},
-                                                                             GemmOperand{Wd16t_s, d, f, f}, nullptr, g2,
-                                                                             s);
+    const GemmOperand A{H, N, fp, fp}, B{Wd16t_s, d, f, f};
+    if (ks <= 1) {
+        g2.out = y;
+        return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(A, B, nullptr, g2, s);
+    }
+    g2.out = part;
+    g2.k_splits = ks;
+    g2.split_stride = static_cast<int64_t>(N) * d;
+    twell_status st = launch_gemm<256, false, false, twell::Epi::StoreF32, true, true>(A, B, nullptr, g2, s);
+    if (st != TWELL_OK) return st;
+    const size_t n = static_cast<size_t>(N) * d;
+    const unsigned blocks = static_cast<unsigned>((n / 4 + 255) / 256);
+    twell::reduce_splits_bf16_kernel<<<blocks, 256, 0, s>>>(part, ks, n, static_cast<__nv_bfloat16*>(y));
+    return launch_status();
 }
 
 }  // namespace
@@ -126,7 +197,7 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
     twell_status st = check_packed(a, N, f, a->tile, a->dtype);
     if (st != TWELL_OK) return st;
     if (N == 0) return TWELL_OK;
-    const twell::UnionWs L(N, f);
+    const twell::UnionWs L(N, d, f);
     if (ws == nullptr || ws_bytes < L.total) return TWELL_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(Wu_s) || !aligned16(Wd16t_s) || !aligned16(y) || !aligned16(ws))
         return TWELL_ERR_INVALID;
@@ -160,7 +231,8 @@ extern "C" twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, con
                                                                       GemmOperand{Wu_s, f, d, d}, nullptr, g, s);
     if (st != TWELL_OK) return st;
     // 3. y = H Wd16_s over K = f_pad
-    return union_down(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    return union_down(H, Wd16t_s, N, d, f, fp, y, reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.part),
+                      dev_status, s);
 }
 
 extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s, const void* Wu_s,
@@ -176,7 +248,7 @@ extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s
     twell_status st = check_packed(out, N, f, T, out->dtype);
     if (st != TWELL_OK) return st;
     if (N == 0) return TWELL_OK;
-    if (ws == nullptr || ws_bytes < gate_union_ws_bytes(N, f)) return TWELL_ERR_WORKSPACE;
+    if (ws == nullptr || ws_bytes < gate_union_ws_bytes(N, d, f)) return TWELL_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(Wg_s) || !aligned16(Wu_s) || !aligned16(Wd16t_s) || !aligned16(y) ||
         !aligned16(ws))
         return TWELL_ERR_INVALID;
@@ -202,5 +274,7 @@ extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s
                                                                      GemmOperand{Wg_s, f, d, d}, &Bu, g, s);
     if (st != TWELL_OK) return st;
     // 3. y = H Wd16_s over K = f_pad
-    return union_down(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                           twell::up256(static_cast<size_t>(N) * fp * 2));
+    return union_down(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
 }

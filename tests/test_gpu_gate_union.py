@@ -7,6 +7,7 @@ the TwELL packed and h = a * u formed in its epilogue, then the fp16 down GEMM) 
 - y against the fp64 oracle (rel-Frobenius <= 5e-3, max-abs <= 2e-2 x RMS per row) on ragged
   batches, the sweep shapes (sampled rows) and the full-size 1.5B-like / 2B-like layers
   (sampled rows plus the densest rows);
+- batches of at most 1024 tokens, whose down GEMM splits K into fp32 partials added in order;
 - edge cases: zero density (y == 0, no entries), every unit kept, N = 1 / 7, an empty batch,
   T = 256 refused, the same bits on a second call.
 """
@@ -142,14 +143,16 @@ def _sampled_rows(N, n, seed, extra=()):
     return np.unique(np.concatenate([[0, 1, N - 1], rng.choice(N, n, replace=False), np.asarray(extra, dtype=np.int64)]))
 
 
-@pytest.mark.parametrize("p", [0.005, 0.01, 0.02, 0.1, 0.5])
-def test_gate_union_sweep_shapes_sampled(cuda_dev, p):
-    """The sweep's shapes (d_model 2048, d_ff 5632, T = 128) at N = 1024, on sampled rows."""
-    L = synthetic.sweep_point(p, 128, N=1024)
+@pytest.mark.parametrize("p,N", [(0.005, 1024), (0.01, 1024), (0.02, 1024), (0.1, 1024), (0.5, 1024),
+                                 (0.01, 8192), (0.02, 8192), (0.05, 8192)])
+def test_gate_union_sweep_shapes_sampled(cuda_dev, p, N):
+    """The sweep's shapes (d_model 2048, d_ff 5632, T = 128) at N = 1024 and, for 1%, 2% and 5%, at
+    the sweep's full 8192 tokens, on sampled rows."""
+    L = synthetic.sweep_point(p, 128, N=N)
     y, _ = _run(cuda_dev, L.torch_inputs(cuda_dev), 128)
     rows = _sampled_rows(L.N, 16, seed=int(p * 1e4))
     y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
-    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"gate union sweep p={p}")
+    assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"gate union sweep p={p} N={N}")
 
 
 @pytest.mark.parametrize("which", ["1.5b", "2b"])
@@ -161,3 +164,21 @@ def test_gate_union_full_size_layers_sampled(cuda_dev, which):
     rows = _sampled_rows(L.N, 24, seed=2, extra=longest)
     y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
     assert_close(y[torch.from_numpy(rows).to(cuda_dev)].double().cpu().numpy(), y_ref, f"gate union {which}")
+
+
+@pytest.mark.parametrize("N", [17, 64, 256, 512, 1024])
+def test_gate_union_small_batches_split_down_gemm(cuda_dev, N):
+    """Batches of at most 1024 tokens split the down GEMM's K into fp32 partials that a second kernel
+    adds in order: the 1.5B-like layer's shapes, every row (N <= 256) or sampled rows plus the densest,
+    against the oracle; the two-call union path on the same TwELL agrees as well."""
+    L = synthetic.layer_1p5b(N=N)
+    t = L.torch_inputs(cuda_dev)
+    Wd16t = binding.twell_convert_f16_transposed(t["Wd_s"])
+    y, tw = binding.twell_ffn_gate_union_fwd(t["x"], t["Wg_s"], t["Wu_s"], Wd16t, 128)
+    y2 = binding.twell_ffn_union_fwd(t["x"], t["Wu_s"], Wd16t, tw)
+    longest = torch.argsort(tw.counts().sum(1), descending=True)[:4].cpu().numpy()
+    rows = np.arange(N) if N <= 256 else _sampled_rows(N, 24, seed=N, extra=longest)
+    y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
+    sel = torch.from_numpy(rows).to(cuda_dev)
+    assert_close(y[sel].double().cpu().numpy(), y_ref, f"gate union split N={N}")
+    assert_close(y2[sel].double().cpu().numpy(), y_ref, f"two-call union split N={N}")
