@@ -493,21 +493,32 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
 # Density (kept fraction of d_ff per token) above which the union path beats the walk, measured with
 # the whole layer on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
 #   density                               0.1%    0.5%    1%      2%      5%      10%     50%
-#   walk (gate + pack, then the walk)     0.193   0.327   0.473   0.791   1.739   3.333   15.33
-#   union (gate + up in one GEMM, down)   0.322   0.324   0.326   0.330   0.336   0.347   0.572
-#   tile union (gate, then gathered)      0.238   0.378   0.481   0.589   0.692   0.787   1.613
-#   dense cuBLAS FFN                      0.368   0.368   0.370   0.371   0.370   0.370   0.378
-# The two cross between 0.5% and 1% (within 1% of each other at 0.5%). The gathered tile-union path
-# is never the fastest under these uniform densities; it stays available as path "tile_union".
+#   walk (gate + pack, then the walk)     0.188   0.326   0.469   0.789   1.727   3.349   15.31
+#   union (gate + up in one GEMM, down)   0.318   0.320   0.322   0.325   0.332   0.347   0.570
+#   tile union (gate, then gathered)      0.235   0.374   0.481   0.585   0.687   0.789   1.619
+#   dense cuBLAS FFN                      0.364   0.365   0.366   0.366   0.368   0.366   0.370
+# They cross near 0.5% at 8192 tokens. On the 1.5B-like layer (0.5% kept) the union path is also the
+# faster of the two for every batch of 32 to 4096 tokens (us; dense in brackets):
+#   tokens      32     64     128    256    512    1024   2048    4096
+#   walk        41.0   45.2   55.7   63.9   72.3   92.3   125.9   188.5
+#   union       36.9   37.0   41.6   43.0   54.1   72.5   92.8    168.7
+#   dense      (32.8) (30.1) (32.5) (34.9) (49.1) (66.3) (109.7) (192.1)
+# so batches of up to 4096 tokens switch at a lower density. The gathered tile-union path is never
+# the fastest under these densities; it stays available as path "tile_union".
 UNION_MIN_DENSITY = 0.006
+UNION_MIN_DENSITY_SMALL_BATCH = 0.004
+SMALL_BATCH_MAX_N = 4096
 
 
 def choose_path(n_tokens: int, density: Optional[float]) -> str:
     """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the walk below
-    UNION_MIN_DENSITY (or without a density estimate); the union GEMMs over all of d_ff above it."""
+    UNION_MIN_DENSITY (UNION_MIN_DENSITY_SMALL_BATCH up to SMALL_BATCH_MAX_N tokens) or without a
+    density estimate; the union path (gate and up projection in one GEMM, down GEMM over all of
+    d_ff) above it."""
     if n_tokens <= DECODE_MAX_N:
         return "decode"
-    if density is None or density < UNION_MIN_DENSITY:
+    limit = UNION_MIN_DENSITY_SMALL_BATCH if n_tokens <= SMALL_BATCH_MAX_N else UNION_MIN_DENSITY
+    if density is None or density < limit:
         return "walk"
     return "union"
 

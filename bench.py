@@ -58,9 +58,12 @@ def _args():
                    help="workload of the main line: 1 = the 1.5B-like layer (default), 2 = the 2B-like layer "
                         "(N=16384, d_model 2560, d_ff 6912, lognormal per-token density; no dead-column step)")
     p.add_argument("--path", choices=["walk", "union", "tile_union"], default="walk",
-                   help="second call of the step: the fused walk (default), the union GEMMs over all of d_ff "
-                        "(twell_ffn_union_fwd) or the tile-union GEMMs (twell_ffn_tile_union_fwd); the last two "
+                   help="the step: gate + pack then the fused walk (default); the union path "
+                        "(twell_ffn_gate_union_fwd: gate and up projection in one GEMM, then the down GEMM over all "
+                        "of d_ff); or gate + pack then the tile-union GEMMs (twell_ffn_tile_union_fwd); the last two "
                         "with Wd_s converted to fp16 once outside the timed region")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="batch size of the --config layer's main line (default: the layer's own, 8192 / 16384)")
     p.add_argument("--density", type=float, default=None,
                    help="run the main line on the sweep's uniform-density layer (N=8192, d_model 2048, d_ff 5632, "
                         "T=128) with this kept fraction instead of the --config layer")
@@ -268,8 +271,9 @@ def run_ours(a, rank, world):
     if a.density is not None:
         L = synthetic.sweep_point(a.density, 128, seed=3 + rank)
     else:
-        L = synthetic.layer_1p5b(seed=1 + rank) if a.config == 1 else synthetic.layer_2b(seed=2 + rank)
-    main_cfg1 = a.density is None and a.config == 1
+        kw = {} if a.tokens is None else {"N": a.tokens}
+        L = synthetic.layer_1p5b(seed=1 + rank, **kw) if a.config == 1 else synthetic.layer_2b(seed=2 + rank, **kw)
+    main_cfg1 = a.density is None and a.config == 1 and a.tokens is None
     t = L.torch_inputs(dev)
     x, Wg, Wu, Wd = t["x"], t["Wg_s"], t["Wu_s"], t["Wd_s"]
     N, d, f, T = L.N, L.d, L.f, L.T
@@ -655,6 +659,19 @@ def run_ours(a, rank, world):
         dist.destroy_process_group()
 
 
+def hybrid_context_bytes(N, f, K, cap_rows, value_bytes=4):
+    """Activation memory the hybrid backward reads from the forward, per layer (x is common to the
+    hybrid and the dense step): a and u (value_bytes each; fp32 as the kernels store them) and the
+    int16 column at each of the N * K block slots, the int16 row counts, the int32 backup list and
+    the backup rows' dense a and u ([cap_rows, d_ff], value_bytes each)."""
+    return N * K * (2 * value_bytes + 2) + N * 2 + cap_rows * 4 + 2 * cap_rows * f * value_bytes
+
+
+def dense_context_bytes(N, f):
+    """The dense step's saved gate pre-activation and up projection, [N, d_ff] bf16 each."""
+    return 2 * N * f * 2
+
+
 def train_step_measure(a, dev, flush, peaks, literal=False):
     """The hybrid training step on the 2B-like layer (N=16384, d=2560, f=6912, K=64, L1 2e-5):
     twell_hybrid_fwd + twell_hybrid_bwd, against a dense cuBLAS bf16 step of the same layer. The
@@ -724,18 +741,10 @@ def train_step_measure(a, dev, flush, peaks, literal=False):
         raise RuntimeError(f"hybrid training step reported status {code}")
     ms_dense = timed(dense, max(5, a.train_steps // 2))
     nb = int(ctx.n_backup.item())
-    # Activation memory the backward needs from the forward, per layer (x itself is common to both):
-    # the hybrid context (a, u fp32 and the column at each of the N*K block slots, the row counts,
-    # the backup list and the backup rows' dense a and u in fp32) against the dense step's saved
-    # gate pre-activation and up projection ([N, d_ff] bf16 each).
-    def hybrid_bytes(cap_rows):
-        return N * K * (4 + 4 + 2) + N * 2 + cap_rows * 4 + 2 * cap_rows * f * 4
-    def hybrid_bytes_bf16(cap_rows):  # the same format with a, u, A_b, U_b stored in bf16
-        return N * K * (2 + 2 + 2) + N * 2 + cap_rows * 4 + 2 * cap_rows * f * 2
-    act = {"hybrid_bytes_as_run": hybrid_bytes(cap), "backup_cap_as_run": cap, "backup_rows": nb,
-           "hybrid_bytes_exact": hybrid_bytes(nb), "dense_bytes": 2 * N * f * 2,
-           "ratio_dense_over_hybrid": (2 * N * f * 2) / hybrid_bytes(cap),
-           "hybrid_bytes_if_bf16_storage": hybrid_bytes_bf16(cap),
+    act = {"hybrid_bytes_as_run": hybrid_context_bytes(N, f, K, cap), "backup_cap_as_run": cap, "backup_rows": nb,
+           "hybrid_bytes_exact": hybrid_context_bytes(N, f, K, nb), "dense_bytes": dense_context_bytes(N, f),
+           "ratio_dense_over_hybrid": dense_context_bytes(N, f) / hybrid_context_bytes(N, f, K, cap),
+           "hybrid_bytes_if_bf16_storage": hybrid_context_bytes(N, f, K, cap, value_bytes=2),
            "note": "what the backward reads from the forward per layer: the hybrid context with a, u, A_b, U_b "
                    "in fp32 as the kernels store them (backup buffers sized from the routed count + 12.5%); "
                    "dense = g and u, [N, d_ff] bf16 each; hybrid_bytes_if_bf16_storage is the format's size "
@@ -834,7 +843,8 @@ def run_sweep(a):
     points = [(p, T) for T in synthetic.SWEEP_TILES for p in synthetic.SWEEP_DENSITIES]
     layers = [(f"sweep p={p:g} T={T}", lambda p=p, T=T: synthetic.sweep_point(p, T)) for p, T in points]
     layers.append(("layer2b", synthetic.layer_2b))
-    layers += [(f"decode N={n}", lambda n=n: synthetic.layer_1p5b(N=n)) for n in (1, 8, 16, 32, 64, 512)]
+    layers += [(f"batch N={n}", lambda n=n: synthetic.layer_1p5b(N=n))
+               for n in (1, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)]
     layers = [(label, make) for label, make in layers if a.sweep_only in label]
     for label, make in layers:
         L = make()
@@ -858,7 +868,7 @@ def run_sweep(a):
         def dense_fn():
             return (torch.relu(x @ Wg.T) * (x @ Wu.T)) @ Wd
 
-        use_graphs = label.startswith("decode")
+        use_graphs = label.startswith("batch")
         if use_graphs:
             ms_gate = timed_in_graph(gate_fn, 50)
             ms_fused = timed_in_graph(fused_fn, 50)

@@ -9,10 +9,18 @@ def test_small_batches_take_the_decode_path():
 
 
 def test_density_chooses_walk_or_union():
-    n = binding.DECODE_MAX_N + 1
+    n = binding.SMALL_BATCH_MAX_N + 1
     assert binding.choose_path(n, None) == "walk"  # no estimate yet: the walk
-    assert binding.choose_path(n, 0.005) == "walk"
-    assert binding.choose_path(n, 0.01) == "union"
+    assert binding.choose_path(8192, 0.005) == "walk"
+    assert binding.choose_path(8192, 0.01) == "union"
     assert binding.choose_path(n, binding.UNION_MIN_DENSITY) == "union"
     assert binding.choose_path(8192, 0.02) == "union"
     assert binding.choose_path(8192, 0.5) == "union"
+
+
+def test_batches_up_to_4096_tokens_switch_at_a_lower_density():
+    for n in (binding.DECODE_MAX_N + 1, 64, 512, binding.SMALL_BATCH_MAX_N):
+        assert binding.choose_path(n, None) == "walk"
+        assert binding.choose_path(n, 0.001) == "walk"
+        assert binding.choose_path(n, 0.005) == "union"
+        assert binding.choose_path(n, binding.UNION_MIN_DENSITY_SMALL_BATCH) == "union"
