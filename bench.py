@@ -590,6 +590,41 @@ def run_ours(a, rank, world):
                                 "speedup_vs_dense": (dense["ms"] / (gc + wc)) if dense else None}
             del Wd16_c
         del Wd16, y16
+
+    # ---- the union path on the same workload (gate and up projection in one GEMM, fp16 down GEMM),
+    # and on the compacted weights: the layer's other path, beside the walk
+    union_sub = None
+    if not a.no_f16down and a.path == "walk" and T in (64, 128):
+        nu = max(10, min(a.steps, 200))
+        Wd16t_m = binding.twell_convert_f16_transposed(Wd, status=status, stream=stream)
+        yu = torch.empty_like(y)
+        gu_ms, _ = medians_gate_walk(
+            lambda: binding.twell_ffn_gate_union_fwd(x, Wg, Wu, Wd16t_m, T, out=packed, y=yu, status=status,
+                                                     stream=stream),
+            lambda: None, nu)
+        binding.check_device_status("union", status)
+        union_sub = {"ms_per_step": gu_ms, "tokens_per_s": N / (gu_ms * 1e-3),
+                     "speedup_vs_dense": (dense["ms"] / gu_ms) if dense else None,
+                     "note": "twell_ffn_gate_union_fwd on the same batch (the TwELL packed in the gate + up GEMM's "
+                             "epilogue, h in fp16, down GEMM over all of d_ff); medians, L2 flushed"}
+        if Wd_c is not None:
+            # the union path wants d_ff a multiple of 8: pad the live units with zero rows (g = 0 is
+            # never kept, so y is unchanged)
+            f_c = Wg_c.shape[0]
+            pad = (f_c + 7) // 8 * 8 - f_c
+            Wg_p, Wu_p, Wd_p = (torch.cat([w, w.new_zeros((pad, d))]) for w in (Wg_c, Wu_c, Wd_c))
+            Wd16t_c = binding.twell_convert_f16_transposed(Wd_p, status=status, stream=stream)
+            packed_p = binding.TwELL.empty(N, f_c + pad, T, torch.float32, dev)
+            yc = torch.empty_like(y)
+            gc_ms, _ = medians_gate_walk(
+                lambda: binding.twell_ffn_gate_union_fwd(x, Wg_p, Wu_p, Wd16t_c, T, out=packed_p, y=yc,
+                                                         status=status, stream=stream),
+                lambda: None, nu)
+            binding.check_device_status("union compacted", status)
+            union_sub["compacted"] = {"ms_per_step": gc_ms, "tokens_per_s": N / (gc_ms * 1e-3), "units": f_c + pad,
+                                      "speedup_vs_dense": (dense["ms"] / gc_ms) if dense else None}
+            del Wd16t_c, yc, Wg_p, Wu_p, Wd_p, packed_p
+        del Wd16t_m, yu
     del packed_c, Wg_c, Wu_c, Wd_c
 
     train = None
@@ -635,6 +670,7 @@ def run_ours(a, rank, world):
                                                 "peak, (x + Wg + distinct active Wu/Wd rows + y) / HBM peak)"},
         "kernels_ms": {first_name: mg} if gate_union else {"twell_gate_pack": mg, second_name: mf},
         "compacted": compacted,
+        "union": union_sub,
         "f16down": f16,
         "warm": {"ms_per_step": warm_ms, "tokens_per_s": weak_scaling_rate(N, warm_ms, world),
                  "l2": "not flushed between steps"},
