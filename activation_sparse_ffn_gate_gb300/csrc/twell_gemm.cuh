@@ -86,6 +86,10 @@ struct GemmArgs {
     uint8_t* idx;
     uint16_t* cnt;
     int T, nt;
+    // launched as a programmatic dependent of the previous kernel on the stream: the prologue
+    // (barriers, TMEM, tensor-map prefetch) overlaps that kernel's last wave, and every thread
+    // waits for it to complete (griddepcontrol.wait) before any role starts (no M_dyn / K_dyn)
+    int pdl;
     // status
     int32_t* status;
     uint64_t wait_limit_ns;
@@ -97,7 +101,7 @@ constexpr int kBK = 64;
 
 template <int BN, bool PAIR = false>
 struct GemmCfg {
-    static constexpr int STAGES = (BN == 256 && !PAIR) ? 4 : 6;
+    static constexpr int STAGES = (BN == 256 && !PAIR) ? 4 : (PAIR ? 7 : 6);
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;  // this CTA's share of B
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -133,6 +137,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a kernel launched as this one's programmatic dependent may be scheduled now (it waits for
+    // this grid to complete before it reads anything this grid writes)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     int M = g.M;
     if (g.M_dyn != nullptr) M = min(M, *g.M_dyn);
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and TMEM exist before either is used
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (g.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's writes are visible
     // the even CTA's barriers, as shared::cluster addresses (PAIR)
     const uint32_t full_lead = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
     const uint32_t tempty_lead = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
@@ -595,20 +603,37 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         cudaSuccess)
         return TWELL_ERR_CUDA;
     g.wait_limit_ns = wait_limit_ns();
+    if (g.pdl && (g.M_dyn != nullptr || g.K_dyn != nullptr)) return TWELL_ERR_UNSUPPORTED;
     const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + TN - 1) / TN;
     if (g.k_splits > 1 && EPI != twell::Epi::StoreF32) return TWELL_ERR_UNSUPPORTED;
     if constexpr (!PAIR) {
         const long long tiles = m_tiles * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
         const int grid = static_cast<int>(tiles < di.sm_count ? tiles : di.sm_count);
-        kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
+        if (!g.pdl) {
+            kern<<<grid, twell::kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, tb2, g);
+            return launch_status();
+        }
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(twell::kGemmThreads);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g) != cudaSuccess) return TWELL_ERR_CUDA;
         return launch_status();
     } else {
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.blockDim = dim3(twell::kGemmThreads);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
@@ -620,6 +645,7 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         const long long units = ((m_tiles + 1) / 2) * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
         if (clusters > units) clusters = static_cast<int>(units);
         cfg.gridDim = dim3(2 * static_cast<unsigned>(clusters));
+        cfg.numAttrs = g.pdl ? 2 : 1;
         if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g) != cudaSuccess) return TWELL_ERR_CUDA;
         return launch_status();
     }

@@ -83,9 +83,11 @@ constexpr int kSplitMaxRows = 2048;
 constexpr int kSplitMaxN = 1024;
 
 // y[i] = bf16(part[0][i] + part[1][i] + ... + part[ks - 1][i]) for four elements per thread.
+// Launched as a programmatic dependent of the down GEMM: it waits for that grid before reading.
 __global__ void __launch_bounds__(256) reduce_splits_bf16_kernel(const float* __restrict__ part, int ks, size_t n,
                                                                  __nv_bfloat16* __restrict__ y)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
     if (i >= n) return;
     float4 a = *reinterpret_cast<const float4*>(part + i);
@@ -168,6 +170,7 @@ twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int 
     g2.K = fp;
     g2.ldo = d;
     g2.status = dev_status;
+    g2.pdl = 1;  // its prologue overlaps the producing GEMM's last wave
     const GemmOperand A{H, N, fp, fp}, B{Wd16t_s, d, f, f};
     if (ks <= 1) {
         g2.out = y;
@@ -179,8 +182,18 @@ twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int 
     twell_status st = launch_gemm<256, false, false, twell::Epi::StoreF32, true, true>(A, B, nullptr, g2, s);
     if (st != TWELL_OK) return st;
     const size_t n = static_cast<size_t>(N) * d;
-    const unsigned blocks = static_cast<unsigned>((n / 4 + 255) / 256);
-    twell::reduce_splits_bf16_kernel<<<blocks, 256, 0, s>>>(part, ks, n, static_cast<__nv_bfloat16*>(y));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>((n / 4 + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, twell::reduce_splits_bf16_kernel, static_cast<const float*>(part), ks, n,
+                           static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
+        return TWELL_ERR_CUDA;
     return launch_status();
 }
 
@@ -269,6 +282,7 @@ extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s
     g.T = T;
     g.nt = (f + T - 1) / T;
     g.status = dev_status;
+    g.pdl = 1;  // its prologue overlaps the tail of the kernel before it on the stream
     const GemmOperand Bu{Wu_s, f, d, d};
     st = launch_gemm<256, false, false, twell::Epi::GateUpF16, true>(GemmOperand{x, N, d, d},
                                                                      GemmOperand{Wg_s, f, d, d}, &Bu, g, s);
