@@ -685,7 +685,9 @@ def run_ours(a, rank, world):
                            "how": "copy in, the layer, copy out one after the other on one stream"}},
         # per step: gate + pack, then the walk's plan and the walk; or the union path's expand, up and
         # down GEMMs; or the tile-union path's union bits, prefix, work list, expand, up and down GEMMs
-        "gpu_launches": (2 if gate_union else {"walk": 3, "union": 4, "tile_union": 7}[a.path]) * a.steps,
+        # union path: gate + up GEMM and down GEMM, plus the split-K reduction for batches of up to 1024
+        "gpu_launches": ((3 if N <= 1024 else 2) if gate_union else {"walk": 3, "union": 4, "tile_union": 7}[a.path])
+                        * a.steps,
         "path": a.path,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
