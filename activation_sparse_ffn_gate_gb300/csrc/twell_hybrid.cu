@@ -20,7 +20,7 @@
 namespace twell {
 
 constexpr int kHybTile = 128;   // TwELL tile of the gate epilogue inside the hybrid path
-constexpr int kRouteRows = 128; // rows per routing block
+constexpr int kRouteRows = 32;  // rows per routing block (two per warp: short dependent-load chains)
 constexpr int kRowBatch = 8;    // nonzeros per batch in the light-row kernels
 constexpr int kMaxK = 65534;    // largest capacity K (counts are uint16, 0xFFFF marks a backup row)
 constexpr int kBackupSplits = 4; // K ranges of the backup rows' y and dx products (few rows, long K)
@@ -91,7 +91,7 @@ struct HybridWs {
 // ------------------------------------------------------------------------------------------
 // Routing
 
-constexpr int kRouteWarps = 16;                          // warps of a routing block (8 rows each)
+constexpr int kRouteWarps = 16;                          // warps of a routing block (two rows each)
 constexpr int kRouteMaxTiles = (65535 + kHybTile - 1) / kHybTile;  // d_ff <= 65535
 
 // Per row (one warp): nnz from the TwELL counts, scanned into per-tile offsets in shared memory;
@@ -1119,7 +1119,7 @@ extern "C" twell_status twell_gemm_test(const void* A, const void* B, int32_t M,
 
 namespace {
 
-constexpr int kNoAllocBlocks = 8192;  // 128-row blocks: at most 1,048,576 token rows per call
+constexpr int kNoAllocBlocks = 32768;  // 32-row blocks: at most 1,048,576 token rows per call
 static __device__ __align__(256) int32_t g_noalloc_blk_counts[kNoAllocBlocks];
 
 std::mutex g_noalloc_mu;

@@ -385,8 +385,8 @@ TWELL_API twell_status twell_gate_gemm(const void* x, const void* Wg_s, int32_t 
  * allocation would synchronise the device). ctx->u, ctx->U_b and ctx->l1 are not used and may be
  * null; cnt, n_backup, dev_status, and col and a (K > 0), backup_rows and A_b (backup_cap > 0)
  * are required.
- * Its only scratch, the overflow-row count of each 128-row block, is a fixed array of 8192 int32
- * inside the library: every GPU that loads the library keeps it (32 KB) until the process exits.
+ * Its only scratch, the overflow-row count of each 32-row block, is a fixed array of 32768 int32
+ * inside the library: every GPU that loads the library keeps it (128 KB) until the process exits.
  * Limit: a->n_rows <= 1,048,576; larger inputs return TWELL_ERR_UNSUPPORTED before any launch.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress), so make
  * that first call before any stream capture. All calls share the one array: two calls that
