@@ -214,7 +214,12 @@ __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_
         const int r = blockIdx.x * kRouteRows + rr;
         if (lane == 0) brows[slot] = r;
         float* arow = A_b + static_cast<size_t>(slot) * f;
-        for (int j = lane; j < f; j += 32) arow[j] = 0.0f;
+        if ((f & 3) == 0 && (reinterpret_cast<uintptr_t>(A_b) & 15) == 0) {  // rows 16-byte aligned
+            float4* a4 = reinterpret_cast<float4*>(arow);
+            for (int j = lane; j < f / 4; j += 32) a4[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else {
+            for (int j = lane; j < f; j += 32) arow[j] = 0.0f;
+        }
         __syncwarp();  // zeros before the kept values, across lanes
         for (int t = lane; t < nt; t += 32) {
             const int c = cnt[static_cast<size_t>(r) * nt + t];
