@@ -939,6 +939,9 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
     __syncwarp();
 
     const uint64_t pol_w = policy_evict_last(), pol_x = policy_evict_first();
+    // launched as a programmatic dependent of the plan kernel: its items, lists and counts (and the
+    // work counter cleared before it) are visible once that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     RowStream<E, 0, 1> rs;
     rs.init(a, nullptr, s_pref, nullptr, lane, 0, 0);
 
@@ -1130,6 +1133,9 @@ __global__ void __launch_bounds__(128) split_plan_kernel(const uint16_t* __restr
                                                          int* __restrict__ list,
                                                          SplitItem* __restrict__ items, HeavyRow* __restrict__ heavy)
 {
+    // the walk (launched as this grid's programmatic dependent) may be scheduled now; it waits for
+    // this grid to complete before it reads the plan
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r - lane >= N) return;  // whole warp past the end
@@ -1252,7 +1258,17 @@ static twell_status launch_bulk_k(const RowArgs<__nv_bfloat16>& a, cudaStream_t 
     const long long need = (work + WPC - 1) / WPC;
     int grid = di.sm_count * per_sm;
     if (grid > need) grid = static_cast<int>(need);
-    kern<<<grid, 32 * WPC, smem, s>>>(b);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * WPC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, b) != cudaSuccess) return TWELL_ERR_CUDA;
     return twell_host::launch_status();
 }
 
