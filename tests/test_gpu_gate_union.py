@@ -182,3 +182,20 @@ def test_gate_union_small_batches_split_down_gemm(cuda_dev, N):
     sel = torch.from_numpy(rows).to(cuda_dev)
     assert_close(y[sel].double().cpu().numpy(), y_ref, f"gate union split N={N}")
     assert_close(y2[sel].double().cpu().numpy(), y_ref, f"two-call union split N={N}")
+
+
+@pytest.mark.parametrize("N", [100, 1024, 1025])
+def test_union_split_boundary_and_partial_tiles(cuda_dev, N):
+    """The down GEMM splits K for at most 1024 tokens and not above; d_model 576 leaves a partial
+    256-column tile in every split, d_ff 1000 a partial K range. Both union entry points against the
+    oracle on every row (N = 100) or sampled rows."""
+    L = synthetic.uniform_layer(N, 576, 1000, 128, 0.03, seed=N + 3)
+    t = L.torch_inputs(cuda_dev)
+    Wd16t = binding.twell_convert_f16_transposed(t["Wd_s"])
+    y, tw = binding.twell_ffn_gate_union_fwd(t["x"], t["Wg_s"], t["Wu_s"], Wd16t, 128)
+    y2 = binding.twell_ffn_union_fwd(t["x"], t["Wu_s"], Wd16t, tw)
+    rows = np.arange(N) if N <= 128 else _sampled_rows(N, 40, seed=N)
+    y_ref = oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s, rows=rows)
+    sel = torch.from_numpy(rows).to(cuda_dev)
+    assert_close(y[sel].double().cpu().numpy(), y_ref, f"gate union d=576 N={N}")
+    assert_close(y2[sel].double().cpu().numpy(), y_ref, f"two-call union d=576 N={N}")
