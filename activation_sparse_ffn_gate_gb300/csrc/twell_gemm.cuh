@@ -72,6 +72,13 @@ struct GemmArgs {
     int a_box_rows;          // rows of A a stage loads (0: the whole 128-row tile); fewer when M is small,
                              // the tile's other rows then hold stale data whose products are never stored
     int64_t split_stride;    // elements between the partial outputs of consecutive splits
+    // StoreBF16 with PAIR, no split: the last tail_split tiles (the partial last wave) are cut into
+    // two K halves, each a unit that stores an fp32 partial at tail_part (per tail tile and half a
+    // [256 x BN] block, rows and columns relative to the tile); the caller adds the halves. A caller
+    // asks with tail_split = -max: launch_gemm splits the last wave when it fills at most half the
+    // clusters and has at most max tiles, and reports the count it chose (0: none).
+    int tail_split;
+    float* tail_part;
     void* out;               // epilogue output
     int64_t ldo;             // its leading dimension (elements)
     const int32_t* rowmap;   // ScatterBF16: destination row of each m
@@ -157,12 +164,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool leader = crank == 0;
     const int unit0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int ustride = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
-    const int units = kbs > 0 ? (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles * ks : 0;
-    // unit u: tile u / ks, k-block range u % ks
-    auto tile_m0 = [&](int u) { return (PAIR ? 2 * (u / ks / n_tiles) + crank : u / ks / n_tiles) * kBM; };
-    auto tile_n0 = [&](int u) { return (u / ks % n_tiles) * TN; };
-    auto kb_begin = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks) * kbs / ks); };
-    auto kb_end = [&](int u) { return static_cast<int>(static_cast<long long>(u % ks + 1) * kbs / ks); };
+    const int tiles = (PAIR ? (m_tiles + 1) / 2 : m_tiles) * n_tiles;
+    // tail split: the last ts tiles as two K halves each (units n_whole .. n_whole + 2 ts)
+    const int ts = (EPI == Epi::StoreBF16 && PAIR && ks == 1 && kbs >= 2) ? min(max(g.tail_split, 0), tiles) : 0;
+    const int n_whole = tiles - ts;
+    const int units = kbs > 0 ? (ts > 0 ? n_whole + 2 * ts : tiles * ks) : 0;
+    // unit u: tile u / ks, k-block range u % ks; past n_whole with a tail split: tile n_whole + (u - n_whole) / 2,
+    // K half (u - n_whole) % 2
+    auto tile_of = [&](int u) { return (ts == 0 || u < n_whole) ? u / ks : n_whole + ((u - n_whole) >> 1); };
+    auto half_of = [&](int u) { return (ts == 0 || u < n_whole) ? -1 : ((u - n_whole) & 1); };
+    auto tile_m0 = [&](int u) {
+        const int tl = tile_of(u);
+        return (PAIR ? 2 * (tl / n_tiles) + crank : tl / n_tiles) * kBM;
+    };
+    auto tile_n0 = [&](int u) { return (tile_of(u) % n_tiles) * TN; };
+    auto kb_begin = [&](int u) {
+        const int hh = half_of(u);
+        if (hh >= 0) return hh ? kbs / 2 : 0;
+        return static_cast<int>(static_cast<long long>(u % ks) * kbs / ks);
+    };
+    auto kb_end = [&](int u) {
+        const int hh = half_of(u);
+        if (hh >= 0) return hh ? kbs : kbs / 2;
+        return static_cast<int>(static_cast<long long>(u % ks + 1) * kbs / ks);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -404,12 +429,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (valid) g.cnt[static_cast<size_t>(row) * g.nt + tile] = static_cast<uint16_t>(c);
                 }
             } else {
+                const int thalf = half_of(t);
                 for (int ch = 0; ch < BN / 32; ++ch) {
                     float v[32];
                     tmem_ld_32x32b_x32(taddr + ch * 32, v);
                     const int col0 = n0 + ch * 32;
                     if (!row_ok || col0 >= g.N) continue;
                     const int nvalid = min(32, g.N - col0);
+                    if (EPI == Epi::StoreBF16 && thalf >= 0) {
+                        // a K half of a tail tile: fp32 partial, rows and columns relative to the tile
+                        const int lr = 32 * q + lane + (PAIR ? crank * kBM : 0);
+                        float* o = g.tail_part +
+                                   ((static_cast<size_t>(tile_of(t) - n_whole) * 2 + thalf) * (CG * kBM) + lr) * BN + ch * 32;
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4)
+                            if (k < nvalid) *reinterpret_cast<float4*>(o + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                        continue;
+                    }
                     if constexpr (EPI == Epi::StoreF32 || EPI == Epi::AccumF32 || EPI == Epi::ScatterF32) {
                         const int orow = (EPI == Epi::ScatterF32) ? g.rowmap[row] : row;
                         float* o = static_cast<float*>(g.out) + static_cast<size_t>(orow) * g.ldo + col0 +
@@ -557,7 +593,7 @@ struct GemmOperand {
 // k-block kb_split on. Returns TWELL_ERR_CUDA on a tensor-map or launch failure.
 template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR = false, bool F16 = false>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
-                         cudaStream_t stream);
+                         cudaStream_t stream, int* tail_chosen = nullptr);
 
 }  // namespace twell_host
 
@@ -565,8 +601,9 @@ namespace twell_host {
 
 template <int BN, bool A_MN, bool B_MN, twell::Epi EPI, bool PAIR, bool F16>
 twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmOperand* B2, twell::GemmArgs g,
-                         cudaStream_t stream)
+                         cudaStream_t stream, int* tail_chosen)
 {
+    if (tail_chosen != nullptr) *tail_chosen = 0;
     static_assert(!PAIR || (!A_MN && !B_MN), "the CTA-pair GEMM takes K-major operands");
     using Cfg = twell::GemmCfg<BN, PAIR>;
     constexpr bool DUAL = EPI == twell::Epi::GateUpF16;
@@ -642,7 +679,18 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         cfg.gridDim = dim3(2 * static_cast<unsigned>(di.sm_count / 2));
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return TWELL_ERR_CUDA;
-        const long long units = ((m_tiles + 1) / 2) * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
+        long long units = ((m_tiles + 1) / 2) * n_tiles * (g.k_splits > 1 ? g.k_splits : 1);
+        if (g.tail_split < 0) {
+            // split the last, partial wave of tiles into K halves when it fills at most half the pairs
+            const long long tail = units % clusters;
+            const int kbs = (g.K + twell::kBK - 1) / twell::kBK;
+            g.tail_split = (EPI == twell::Epi::StoreBF16 && g.k_splits <= 1 && g.tail_part != nullptr && kbs >= 2 &&
+                            units > clusters && tail > 0 && 2 * tail <= clusters && tail <= -g.tail_split)
+                               ? static_cast<int>(tail)
+                               : 0;
+            units += g.tail_split;
+            if (tail_chosen != nullptr) *tail_chosen = g.tail_split;
+        }
         if (clusters > units) clusters = static_cast<int>(units);
         cfg.gridDim = dim3(2 * static_cast<unsigned>(clusters));
         cfg.numAttrs = g.pdl ? 2 : 1;

@@ -81,6 +81,32 @@ __global__ void __launch_bounds__(256) expand_f16_mask_kernel(const Ein* __restr
 // 128-row tiles, i.e. ks * N <= 2048, and splitting only for N <= 1024.
 constexpr int kSplitMaxRows = 2048;
 constexpr int kSplitMaxN = 1024;
+// Above kSplitMaxN tokens: the down GEMM's last, partial wave of 256 x 256 tiles may be cut into K
+// halves (at most this many tiles; two fp32 [256 x 256] partials each)
+constexpr int kTailMax = 40;
+constexpr size_t kTailTileBytes = 2ull * 256 * 256 * 4;
+
+// y over the tail tiles = bf16(half 0 + half 1), four columns per thread. Launched as a programmatic
+// dependent of the down GEMM: it waits for that grid before reading.
+__global__ void __launch_bounds__(256) reduce_tail_bf16_kernel(const float* __restrict__ part, int ts, int full,
+                                                               int n_tiles, int M, int N,
+                                                               __nv_bfloat16* __restrict__ y)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<size_t>(ts) * 256 * 64) return;
+    const int tt = static_cast<int>(i / (256 * 64)), lr = static_cast<int>(i / 64 % 256), c4 = static_cast<int>(i % 64);
+    const int t = full + tt;
+    const int m = 2 * (t / n_tiles) * 128 + lr, n = (t % n_tiles) * 256 + 4 * c4;
+    if (m >= M || n >= N) return;
+    const float4 a = *reinterpret_cast<const float4*>(part + ((static_cast<size_t>(tt) * 2) * 256 + lr) * 256 + 4 * c4);
+    const float4 b = *reinterpret_cast<const float4*>(part + ((static_cast<size_t>(tt) * 2 + 1) * 256 + lr) * 256 + 4 * c4);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x + b.x, a.y + b.y), hi = __floats2bfloat162_rn(a.z + b.z, a.w + b.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + static_cast<size_t>(m) * N + n) = w;
+}
 
 // y[i] = bf16(part[0][i] + part[1][i] + ... + part[ks - 1][i]) for four elements per thread.
 // Launched as a programmatic dependent of the down GEMM: it waits for that grid before reading.
@@ -107,10 +133,11 @@ __global__ void __launch_bounds__(256) reduce_splits_bf16_kernel(const float* __
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// bytes of the split partials a call may need (0 above kSplitMaxN tokens)
+// bytes of the split partials a call may need: K ranges up to kSplitMaxN tokens, the tail tiles' K
+// halves above
 inline size_t split_bytes(int N, int d)
 {
-    return N <= kSplitMaxN ? up256(static_cast<size_t>(kSplitMaxRows) * d * 4) : 0;
+    return N <= kSplitMaxN ? up256(static_cast<size_t>(kSplitMaxRows) * d * 4) : up256(kTailMax * kTailTileBytes);
 }
 
 struct UnionWs {
@@ -174,7 +201,27 @@ twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int 
     const GemmOperand A{H, N, fp, fp}, B{Wd16t_s, d, f, f};
     if (ks <= 1) {
         g2.out = y;
-        return launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(A, B, nullptr, g2, s);
+        if (N > twell::kSplitMaxN) {  // the partial last wave in K halves, added by reduce_tail_bf16_kernel
+            g2.tail_split = -twell::kTailMax;
+            g2.tail_part = part;
+        }
+        int ts = 0;
+        twell_status st = launch_gemm<256, false, false, twell::Epi::StoreBF16, true, true>(A, B, nullptr, g2, s, &ts);
+        if (st != TWELL_OK || ts == 0) return st;
+        const int n_tiles = (d + 255) / 256, tiles = ((N + 255) / 256) * n_tiles;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>((static_cast<size_t>(ts) * 256 * 64 + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, twell::reduce_tail_bf16_kernel, static_cast<const float*>(part), ts, tiles - ts,
+                               n_tiles, N, d, static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
+            return TWELL_ERR_CUDA;
+        return launch_status();
     }
     g2.out = part;
     g2.k_splits = ks;
