@@ -1128,14 +1128,26 @@ __global__ void __launch_bounds__(32 * WPC, 1) ffn_bulk_kernel(const RowArgs<__n
 // get ceil(nnz / seg) consecutive items while the item list has room (one atomic per warp
 // reserves the warp's items); the other rows go to the list of their class (above kClassA
 // nonzeros, above kClassB, the rest). hdr[1..4] (zero at launch): items reserved, rows per class.
+// The walk's work counter and the plan's counts set to zero, as a programmatic dependent of the
+// kernel before it on the stream (normally the gate GEMM): it waits for that grid, then lets the plan
+// kernel be scheduled. One warp.
+__global__ void __launch_bounds__(32) zero_header_kernel(int* __restrict__ hdr, int n)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x < n) hdr[threadIdx.x] = 0;
+}
+
 __global__ void __launch_bounds__(128) split_plan_kernel(const uint16_t* __restrict__ cnt, int N, int nt, int T,
                                                          int seg, int item_cap, int* __restrict__ hdr,
                                                          int* __restrict__ list,
                                                          SplitItem* __restrict__ items, HeavyRow* __restrict__ heavy)
 {
     // the walk (launched as this grid's programmatic dependent) may be scheduled now; it waits for
-    // this grid to complete before it reads the plan
+    // this grid to complete before it reads the plan. This grid itself is the dependent of the
+    // header-zeroing kernel: the counts it reads and the counters it adds to are ready after the wait.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r - lane >= N) return;  // whole warp past the end
@@ -1239,8 +1251,19 @@ static twell_status launch_bulk_k(const RowArgs<__nv_bfloat16>& a, cudaStream_t 
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * WPC, smem) != cudaSuccess || per_sm < 1)
         return TWELL_ERR_CUDA;
-    // the work counter and the plan's counts start at zero; the plan splits the long rows
-    if (cudaMemsetAsync(a.tickets, 0, 5 * sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    // the work counter and the plan's counts start at zero (a dependent one-warp kernel rather than a
+    // memset, so that the gate, this, the plan and the walk chain as programmatic dependents); the
+    // plan splits the long rows
+    cudaLaunchConfig_t zc = {};
+    cudaLaunchAttribute zattr[1];
+    zattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    zattr[0].val.programmaticStreamSerializationAllowed = 1;
+    zc.gridDim = dim3(1);
+    zc.blockDim = dim3(32);
+    zc.stream = s;
+    zc.attrs = zattr;
+    zc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&zc, zero_header_kernel, a.tickets, 5) != cudaSuccess) return TWELL_ERR_CUDA;
     RowArgs<__nv_bfloat16> b = a;
     b.split = 1;
     // Items of up to 128 nonzeros; for a small batch the largest power of two with at least one item
@@ -1248,9 +1271,12 @@ static twell_status launch_bulk_k(const RowArgs<__nv_bfloat16>& a, cudaStream_t 
     int seg = kSplitSeg;
     const long long warps = static_cast<long long>(di.sm_count) * per_sm * WPC;
     while (seg > kSplitSegMin && seg * warps > 32ll * a.N) seg >>= 1;
-    split_plan_kernel<<<(a.N + 127) / 128, 128, 0, s>>>(a.cnt, a.N, a.nt, a.T, seg, a.item_cap, a.tickets,
-                                                        const_cast<int*>(a.list), const_cast<SplitItem*>(a.items),
-                                                        a.heavy);
+    cudaLaunchConfig_t pc = zc;
+    pc.gridDim = dim3((a.N + 127) / 128);
+    pc.blockDim = dim3(128);
+    if (cudaLaunchKernelEx(&pc, split_plan_kernel, a.cnt, a.N, a.nt, a.T, seg, a.item_cap, a.tickets,
+                           const_cast<int*>(a.list), const_cast<SplitItem*>(a.items), a.heavy) != cudaSuccess)
+        return TWELL_ERR_CUDA;
     if (twell_host::launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     // a warp per work item at most: the rows plus the items split rows can be cut into
     const long long most_items = static_cast<long long>(a.N) * ((a.f + seg - 1) / seg);
