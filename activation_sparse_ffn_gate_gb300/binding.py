@@ -493,19 +493,20 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
 # Density (kept fraction of d_ff per token) above which the union path beats the walk, measured with
 # the whole layer on the 1.5B-like shapes (d_model 2048, d_ff 5632, 8192 tokens, T = 128, L2 flushed; ms):
 #   density                               0.1%    0.5%    1%      2%      5%      10%     50%
-#   walk (gate + pack, then the walk)     0.188   0.326   0.469   0.789   1.727   3.349   15.31
-#   union (gate + up in one GEMM, down)   0.318   0.320   0.322   0.325   0.332   0.347   0.570
-#   tile union (gate, then gathered)      0.235   0.374   0.481   0.585   0.687   0.789   1.619
-#   dense cuBLAS FFN                      0.364   0.365   0.366   0.366   0.368   0.366   0.370
-# They cross near 0.5% at 8192 tokens. On the 1.5B-like layer (0.5% kept) the union path is also the
-# faster of the two for every batch of 32 to 4096 tokens (us; dense in brackets):
+#   walk (gate + pack, then the walk)     0.188   0.324   0.465   0.782   1.723   3.320   15.27
+#   union (gate + up in one GEMM, down)   0.309   0.313   0.313   0.317   0.321   0.340   0.571
+#   tile union (gate, then gathered)      0.236   0.378   0.481   0.586   0.688   0.790   1.623
+#   dense cuBLAS FFN                      0.365   0.366   0.367   0.366   0.366   0.366   0.369
+# The walk's time grows about linearly with the density, so the two cross near 0.45%. On the
+# 1.5B-like layer (0.5% kept) the union path is also the faster of the two for every batch of 32 to
+# 4096 tokens (us; dense in brackets):
 #   tokens      32     64     128    256    512    1024   2048    4096
-#   walk        41.0   45.2   55.7   63.9   72.3   92.3   125.9   188.5
-#   union       36.9   37.0   41.6   43.0   54.1   72.5   92.8    168.7
-#   dense      (32.8) (30.1) (32.5) (34.9) (49.1) (66.3) (109.7) (192.1)
-# so batches of up to 4096 tokens switch at a lower density. The gathered tile-union path is never
-# the fastest under these densities; it stays available as path "tile_union".
-UNION_MIN_DENSITY = 0.006
+#   walk        38.6   40.7   44.5   53.3   65.5   88.8   120.6   180.8
+#   union       32.7   32.9   35.5   38.6   51.2   65.4   89.7    167.1
+#   dense      (32.7) (28.8) (31.6) (34.8) (46.0) (66.2) (109.0) (189.4)
+# so batches of up to 4096 tokens switch a little lower. The gathered tile-union path is never the
+# fastest under these densities; it stays available as path "tile_union".
+UNION_MIN_DENSITY = 0.0045
 UNION_MIN_DENSITY_SMALL_BATCH = 0.004
 SMALL_BATCH_MAX_N = 4096
 

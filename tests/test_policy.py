@@ -11,7 +11,8 @@ def test_small_batches_take_the_decode_path():
 def test_density_chooses_walk_or_union():
     n = binding.SMALL_BATCH_MAX_N + 1
     assert binding.choose_path(n, None) == "walk"  # no estimate yet: the walk
-    assert binding.choose_path(8192, 0.005) == "walk"
+    assert binding.choose_path(8192, 0.004) == "walk"
+    assert binding.choose_path(8192, 0.005) == "union"
     assert binding.choose_path(8192, 0.01) == "union"
     assert binding.choose_path(n, binding.UNION_MIN_DENSITY) == "union"
     assert binding.choose_path(8192, 0.02) == "union"
