@@ -265,6 +265,15 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 }
 // Start bringing `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 (no completion
 // to wait for): a row needed a little later then comes from L2 instead of HBM.
+// First statement of a kernel launched as a programmatic dependent (launch_dep): the kernel after it
+// may be scheduled now, and this one waits until the kernel before it has completed and its writes
+// are visible. In a kernel launched without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
@@ -488,6 +497,25 @@ inline twell_status launch_status()
 {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+// Launch `kern` as a programmatic dependent of the kernel before it on `s`; the kernel must begin
+// with twell::pdl_begin() (its first statement), so that it reads and writes nothing before the
+// previous kernel has completed.
+template <typename... KArgs, typename... Args>
+twell_status launch_dep(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 }  // namespace twell_host
 

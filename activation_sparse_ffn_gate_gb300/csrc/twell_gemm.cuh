@@ -95,7 +95,8 @@ struct GemmArgs {
     int T, nt;
     // launched as a programmatic dependent of the previous kernel on the stream: the prologue
     // (barriers, TMEM, tensor-map prefetch) overlaps that kernel's last wave, and every thread
-    // waits for it to complete (griddepcontrol.wait) before any role starts (no M_dyn / K_dyn)
+    // waits for it to complete (griddepcontrol.wait) before any role starts; with M_dyn / K_dyn the
+    // wait comes first, before the extents are read
     int pdl;
     // status
     int32_t* status;
@@ -148,6 +149,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // this grid to complete before it reads anything this grid writes)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // an extent read from the device is written by an earlier kernel: wait for it first
+    if (g.pdl && (g.M_dyn != nullptr || g.K_dyn != nullptr)) asm volatile("griddepcontrol.wait;" ::: "memory");
     int M = g.M;
     if (g.M_dyn != nullptr) M = min(M, *g.M_dyn);
     int K = g.K;
@@ -640,7 +643,6 @@ twell_status launch_gemm(const GemmOperand& A, const GemmOperand& B, const GemmO
         cudaSuccess)
         return TWELL_ERR_CUDA;
     g.wait_limit_ns = wait_limit_ns();
-    if (g.pdl && (g.M_dyn != nullptr || g.K_dyn != nullptr)) return TWELL_ERR_UNSUPPORTED;
     const long long m_tiles = (g.M + twell::kBM - 1) / twell::kBM, n_tiles = (g.N + TN - 1) / TN;
     if (g.k_splits > 1 && EPI != twell::Epi::StoreF32) return TWELL_ERR_UNSUPPORTED;
     if constexpr (!PAIR) {

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_rows_kernel(
     int nt, int K, float* __restrict__ ha, uint16_t* __restrict__ hcol, uint16_t* __restrict__ hcnt,
     int* __restrict__ blk, double* l1acc, int32_t* status)
 {
+    pdl_begin();
     __shared__ int s_pref[kRouteWarps][kRouteMaxTiles + 1];
     __shared__ int s_heavy;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -171,6 +172,7 @@ __global__ void route_backup_kernel(const float* __restrict__ vals, const uint8_
                                     int32_t* __restrict__ n_backup, float* __restrict__ A_b,
                                     __nv_bfloat16* __restrict__ x_b, int32_t* status)
 {
+    pdl_begin();
     __shared__ int s_off, s_total, s_rank[kRouteRows];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     if (tid < 32) {
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(512) hybrid_light_fwd_kernel(const __nv_bfloat
                                                                __nv_bfloat16* __restrict__ y, double* l1acc,
                                                                int32_t* status)
 {
+    pdl_begin();
     __shared__ float s_red[16][kRowBatch];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int q = tid, nchunks = d / 8;
@@ -365,6 +368,7 @@ __global__ void __launch_bounds__(512) hybrid_light_bwd_kernel(const __nv_bfloat
                                                                float* __restrict__ ent, float* __restrict__ dx,
                                                                int32_t* status)
 {
+    pdl_begin();
     __shared__ float s_red[16][kRowBatch];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int q = tid, nchunks = d / 8;
@@ -447,12 +451,14 @@ __global__ void __launch_bounds__(512) hybrid_light_bwd_kernel(const __nv_bfloat
 
 __global__ void fill_i32_kernel(int* p, int n, int v)
 {
+    pdl_begin();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
 }
 
 __global__ void col_hist_kernel(const uint16_t* __restrict__ hcol, const uint16_t* __restrict__ hcnt, int N, int K,
                                 int f, int* __restrict__ ccount)
 {
+    pdl_begin();
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < static_cast<long long>(N) * K;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int r = static_cast<int>(e / K), k = static_cast<int>(e % K);
@@ -466,6 +472,7 @@ __global__ void col_hist_kernel(const uint16_t* __restrict__ hcol, const uint16_
 // Exclusive scan of the f column counts (one CTA): coff[0..f], and a copy into the cursors.
 __global__ void col_scan_kernel(const int* __restrict__ ccount, int f, int* __restrict__ coff, int* __restrict__ ccur)
 {
+    pdl_begin();
     __shared__ int s_w[32];
     __shared__ int s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -507,6 +514,7 @@ struct EntRec {
 __global__ void col_scatter_kernel(const uint16_t* __restrict__ hcol, const uint16_t* __restrict__ hcnt, int N, int K,
                                    int f, const float* __restrict__ ent, int* __restrict__ ccur, EntRec* __restrict__ rec)
 {
+    pdl_begin();
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < static_cast<long long>(N) * K;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int r = static_cast<int>(e / K), k = static_cast<int>(e % K);
@@ -527,6 +535,7 @@ constexpr int kDwSmemRecs = 512;
 // below run in a fixed order whatever order the scatter's atomics produced.
 __global__ void col_sort_kernel(const int* __restrict__ coff, int f, EntRec* __restrict__ rec)
 {
+    pdl_begin();
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < f; j += gridDim.x * blockDim.x) {
         const int s = coff[j], e = coff[j + 1];
         if (e - s <= kDwSmemRecs) continue;
@@ -555,6 +564,7 @@ __global__ void __launch_bounds__(512) col_dw_kernel(const int* __restrict__ cof
                                                      int f, int d, const __nv_bfloat16* __restrict__ v,
                                                      float* __restrict__ dWa, float* __restrict__ dWb)
 {
+    pdl_begin();
     __shared__ EntRec s_in[kDwSmemRecs], s_out[kDwSmemRecs];
     const int q = threadIdx.x, nchunks = d / 8;
     const uint64_t pol = policy_evict_last();
@@ -633,6 +643,7 @@ __global__ void backup_h_kernel(const float* __restrict__ A_b, const float* __re
                                 const int32_t* __restrict__ n_backup, int cap, int f, int f_pad,
                                 __nv_bfloat16* __restrict__ H, double* l1acc)
 {
+    pdl_begin();
     const int nb = min(*n_backup, cap);
     float l1 = 0.0f;
     const long long total = static_cast<long long>(nb) * f_pad;
@@ -662,6 +673,7 @@ __global__ void reduce_rows_kernel(const float* __restrict__ part, int splits, l
                                    const int32_t* __restrict__ n_dyn, int cap, int d, const int32_t* __restrict__ rowmap,
                                    O* __restrict__ out)
 {
+    pdl_begin();
     const int nb = min(*n_dyn, cap);
     const int q4 = d / 4;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < static_cast<long long>(nb) * q4;
@@ -689,6 +701,7 @@ __global__ void reduce_rows_kernel(const float* __restrict__ part, int splits, l
 
 __global__ void l1_finalize_kernel(const double* l1acc, float scale, float* l1)
 {
+    pdl_begin();
     *l1 = static_cast<float>(*l1acc * static_cast<double>(scale));
 }
 
@@ -697,6 +710,7 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ src, const 
                                    const int32_t* __restrict__ n_backup, int cap, int d,
                                    __nv_bfloat16* __restrict__ out)
 {
+    pdl_begin();
     const int nb = min(*n_backup, cap);
     const int pad_end = min((nb + 63) / 64 * 64, (cap + 63) / 64 * 64);
     const int nq = d / 8;
@@ -720,6 +734,7 @@ __global__ void backup_grad_kernel(const float* __restrict__ A_b, const float* _
                                    int f_pad, float l1_scale, const int32_t* __restrict__ brows, int* __restrict__ ccur,
                                    EntRec* __restrict__ rec, __nv_bfloat16* __restrict__ DUG)
 {
+    pdl_begin();
     const int nb = min(*n_backup, cap);
     const int rows = min((nb + 63) / 64 * 64, (cap + 63) / 64 * 64);
     const long long total = static_cast<long long>(rows) * f_pad;
@@ -752,6 +767,7 @@ __global__ void backup_grad_kernel(const float* __restrict__ A_b, const float* _
 __global__ void col_hist_backup_kernel(const float* __restrict__ A_b, const int32_t* __restrict__ n_backup, int cap,
                                        int f, int* __restrict__ ccount)
 {
+    pdl_begin();
     const int nb = min(*n_backup, cap);
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < static_cast<long long>(nb) * f;
          e += static_cast<long long>(gridDim.x) * blockDim.x)
@@ -820,12 +836,12 @@ twell_status run_route(const twell::HybridWs& L, uint8_t* ws, int N, int f, int 
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(ws + L.tw_cnt);
     int* blk = reinterpret_cast<int*>(ws + L.blk);
     double* l1acc = reinterpret_cast<double*>(ws + L.l1acc);
-    twell::route_rows_kernel<<<L.nblk, 32 * twell::kRouteWarps, 0, s>>>(
-        vals, idx, cnt, N, f, L.nt, K, static_cast<float*>(c->a), c->col, c->cnt, blk, l1acc, c->dev_status);
+    if (launch_dep(twell::route_rows_kernel, dim3(L.nblk), dim3(32 * twell::kRouteWarps), 0, s,
+        vals, idx, cnt, N, f, L.nt, K, static_cast<float*>(c->a), c->col, c->cnt, blk, l1acc, c->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    twell::route_backup_kernel<<<L.nblk, 256, 0, s>>>(vals, idx, cnt, c->cnt, blk, L.nblk, N, f, L.nt, c->backup_cap, x,
+    if (launch_dep(twell::route_backup_kernel, dim3(L.nblk), dim3(256), 0, s, vals, idx, cnt, c->cnt, blk, L.nblk, N, f, L.nt, c->backup_cap, x,
                                                       d, c->backup_rows, c->n_backup, static_cast<float*>(c->A_b),
-                                                      reinterpret_cast<bf*>(ws + L.x_b), c->dev_status);
+                                                      reinterpret_cast<bf*>(ws + L.x_b), c->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
     return launch_status();
 }
 
@@ -906,10 +922,10 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
                         static_cast<float*>(ctx->u), y, l1acc, reinterpret_cast<int*>(w + L.tick), ctx->dev_status, s);
     if (st == TWELL_ERR_UNSUPPORTED) {
         const int threads = (d / 8 + 31) / 32 * 32;
-        twell::hybrid_light_fwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
+        if (launch_dep(twell::hybrid_light_fwd_kernel, dim3(grid_for(N, 1, di.sm_count * 4)), dim3(threads), 0, s,
             static_cast<const bf*>(x), static_cast<const bf*>(Wu_s), static_cast<const bf*>(Wd_s), N, d, f, K,
             static_cast<const float*>(ctx->a), ctx->col, ctx->cnt, static_cast<float*>(ctx->u), static_cast<bf*>(y),
-            l1acc, ctx->dev_status);
+            l1acc, ctx->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
         st = launch_status();
     }
     if (st != TWELL_OK) return st;
@@ -918,6 +934,7 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
         bf* x_b = reinterpret_cast<bf*>(w + L.x_b);
         bf* H_b = reinterpret_cast<bf*>(w + L.h_b);
         twell::GemmArgs g{};
+        g.pdl = 1;  // prologue overlaps the previous kernel's tail
         g.M = cap;
         g.N = f;
         g.K = d;
@@ -928,14 +945,15 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
         st = launch_gemm<256, false, false, twell::Epi::StoreF32>(GemmOperand{x_b, (int64_t)L.capr, d, d},
                                                                   GemmOperand{Wu_s, f, d, d}, nullptr, g, s);
         if (st != TWELL_OK) return st;
-        twell::backup_h_kernel<<<grid_for(static_cast<long long>(cap) * L.f_pad, 256, di.sm_count * 8), 256, 0, s>>>(
+        if (launch_dep(twell::backup_h_kernel, dim3(grid_for(static_cast<long long>(cap) * L.f_pad, 256, di.sm_count * 8)), dim3(256), 0, s,
             static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), ctx->n_backup, cap, f, L.f_pad,
-            H_b, l1acc);
+            H_b, l1acc) != TWELL_OK) return TWELL_ERR_CUDA;
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
         // y[rows] = [h_hi | h_lo] [Wd_s ; Wd_s]: kBackupSplits K ranges into fp32 partials, added
         // up in order into the bf16 rows
         float* y_part = reinterpret_cast<float*>(w + L.y_part);
         twell::GemmArgs g2{};
+        g2.pdl = 1;  // prologue overlaps the previous kernel's tail
         g2.M = cap;
         g2.N = d;
         g2.K = 2 * L.f_pad;
@@ -950,15 +968,15 @@ extern "C" twell_status twell_hybrid_fwd(const void* x, const void* Wg_s, const 
         st = launch_gemm<256, false, true, twell::Epi::StoreF32>(
             GemmOperand{H_b, (int64_t)L.capr, 2 * L.f_pad, 2 * L.f_pad}, Bd, &Bd, g2, s);
         if (st != TWELL_OK) return st;
-        twell::reduce_rows_kernel<bf><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
+        if (launch_dep(twell::reduce_rows_kernel<bf>, dim3(grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8)), dim3(256), 0, s,
             y_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows,
-            static_cast<bf*>(y));
+            static_cast<bf*>(y)) != TWELL_OK) return TWELL_ERR_CUDA;
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     }
     // 7. L1 term
-    twell::l1_finalize_kernel<<<1, 1, 0, s>>>(l1acc, static_cast<float>(static_cast<double>(l1_coef) /
+    if (launch_dep(twell::l1_finalize_kernel, dim3(1), dim3(1), 0, s, l1acc, static_cast<float>(static_cast<double>(l1_coef) /
                                                                          (static_cast<double>(N) * f)),
-                                              ctx->l1);
+                                              ctx->l1) != TWELL_OK) return TWELL_ERR_CUDA;
     return launch_status();
 }
 
@@ -1003,10 +1021,10 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
                             static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx,
                             reinterpret_cast<int*>(w + L.btick), ctx->dev_status, s);
         if (st == TWELL_ERR_UNSUPPORTED) {
-            twell::hybrid_light_bwd_kernel<<<grid_for(N, 1, di.sm_count * 4), threads, 0, s>>>(
+            if (launch_dep(twell::hybrid_light_bwd_kernel, dim3(grid_for(N, 1, di.sm_count * 4)), dim3(threads), 0, s,
                 static_cast<const bf*>(dy), static_cast<const bf*>(Wg_s), static_cast<const bf*>(Wu_s),
                 static_cast<const bf*>(Wd_s), N, d, f, K, static_cast<const float*>(ctx->a),
-                static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx, ctx->dev_status);
+                static_cast<const float*>(ctx->u), ctx->col, ctx->cnt, l1_scale, ent, dx, ctx->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
             st = launch_status();
         }
         if (st != TWELL_OK) return st;
@@ -1015,16 +1033,16 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
     //    their dense a), per hidden unit, for the weight gradients
     const long long ne = static_cast<long long>(N) * K;
     const bool backup = cap > 0 && N > 0;
-    twell::fill_i32_kernel<<<grid_for(f, 256, 256), 256, 0, s>>>(ccount, f, 0);
+    if (launch_dep(twell::fill_i32_kernel, dim3(grid_for(f, 256, 256)), dim3(256), 0, s, ccount, f, 0) != TWELL_OK) return TWELL_ERR_CUDA;
     if (ne > 0)
-        twell::col_hist_kernel<<<grid_for(ne, 256, di.sm_count * 8), 256, 0, s>>>(ctx->col, ctx->cnt, N, K, f, ccount);
+        if (launch_dep(twell::col_hist_kernel, dim3(grid_for(ne, 256, di.sm_count * 8)), dim3(256), 0, s, ctx->col, ctx->cnt, N, K, f, ccount) != TWELL_OK) return TWELL_ERR_CUDA;
     if (backup)
-        twell::col_hist_backup_kernel<<<grid_for(static_cast<long long>(cap) * f, 256, di.sm_count * 8), 256, 0, s>>>(
-            static_cast<const float*>(ctx->A_b), ctx->n_backup, cap, f, ccount);
-    twell::col_scan_kernel<<<1, 1024, 0, s>>>(ccount, f, coff, ccur);
+        if (launch_dep(twell::col_hist_backup_kernel, dim3(grid_for(static_cast<long long>(cap) * f, 256, di.sm_count * 8)), dim3(256), 0, s,
+            static_cast<const float*>(ctx->A_b), ctx->n_backup, cap, f, ccount) != TWELL_OK) return TWELL_ERR_CUDA;
+    if (launch_dep(twell::col_scan_kernel, dim3(1), dim3(1024), 0, s, ccount, f, coff, ccur) != TWELL_OK) return TWELL_ERR_CUDA;
     if (ne > 0)
-        twell::col_scatter_kernel<<<grid_for(ne, 256, di.sm_count * 8), 256, 0, s>>>(ctx->col, ctx->cnt, N, K, f, ent,
-                                                                                     ccur, rec);
+        if (launch_dep(twell::col_scatter_kernel, dim3(grid_for(ne, 256, di.sm_count * 8)), dim3(256), 0, s, ctx->col, ctx->cnt, N, K, f, ent,
+                                                                                     ccur, rec) != TWELL_OK) return TWELL_ERR_CUDA;
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
 
     // 3. backup rows: dH_b = dy_b Wd_s^T (tcgen05), then du, dg (and their column records)
@@ -1033,10 +1051,11 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
     bf* DUG = reinterpret_cast<bf*>(w + L.dug);
     if (backup) {
         const unsigned gg = grid_for(static_cast<long long>(L.capr) * d / 8, 256, di.sm_count * 8);
-        twell::gather_rows_kernel<<<gg, 256, 0, s>>>(static_cast<const bf*>(dy), ctx->backup_rows, ctx->n_backup, cap,
-                                                     d, dy_b);
+        if (launch_dep(twell::gather_rows_kernel, dim3(gg), dim3(256), 0, s, static_cast<const bf*>(dy), ctx->backup_rows, ctx->n_backup, cap,
+                                                     d, dy_b) != TWELL_OK) return TWELL_ERR_CUDA;
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
         twell::GemmArgs g{};
+        g.pdl = 1;  // prologue overlaps the previous kernel's tail
         g.M = cap;
         g.N = f;
         g.K = d;
@@ -1047,18 +1066,17 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
         st = launch_gemm<256, false, false, twell::Epi::StoreF32>(GemmOperand{dy_b, (int64_t)L.capr, d, d},
                                                                   GemmOperand{Wd_s, f, d, d}, nullptr, g, s);
         if (st != TWELL_OK) return st;
-        twell::backup_grad_kernel<<<grid_for(static_cast<long long>(L.capr) * L.f_pad, 256, di.sm_count * 8), 256, 0,
-                                    s>>>(static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), dH,
-                                         ctx->n_backup, cap, f, L.f_pad, l1_scale, ctx->backup_rows, ccur, rec, DUG);
+        if (launch_dep(twell::backup_grad_kernel, dim3(grid_for(static_cast<long long>(L.capr) * L.f_pad, 256, di.sm_count * 8)), dim3(256), 0, s, static_cast<const float*>(ctx->A_b), static_cast<const float*>(ctx->U_b), dH,
+                                         ctx->n_backup, cap, f, L.f_pad, l1_scale, ctx->backup_rows, ccur, rec, DUG) != TWELL_OK) return TWELL_ERR_CUDA;
         if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     }
 
     // 4. weight gradients of every kept entry, per hidden unit, in row order (overwrites dW)
-    twell::col_sort_kernel<<<grid_for(f, 128, di.sm_count * 4), 128, 0, s>>>(coff, f, rec);
-    twell::col_dw_kernel<0><<<f, threads, 0, s>>>(
-        coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s);
-    twell::col_dw_kernel<1><<<f, threads, 0, s>>>(
-        coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr);
+    if (launch_dep(twell::col_sort_kernel, dim3(grid_for(f, 128, di.sm_count * 4)), dim3(128), 0, s, coff, f, rec) != TWELL_OK) return TWELL_ERR_CUDA;
+    if (launch_dep(twell::col_dw_kernel<0>, dim3(f), dim3(threads), 0, s,
+        coff, rec, f, d, static_cast<const bf*>(x), dWg_s, dWu_s) != TWELL_OK) return TWELL_ERR_CUDA;
+    if (launch_dep(twell::col_dw_kernel<1>, dim3(f), dim3(threads), 0, s,
+        coff, rec, f, d, static_cast<const bf*>(dy), dWd_s, nullptr) != TWELL_OK) return TWELL_ERR_CUDA;
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
     if (!backup) return TWELL_OK;
 
@@ -1066,6 +1084,7 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
     //    kBackupSplits K ranges added up in order
     float* dx_part = reinterpret_cast<float*>(w + L.dx_part);
     twell::GemmArgs g{};
+    g.pdl = 1;  // prologue overlaps the previous kernel's tail
     g.M = cap;
     g.N = d;
     g.K = 4 * L.f_pad;
@@ -1080,8 +1099,8 @@ extern "C" twell_status twell_hybrid_bwd(const void* x, const void* Wg_s, const 
     st = launch_gemm<256, false, true, twell::Epi::StoreF32>(GemmOperand{DUG, (int64_t)L.capr, 4 * L.f_pad, 4 * L.f_pad},
                                                              GemmOperand{Wu_s, f, d, d}, &B2, g, s);
     if (st != TWELL_OK) return st;
-    twell::reduce_rows_kernel<float><<<grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8), 256, 0, s>>>(
-        dx_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows, dx);
+    if (launch_dep(twell::reduce_rows_kernel<float>, dim3(grid_for(static_cast<long long>(cap) * d / 4, 256, di.sm_count * 8)), dim3(256), 0, s,
+        dx_part, twell::kBackupSplits, static_cast<long long>(L.capr) * d, ctx->n_backup, cap, d, ctx->backup_rows, dx) != TWELL_OK) return TWELL_ERR_CUDA;
     return launch_status();
 }
 
@@ -1166,13 +1185,13 @@ extern "C" twell_status twell_hybrid_route_noalloc(const twell_packed* a, int32_
     if (st != TWELL_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int nt = (f + twell::kHybTile - 1) / twell::kHybTile;
-    twell::route_rows_kernel<<<nblk, 32 * twell::kRouteWarps, 0, s>>>(
+    if (launch_dep(twell::route_rows_kernel, dim3(nblk), dim3(32 * twell::kRouteWarps), 0, s,
         static_cast<const float*>(a->vals), a->idx, a->cnt, N, f, nt, K, static_cast<float*>(ctx->a), ctx->col, ctx->cnt,
-        blk, nullptr, ctx->dev_status);
+        blk, nullptr, ctx->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
     if (launch_status() != TWELL_OK) return TWELL_ERR_CUDA;
-    twell::route_backup_kernel<<<nblk, 256, 0, s>>>(static_cast<const float*>(a->vals), a->idx, a->cnt, ctx->cnt, blk,
+    if (launch_dep(twell::route_backup_kernel, dim3(nblk), dim3(256), 0, s, static_cast<const float*>(a->vals), a->idx, a->cnt, ctx->cnt, blk,
                                                     nblk, N, f, nt, ctx->backup_cap, nullptr, 8, ctx->backup_rows,
                                                     ctx->n_backup, static_cast<float*>(ctx->A_b), nullptr,
-                                                    ctx->dev_status);
+                                                    ctx->dev_status) != TWELL_OK) return TWELL_ERR_CUDA;
     return launch_status();
 }

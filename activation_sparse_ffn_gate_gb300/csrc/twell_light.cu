@@ -237,6 +237,14 @@ struct RowOps {
     }
 };
 
+// The work-ticket counter is reset by a dependent one-thread kernel (not a memset), so that the
+// reset and the walk can both be launched early behind the producing kernel.
+__global__ void zero_ticket_kernel(int* tickets)
+{
+    pdl_begin();
+    *tickets = 0;
+}
+
 // NS: 256-column spans of d_model; S: ring slots per warp; WPC: warps per CTA; BWD: backward.
 template <int NS, int S, int WPC, bool BWD>
 __global__ void __launch_bounds__(32 * WPC, 1) light_kernel(const LightArgs a)
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(32 * WPC, 1) light_kernel(const LightArgs a)
         fence_mbar_init();
     }
     __syncwarp();
+    pdl_begin();  // the barriers above touch shared memory only
 
     const uint64_t pol_w = policy_evict_last(), pol_v = policy_evict_first();
     const __nv_bfloat16* Wr[3] = {a.W0, a.W1, a.W2};
@@ -375,11 +384,11 @@ twell_status launch_light(const LightArgs& a, cudaStream_t s)
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * WPC, smem) != cudaSuccess || per_sm < 1)
         return TWELL_ERR_CUDA;
-    if (cudaMemsetAsync(a.tickets, 0, sizeof(int), s) != cudaSuccess) return TWELL_ERR_CUDA;
+    if (twell_host::launch_dep(zero_ticket_kernel, dim3(1), dim3(1), 0, s, a.tickets) != TWELL_OK) return TWELL_ERR_CUDA;
     const int need = (a.N + WPC - 1) / WPC;
     int grid = di.sm_count * per_sm;
     if (grid > need) grid = need;
-    kern<<<grid, 32 * WPC, smem, s>>>(a);
+    if (twell_host::launch_dep(kern, dim3(grid), dim3(32 * WPC), smem, s, a) != TWELL_OK) return TWELL_ERR_CUDA;
     return twell_host::launch_status();
 }
 
