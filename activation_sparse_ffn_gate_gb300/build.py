@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtwell_gb300.so")
 
 SOURCES = ["twell_host.cu", "twell_gate.cu", "twell_ffn.cu", "twell_pack.cu", "twell_hybrid.cu", "twell_light.cu",
-           "twell_union.cu", "twell_decode.cu", "twell_tile_union.cu"]
+           "twell_union.cu", "twell_union_small.cu", "twell_decode.cu", "twell_tile_union.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
               "-I" + INCLUDE, "-I" + CSRC]

@@ -109,10 +109,11 @@ constexpr int kBK = 64;
 
 template <int BN, bool PAIR = false>
 struct GemmCfg {
-    static constexpr int STAGES = (BN == 256 && !PAIR) ? 4 : (PAIR ? 7 : 6);
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;
     static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;  // this CTA's share of B
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    // one CTA: as many stages as fit in 192 KB (4 at BN = 256, 6 at 128, 8 at 64, 9 at 32)
+    static constexpr int STAGES = PAIR ? 7 : (196608 / STAGE_BYTES < 10 ? static_cast<int>(196608 / STAGE_BYTES) : 10);
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 };
