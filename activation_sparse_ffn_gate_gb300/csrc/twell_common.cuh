@@ -480,13 +480,12 @@ size_t union_ws_bytes(int N, int d, int f);
 size_t gate_union_ws_bytes(int N, int d, int f);
 // The union path for batches of at most kSmallMaxN tokens, weights on the M side of the products
 // (twell_union_small.cu): gate + up with the TwELL pack and h = a * u into H [N, ldo] (fp16), and
-// the down product y = H Wd16t_s^T split along K into at most kSmallMaxSplits fp32 partials
-// ([ks][d][NP] at `part`, NP = N rounded up to 32, 64 or 128) added in order.
+// the down product y = H Wd16t_s^T (f_pad = fp, a multiple of 64) split along K over a cluster,
+// whose fp32 partials are added in a fixed order in distributed shared memory.
 constexpr int kSmallMaxN = 128;
-constexpr int kSmallMaxSplits = 16;
 twell_status gate_up_small(const void* x, const void* Wg_s, const void* Wu_s, int N, int d, int f, int T,
                            const twell_packed* out, __half* H, int ldo, int32_t* dev_status, cudaStream_t s);
-twell_status down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
+twell_status down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
                         int32_t* dev_status, cudaStream_t s);
 // Bytes of the workspace twell_ffn_tile_union_fwd needs (twell_tile_union.cu).
 size_t tile_union_ws_bytes(int N, int f);

@@ -190,7 +190,7 @@ int union_down_splits(int N, int d, int fp)
 twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
                         int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= kSmallMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
+    if (N <= kSmallMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     const int ks = union_down_splits(N, d, fp);
     twell::GemmArgs g2{};
     g2.M = N;
@@ -321,7 +321,7 @@ extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s
     if (N <= kSmallMaxN) {  // weights on the M side of both products
         st = gate_up_small(x, Wg_s, Wu_s, N, d, f, T, out, H, fp, dev_status, s);
         if (st != TWELL_OK) return st;
-        return down_small(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
+        return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     }
     // 1 + 2. g and u of each 128-unit block in one tile: TwELL of ReLU(g), h = a * u into H
     twell::GemmArgs g{};

@@ -12,15 +12,18 @@
 //      accumulates [g; u]^T of the 64 units for all tokens into TMEM. The epilogue moves g and u
 //      to shared memory as [unit][token]; one thread per token and 32-unit half counts, then
 //      packs its units exactly as twell_gate_pack packs (ReLU, ascending unit order), storing
-//      h = a * u (fp16; a = the packed value, 0 where g <= 0). The two CTAs of a cluster hold the two halves of a 128-unit block: with T = 128
-//      the second CTA's entries follow the first's, whose per-token counts it reads from the
-//      first CTA's shared memory (distributed shared memory). With T = 64 each CTA is a tile.
-//   2. the down product y^T = Wd16t_s H^T on the generic tcgen05 GEMM (A = Wd16t_s [d, f] fp16,
-//      B = H [N, f_pad] fp16, both K-major, a 128 x NP tile), split along K into ks ranges so that
-//      ceil(d / 128) * ks work units fill the SMs; fp32 partials [ks][d][NP];
-//   3. reduce_splits_t_bf16_kernel adds the partials in range order (a fixed order) and writes
-//      y [N, d] in bf16 through a 32 x 32 shared-memory transpose.
-// All three launch as programmatic dependents of the kernel before them on the stream.
+//      h = a * u (fp16; a = the packed value, 0 where g <= 0). The two CTAs of a cluster hold the
+//      two halves of a 128-unit block: with T = 128 the second CTA's entries follow the first's,
+//      whose per-token counts it reads from the first CTA's shared memory (distributed shared
+//      memory). With T = 64 each CTA is a tile.
+//      The K loop streams the CTA's 512 KB of Wg_s and Wu_s rows (d_model 2048) through a ring of
+//      6-9 stages; at 64 tokens it runs at ~57 GB/s per SM (88 SMs: ~5 TB/s of HBM).
+//   At 256 tokens this orientation was slower than the SM-pair tiles (45 against 40 us on the
+//   1.5B-like layer: the N = 256 MMAs and 1 MB of x per CTA from L2), so it stops at 128.
+//   2. down_small_kernel: y^T = Wd16t_s H^T, one 128-row block of Wd16t_s (128 columns of y) per
+//      cluster of up to 8 CTAs, each a K range of f_pad; the fp32 partials meet in the cluster's
+//      shared memory and are added in rank order (a fixed order) into bf16 y.
+// Both launch as programmatic dependents of the kernel before them on the stream.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -288,34 +291,207 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-// y[t, j] = bf16(part[0][j][t] + ... + part[ks - 1][j][t]) (ks <= kMaxSplits) through a 32 x 32
-// transpose in shared memory; every thread issues its ks loads before it adds them in order.
-// Block (32, 32); grid (ceil(N / 32), ceil(d / 32)).
-constexpr int kMaxSplits = 16;
-__global__ void __launch_bounds__(1024) reduce_splits_t_bf16_kernel(const float* __restrict__ part, int ks,
-                                                                    size_t split_stride, int ldp, int N, int d,
-                                                                    __nv_bfloat16* __restrict__ y)
+// Down product of the small-batch path: y^T = Wd16t_s H^T for one 128-row block of Wd16t_s (128
+// output columns of y) per cluster of ks CTAs, CTA r taking the r-th of ks near-equal K ranges of
+// f_pad (fp16 operands, A = Wd16t_s rows K-major, B = H [NP, 64] per k-block, one tcgen05.mma of
+// M = 128, N = NP per 16 of K). Its fp32 partial goes from TMEM to shared memory as [token][row];
+// after a cluster barrier CTA r adds, for its ~128 / ks rows, the ks partials in rank order (a
+// fixed order) from the cluster's shared memory, 16 bytes at a time, and writes those columns of y
+// in bf16.
+struct DownArgs {
+    int N, d, fp, ks;
+    __nv_bfloat16* y;
+    int32_t* status;
+    uint64_t wait_limit_ns;
+};
+
+constexpr int kDownMaxCluster = 8;
+
+template <int NP>
+struct DownCfg {
+    static constexpr uint32_t A_BYTES = 128 * kBK * 2;
+    static constexpr uint32_t B_BYTES = NP * kBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = kSmallRing / STAGE_BYTES < 10 ? static_cast<int>(kSmallRing / STAGE_BYTES) : 10;
+    static constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256;
+    static_assert(128u * NP * 4 <= STAGES * STAGE_BYTES, "the partial fits in the ring it replaces");
+};
+
+template <int NP>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    down_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                      const DownArgs a)
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    __shared__ float tile[32][33];
-    const int t0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    {
-        const int j = j0 + ty, t = t0 + tx;
-        const bool ok = j < d && t < N;
-        const float* p = part + static_cast<size_t>(ok ? j : 0) * ldp + (ok ? t : 0);
-        float v[kMaxSplits];
-#pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) v[s] = (ok && s < ks) ? p[static_cast<size_t>(s) * split_stride] : 0.0f;
-        float acc = v[0];
-#pragma unroll
-        for (int s = 1; s < kMaxSplits; ++s)
-            if (s < ks) acc += v[s];
-        tile[ty][tx] = acc;
+    using C = DownCfg<NP>;
+    constexpr int STAGES = C::STAGES;
+    constexpr uint32_t IDESC = idesc_f16_f32(128, NP, false, false);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* drain = tfull + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* P = reinterpret_cast<float*>(smem);  // after the main loop: the partial [token][128 rows]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+    const int ks = a.ks;
+    const int r = static_cast<int>(cluster.block_rank());
+    const int m0 = static_cast<int>(blockIdx.x) / ks * 128;
+    const int kbs = a.fp / kBK;
+    const int kb0 = kbs * r / ks, kb1 = kbs * (r + 1) / ks;  // non-empty: ks <= kbs
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
     }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmH);
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(tmem_slot, NP);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before();
     __syncthreads();
-    const int t = t0 + ty, j = j0 + tx;
-    if (t < N && j < d) y[static_cast<size_t>(t) * d + j] = __float2bfloat16_rn(tile[tx][ty]);
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // H is the previous grid's output
+
+    bool have_acc = false;
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_limit_ns)) break;
+                uint8_t* sa = smem + stage * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                tma_load_2d(sa, &tmW, kb * kBK, m0, &full[stage]);
+                tma_load_2d(sa + C::A_BYTES, &tmH, kb * kBK, 0, &full[stage]);
+                issued_mask |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded(&full[s], (issued_phase >> s) & 1u, nullptr, a.status, a.wait_limit_ns);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bounded(&full[stage], phase, abort_flag, a.status, a.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
+                const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                    tc_mma_f16<1>(tmem_base, desc_sw128(a_addr + k * 32, 16), desc_sw128(b_addr + k * 32, 16), IDESC,
+                                  (kb != kb0 || k != 0) ? 1u : 0u);
+                tc_commit<1>(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) tc_commit<1>(tfull);
+            tc_commit<1>(drain);
+            wait_bounded(drain, 0, nullptr, a.status, a.wait_limit_ns);
+        }
+    } else {
+        const int q = warp & 3;
+        int ok = 1;
+        if (lane == 0) ok = wait_bounded(tfull, 0, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+            tc_fence_after();
+            float* dst = P + 32 * q + lane;
+#pragma unroll 1
+            for (int ch = 0; ch < NP / 32; ++ch) {
+                float v[32];
+                tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + ch * 32, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dst[(ch * 32 + k) * 128] = v[k];
+            }
+            have_acc = true;
+        }
+    }
+    tc_fence_before();
+    int have = __syncthreads_or(have_acc ? 1 : 0) && !*abort_flag;
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc<1>(tmem_base, NP);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // every partial is in place
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const float* part[kDownMaxCluster];
+#pragma unroll
+    for (int i = 0; i < kDownMaxCluster; ++i) {
+        part[i] = cluster.map_shared_rank(P, i < ks ? i : 0);
+        if (i < ks) have = have && !*cluster.map_shared_rank(const_cast<int*>(abort_flag), i);
+    }
+    if (have) {
+        // rows [j0, j1) of the block (multiples of 4), four at a time: element e = token e / n4, rows
+        // j0 + 4 (e % n4) .. + 3; consecutive threads read 16 consecutive bytes of each partial
+        const int j0 = 128 * r / ks / 4 * 4, j1 = r + 1 == ks ? 128 : 128 * (r + 1) / ks / 4 * 4;
+        const int n4 = (j1 - j0) / 4, total = n4 * a.N;
+        for (int e0 = threadIdx.x; e0 < total; e0 += 2 * kSmallThreads) {
+            float4 v[2][kDownMaxCluster];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int e = min(e0 + b * kSmallThreads, total - 1);
+                const int off = (e / n4) * 128 + j0 + 4 * (e % n4);
+#pragma unroll
+                for (int i = 0; i < kDownMaxCluster; ++i)
+                    v[b][i] = i < ks ? *reinterpret_cast<const float4*>(part[i] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int e = e0 + b * kSmallThreads;
+                if (e >= total) break;
+                float4 acc = v[b][0];
+#pragma unroll
+                for (int i = 1; i < kDownMaxCluster; ++i)
+                    if (i < ks) {
+                        acc.x += v[b][i].x;
+                        acc.y += v[b][i].y;
+                        acc.z += v[b][i].z;
+                        acc.w += v[b][i].w;
+                    }
+                const int col = m0 + j0 + 4 * (e % n4);
+                __nv_bfloat16* o = a.y + static_cast<size_t>(e / n4) * a.d + col;
+                if (col + 3 < a.d) {  // d is a multiple of 8: y rows are 16-byte aligned, col a multiple of 4
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                    uint2 w;
+                    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(o) = w;
+                } else {
+                    const float av[4] = {acc.x, acc.y, acc.z, acc.w};
+                    for (int k = 0; k < 4 && col + k < a.d; ++k) o[k] = __float2bfloat16_rn(av[k]);
+                }
+            }
+        }
+    }
+    // the partials stay in place until every CTA of the cluster has read them (relaxed: this
+    // barrier orders no memory, so no thread waits here for its stores to drain)
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 template <int NP>
@@ -348,42 +524,59 @@ twell_status launch_gate_up_small(const void* x, const void* Wg_s, const void* W
     return twell_host::launch_status();
 }
 
-// K ranges of the transposed down product: ceil(d / 128) * ks units fill the SMs at most once,
-// each range four k-blocks or more, ks <= kSmallMaxSplits.
-int small_down_splits(int d, int fp)
-{
-    twell_host::DevInfo di;
-    if (twell_host::dev_info(&di) != TWELL_OK) return 1;
-    const int m_tiles = (d + kBM - 1) / kBM;
-    int ks = std::max(di.sm_count / m_tiles, 1);
-    ks = std::min(ks, std::min(twell_host::kSmallMaxSplits, kMaxSplits));
-    ks = std::min(ks, std::max(fp / kBK / 4, 1));
-    return ks;
-}
-
 template <int NP>
-twell_status launch_down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
+twell_status launch_down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
                                int32_t* dev_status, cudaStream_t s)
 {
-    const int ks = small_down_splits(d, fp);
-    GemmArgs g{};
-    g.M = d;
-    g.N = N;
-    g.K = fp;
-    g.k_splits = ks;
-    g.split_stride = static_cast<int64_t>(d) * NP;
-    g.out = part;
-    g.ldo = NP;
-    g.status = dev_status;
-    g.pdl = 1;
-    const twell_host::GemmOperand A{Wd16t_s, d, f, f}, B{H, N, fp, fp};
-    twell_status st = twell_host::launch_gemm<NP, false, false, Epi::StoreF32, false, true>(A, B, nullptr, g, s);
+    using C = DownCfg<NP>;
+    twell_host::DevInfo di;
+    if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
+    const int m_tiles = (d + 127) / 128;
+    auto kern = down_small_kernel<NP>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES)) !=
+        cudaSuccess)
+        return TWELL_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // K ranges per 128-row block: the largest cluster (up to 8) of which m_tiles fit on the GPU at
+    // once (clusters are placed within one GPC: fewer of 8 fit than SMs / 8); counts cached per size
+    static int fit[kDownMaxCluster + 1][3] = {};
+    const int slot = NP == 32 ? 0 : (NP == 64 ? 1 : 2);
+    int ks = 1;
+    for (int c = std::min(kDownMaxCluster, fp / kBK); c > 1; --c) {
+        if (fit[c][slot] == 0) {
+            attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+            cfg.gridDim = dim3(static_cast<unsigned>(c * m_tiles));
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return TWELL_ERR_CUDA;
+            fit[c][slot] = n > 0 ? n : -1;
+        }
+        if (fit[c][slot] >= m_tiles) {
+            ks = c;
+            break;
+        }
+    }
+    CUtensorMap tw, th;
+    twell_status st = twell_host::make_tmap_bf16(&tw, Wd16t_s, f, d, f, 64, 128);
     if (st != TWELL_OK) return st;
-    return twell_host::launch_dep(reduce_splits_t_bf16_kernel, dim3((N + 31) / 32, (d + 31) / 32), dim3(32, 32), 0, s,
-                                  static_cast<const float*>(part), ks, static_cast<size_t>(d) * NP, NP, N, d,
-                                  static_cast<__nv_bfloat16*>(y)) == TWELL_OK
-               ? twell_host::launch_status()
-               : TWELL_ERR_CUDA;
+    st = twell_host::make_tmap_bf16(&th, H, fp, N, fp, 64, NP);
+    if (st != TWELL_OK) return st;
+    DownArgs a{N, d, fp, ks, static_cast<__nv_bfloat16*>(y), dev_status, twell_host::wait_limit_ns()};
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+    cfg.gridDim = dim3(static_cast<unsigned>(m_tiles * ks));
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, tw, th, a) != cudaSuccess) return TWELL_ERR_CUDA;
+    return twell_host::launch_status();
 }
 
 }  // namespace
@@ -414,10 +607,10 @@ twell_status twell_host::gate_up_small(const void* x, const void* Wg_s, const vo
 }
 
 twell_status twell_host::down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
-                                    float* part, int32_t* dev_status, cudaStream_t s)
+                                    int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= 0 || N > kSmallMaxN) return TWELL_ERR_UNSUPPORTED;
-    if (N <= 32) return twell::launch_down_small<32>(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
-    if (N <= 64) return twell::launch_down_small<64>(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
-    return twell::launch_down_small<128>(H, Wd16t_s, N, d, f, fp, y, part, dev_status, s);
+    if (N <= 0 || N > kSmallMaxN || fp % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+    if (N <= 32) return twell::launch_down_small<32>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    if (N <= 64) return twell::launch_down_small<64>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    return twell::launch_down_small<128>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
 }
