@@ -88,7 +88,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     int* base_s = cnt_s + NP;                                     // second CTA: the same, copied
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int u0 = blockIdx.x * kSmallUnits;
     const int kbs = (a.d + kBK - 1) / kBK;
 
@@ -116,6 +115,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // x and the weights are the previous grids' to write
+    // only now may the down kernel start: it reads Wd16t_s before its own wait, so every kernel
+    // before this call must have completed by then
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     bool have_acc = false;
     if (warp == 0) {
@@ -354,9 +356,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    // The first stages' Wd16t_s tiles are requested before the wait for the previous grid: no
+    // kernel that can still be running writes Wd16t_s (the kernel before this one on the stream
+    // lets it start only after its own wait, or started after all earlier work had completed).
+    const int npre = min(kb1 - kb0, STAGES);
+    if (threadIdx.x == 0) {  // the thread that initialised the barriers
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmH);
+        for (int i = 0; i < npre; ++i) {
+            mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+            tma_load_2d(smem + i * C::STAGE_BYTES, &tmW, (kb0 + i) * kBK, m0, &full[i]);
+        }
     }
     if (warp == 1) {
         tmem_alloc<1>(tmem_slot, NP);
@@ -373,10 +383,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_limit_ns)) break;
                 uint8_t* sa = smem + stage * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                tma_load_2d(sa, &tmW, kb * kBK, m0, &full[stage]);
+                if (kb - kb0 >= npre) {  // (the first npre stages are free and hold their A tile already)
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_limit_ns)) break;
+                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                    tma_load_2d(sa, &tmW, kb * kBK, m0, &full[stage]);
+                }
                 tma_load_2d(sa + C::A_BYTES, &tmH, kb * kBK, 0, &full[stage]);
                 issued_mask |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);

@@ -8,6 +8,10 @@ the TwELL packed and h = a * u formed in its epilogue, then the fp16 down GEMM) 
   batches, the sweep shapes (sampled rows) and the full-size 1.5B-like / 2B-like layers
   (sampled rows plus the densest rows);
 - batches of at most 1024 tokens, whose down GEMM splits K into fp32 partials added in order;
+- batches of at most 128 tokens, on the kernels with the weights on the MMA's M side (N = 32 / 64 /
+  128 token columns, a cluster pair per 128-unit tile, the down product's K split over a cluster):
+  every N up to and across those widths, T = 64 / 128, d_model not a multiple of 128, d_ff whose
+  last 128-unit block is mostly past d_ff, every unit kept, no unit kept, the same bits twice;
 - edge cases: zero density (y == 0, no entries), every unit kept, N = 1 / 7, an empty batch,
   T = 256 refused, the same bits on a second call.
 """
@@ -199,3 +203,55 @@ def test_union_split_boundary_and_partial_tiles(cuda_dev, N):
     sel = torch.from_numpy(rows).to(cuda_dev)
     assert_close(y[sel].double().cpu().numpy(), y_ref, f"gate union d=576 N={N}")
     assert_close(y2[sel].double().cpu().numpy(), y_ref, f"two-call union d=576 N={N}")
+
+
+def _int_layer(N, d, f, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.integers(-1, 2, (N, d)).astype(np.float32)
+    x[:, 0] = 1.0
+    Wg = rng.integers(-1, 2, (f, d)).astype(np.float32)
+    Wg[:, 0] = rng.integers(-6, 2, f)
+    Wu = synthetic.round_bf16_np((rng.standard_normal((f, d)) / np.sqrt(d)).astype(np.float32))
+    Wd = synthetic.round_bf16_np((rng.standard_normal((f, d)) / np.sqrt(f)).astype(np.float32))
+    return x, Wg, Wu, Wd
+
+
+@pytest.mark.parametrize("T", [64, 128])
+@pytest.mark.parametrize("N,d,f", [(1, 512, 1000), (31, 136, 1032), (32, 512, 1000), (33, 576, 1032),
+                                   (64, 136, 704), (65, 512, 1000), (100, 576, 1032), (127, 256, 1024),
+                                   (128, 512, 1280)])
+def test_gate_union_small_batch_kernels(cuda_dev, T, N, d, f):
+    """Batches of at most 128 tokens (the transposed gate + up and down kernels): on integer x and
+    Wg_s the TwELL is the oracle's bit for bit (fp32 values) and twell_gate_pack's; y matches the
+    oracle's walk of that TwELL on every row, repeats bit for bit, and the bf16-value TwELL matches
+    the oracle's rounded values."""
+    x, Wg, Wu, Wd = _int_layer(N, d, f, seed=N * 7 + f + T)
+    t = {"x": _to(cuda_dev, x), "Wg_s": _to(cuda_dev, Wg), "Wu_s": _to(cuda_dev, Wu), "Wd_s": _to(cuda_dev, Wd)}
+    G = oracle.gate(x, Wg)
+    vals, idx, cnt = oracle.twell_pack(G, T)
+    assert cnt.sum() > 0
+    for vdt in (torch.float32, torch.bfloat16):
+        y, tw = _run(cuda_dev, t, T, vdt)
+        exact = vals if vdt == torch.float32 else oracle.round_bf16(vals)
+        _compare_packed(tw, vals, idx, cnt, exact)
+        ref_tw = binding.twell_gate_pack(t["x"], t["Wg_s"], T, vals_dtype=vdt)
+        assert torch.equal(tw.cnt, ref_tw.cnt)
+        assert torch.equal(binding.twell_unpack(tw), binding.twell_unpack(ref_tw))
+        y_ref = oracle.twell_walk(exact, idx, cnt, T, x.astype(np.float64), Wu.astype(np.float64),
+                                  Wd.astype(np.float64))
+        assert_close(y.double().cpu().numpy(), y_ref, f"gate union small N={N} d={d} f={f} T={T} {vdt}")
+        y2, tw2 = _run(cuda_dev, t, T, vdt)
+        assert torch.equal(y, y2) and torch.equal(tw.cnt, tw2.cnt)
+
+
+@pytest.mark.parametrize("N", [40, 128])
+def test_gate_union_small_batch_all_and_none_kept(cuda_dev, N):
+    """Every unit kept (each T-tile count T, h everywhere) and no unit kept (y exactly 0)."""
+    L = synthetic.uniform_layer(N, 512, 1000, 128, 0.5, seed=N)
+    L.Wg_s[:, 0] = 1e4
+    y, tw = _run(cuda_dev, L.torch_inputs(cuda_dev), 128)
+    assert int(tw.counts().sum().item()) == N * 1000
+    assert_close(y.double().cpu().numpy(), oracle.ffn(L.x, L.Wg_s, L.Wu_s, L.Wd_s), f"small all kept N={N}")
+    L.Wg_s[:, 0] = -1e4
+    y, tw = _run(cuda_dev, L.torch_inputs(cuda_dev), 128)
+    assert int(tw.counts().sum().item()) == 0 and torch.count_nonzero(y).item() == 0
