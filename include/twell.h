@@ -232,7 +232,9 @@ TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const v
  * (tcgen05 GEMM on SM pairs, the product formed in its epilogue where the mask is set, h stored in
  * place as fp16: 11 significant bits); y = H Wd16_s (tcgen05 GEMM on SM pairs over f_pad, fp16
  * operands, bf16 y). Wd16t_s is the transpose of Wd_s converted once to fp16 ([d, f]:
- * twell_convert_f16_transposed), so that the down GEMM reads both operands K-major.
+ * twell_convert_f16_transposed), so that the down GEMM reads both operands K-major. For N <= 128
+ * the down product runs transposed (y^T = Wd16t_s H^T, rows of Wd16t_s on the MMA's M side, K split
+ * over a cluster of CTAs whose fp32 partials are added in a fixed order in shared memory).
  * bf16 x, Wu_s, y; d and f multiples of 8; x [N, d], Wu_s [f, d], Wd16t_s [d, f], y [N, d], device,
  * 16-byte aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (H and the
  * masks, 2.125 * N * f_pad bytes), required when N > 0. A corrupt TwELL entry (count above the tile
@@ -250,6 +252,9 @@ TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, cons
  * packs ReLU(g) into *out -- the TwELL twell_gate_pack writes, bit for bit ([AIM] ¶3, [TC] §2:
  * the pack in the gate GEMM's epilogue) -- and stores h = a * u (a = the packed value; fp16, 11
  * significant bits; 0 where g <= 0) into the workspace; then y = H Wd16_s as in twell_ffn_union_fwd.
+ * For N <= 128 both products run transposed, the weights on the MMA's M side and the tokens as its
+ * N columns: each CTA stacks 64 units' Wg_s rows over their Wu_s rows, and two CTAs form one
+ * 128-unit tile whose TwELL is the same, bit for bit.
  * For layers whose density the walk no longer serves: the union of the units a tile of 128 tokens
  * keeps is then most of d_ff ([TC] §3: tensor cores for the heavy work).
  * bf16 x, Wg_s, Wu_s, y (dtype must be TWELL_BF16); d and f multiples of 8; T = 64 or 128 (else
