@@ -478,11 +478,12 @@ size_t fused_ws_bytes(int N, int d, int f);
 // Bytes of the workspace twell_ffn_union_fwd needs (twell_union.cu).
 size_t union_ws_bytes(int N, int d, int f);
 size_t gate_union_ws_bytes(int N, int d, int f);
-// The union path for batches of at most kSmallMaxN tokens, weights on the M side of the products
+// The union path for batches of at most kTransposedMaxN tokens, weights on the M side of the products
 // (twell_union_small.cu): gate + up with the TwELL pack and h = a * u into H [N, ldo] (fp16), and
 // the down product y = H Wd16t_s^T (f_pad = fp, a multiple of 64) split along K over a cluster,
 // whose fp32 partials are added in a fixed order in distributed shared memory.
-constexpr int kSmallMaxN = 128;
+// With Wu_s == nullptr gate_up_small packs the TwELL only (the walk path's gate; H unused).
+constexpr int kTransposedMaxN = 128;
 twell_status gate_up_small(const void* x, const void* Wg_s, const void* Wu_s, int N, int d, int f, int T,
                            const twell_packed* out, __half* H, int ldo, int32_t* dev_status, cudaStream_t s);
 twell_status down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,

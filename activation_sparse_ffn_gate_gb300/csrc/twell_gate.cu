@@ -139,6 +139,10 @@ extern "C" twell_status twell_gate_pack(const void* x, const void* Wg_s, int32_t
     g.status = dev_status;
     GemmOperand A{x, N, d, d};
     GemmOperand B{Wg_s, f, d, d};
+    // Up to 128 tokens: the transposed kernel (64 units' Wg_s rows per CTA on the MMA's M side, the
+    // tokens as its N columns, two CTAs per 128-unit tile): 88 CTAs stream Wg_s at d_ff 5632.
+    if (N <= kTransposedMaxN && (T == 64 || T == 128))
+        return gate_up_small(x, Wg_s, nullptr, N, d, f, T, out, nullptr, 0, dev_status, s);
     // A small batch (decoding a few tokens) fills one or two 128-row tiles: 128 x T tiles on single
     // SMs spread d_ff over more SMs and pad M to 128 rows instead of 256 (the 256 x 256 pair tiles
     // left the decode gate tensor-bound on padding rows, 44 SMs busy at N = 8).

@@ -190,7 +190,7 @@ int union_down_splits(int N, int d, int fp)
 twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
                         int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= kSmallMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    if (N <= kTransposedMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     const int ks = union_down_splits(N, d, fp);
     twell::GemmArgs g2{};
     g2.M = N;
@@ -318,7 +318,7 @@ extern "C" twell_status twell_ffn_gate_union_fwd(const void* x, const void* Wg_s
     const int fp = (f + 63) / 64 * 64;
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                            twell::up256(static_cast<size_t>(N) * fp * 2));
-    if (N <= kSmallMaxN) {  // weights on the M side of both products
+    if (N <= kTransposedMaxN) {  // weights on the M side of both products
         st = gate_up_small(x, Wg_s, Wu_s, N, d, f, T, out, H, fp, dev_status, s);
         if (st != TWELL_OK) return st;
         return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);

@@ -61,7 +61,10 @@ struct SmallArgs {
     uint64_t wait_limit_ns;
 };
 
-template <int NP>
+// GATE_ONLY (the walk path's gate): the A tile's first 64 rows are the units' Wg_s rows and the
+// rest is not loaded (its products, in TMEM lanes 64-127, are never read); the epilogue packs the
+// TwELL only.
+template <int NP, bool GATE_ONLY>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     gate_up_small_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmU,
                          const __grid_constant__ CUtensorMap tmX, const SmallArgs a)
@@ -69,6 +72,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     using C = SmallCfg<NP>;
     constexpr int STAGES = C::STAGES;
     constexpr uint32_t IDESC = idesc_bf16_f32(128, NP, false, false);
+    constexpr uint32_t LOAD_BYTES = GATE_ONLY ? C::A_BYTES / 2 + C::B_BYTES : C::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
@@ -128,9 +132,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
                 if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.status, a.wait_limit_ns)) break;
                 uint8_t* sa = smem + stage * C::STAGE_BYTES;
                 const int k0 = kb * kBK;
-                mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                mbar_arrive_expect_tx(&full[stage], LOAD_BYTES);
                 tma_load_2d(sa, &tmG, k0, u0, &full[stage]);
-                tma_load_2d(sa + 8192, &tmU, k0, u0, &full[stage]);
+                if constexpr (!GATE_ONLY) tma_load_2d(sa + 8192, &tmU, k0, u0, &full[stage]);
                 tma_load_2d(sa + C::A_BYTES, &tmX, k0, 0, &full[stage]);
                 issued_mask |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -178,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
         int ok = 1;
         if (lane == 0) ok = wait_bounded(tfull, 0, abort_flag, a.status, a.wait_limit_ns) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
+        if (ok && !(GATE_ONLY && q >= 2)) {
             tc_fence_after();
             const int row = 32 * q + lane;
             float* dst = (row < kSmallUnits ? gs : us) + (row % kSmallUnits) * GP;
@@ -237,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 gr[j] = gs[(32 * hf + j) * GP + t];
-                ur[j] = us[(32 * hf + j) * GP + t];
+                ur[j] = GATE_ONLY ? 0.0f : us[(32 * hf + j) * GP + t];
             }
             int c = 0;
 #pragma unroll
@@ -264,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
                     const __half2 hh = __floats2half2_rn(hv[0], hv[1]);
                     hw[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
                 }
-                if (uh + j0 < a.ldo)  // ldo is a multiple of 64: the half is whole
+                if (!GATE_ONLY && uh + j0 < a.ldo)  // ldo is a multiple of 64: the half is whole
                     *reinterpret_cast<uint4*>(a.H + static_cast<size_t>(t) * a.ldo + uh + j0) =
                         make_uint4(hw[0], hw[1], hw[2], hw[3]);
             }
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-template <int NP>
+template <int NP, bool GATE_ONLY>
 twell_status launch_gate_up_small(const void* x, const void* Wg_s, const void* Wu_s, const SmallArgs& a,
                                   cudaStream_t s)
 {
@@ -514,11 +518,12 @@ twell_status launch_gate_up_small(const void* x, const void* Wg_s, const void* W
     CUtensorMap tg, tu, tx;
     twell_status st = twell_host::make_tmap_bf16(&tg, Wg_s, a.d, a.f, a.d, 64, kSmallUnits);
     if (st != TWELL_OK) return st;
-    st = twell_host::make_tmap_bf16(&tu, Wu_s, a.d, a.f, a.d, 64, kSmallUnits);
+    tu = tg;
+    if (!GATE_ONLY) st = twell_host::make_tmap_bf16(&tu, Wu_s, a.d, a.f, a.d, 64, kSmallUnits);
     if (st != TWELL_OK) return st;
     st = twell_host::make_tmap_bf16(&tx, x, a.d, a.N, a.d, 64, NP);
     if (st != TWELL_OK) return st;
-    auto kern = gate_up_small_kernel<NP>;
+    auto kern = gate_up_small_kernel<NP, GATE_ONLY>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES)) !=
         cudaSuccess)
         return TWELL_ERR_CUDA;
@@ -598,7 +603,7 @@ twell_status twell_host::gate_up_small(const void* x, const void* Wg_s, const vo
                                        const twell_packed* out, __half* H, int ldo, int32_t* dev_status,
                                        cudaStream_t s)
 {
-    if (N <= 0 || N > kSmallMaxN || (T != 64 && T != 128)) return TWELL_ERR_UNSUPPORTED;
+    if (N <= 0 || N > kTransposedMaxN || (T != 64 && T != 128)) return TWELL_ERR_UNSUPPORTED;
     twell::SmallArgs a{};
     a.N = N;
     a.d = d;
@@ -613,15 +618,20 @@ twell_status twell_host::gate_up_small(const void* x, const void* Wg_s, const vo
     a.H = H;
     a.status = dev_status;
     a.wait_limit_ns = wait_limit_ns();
-    if (N <= 32) return twell::launch_gate_up_small<32>(x, Wg_s, Wu_s, a, s);
-    if (N <= 64) return twell::launch_gate_up_small<64>(x, Wg_s, Wu_s, a, s);
-    return twell::launch_gate_up_small<128>(x, Wg_s, Wu_s, a, s);
+    if (Wu_s == nullptr) {
+        if (N <= 32) return twell::launch_gate_up_small<32, true>(x, Wg_s, Wu_s, a, s);
+        if (N <= 64) return twell::launch_gate_up_small<64, true>(x, Wg_s, Wu_s, a, s);
+        return twell::launch_gate_up_small<128, true>(x, Wg_s, Wu_s, a, s);
+    }
+    if (N <= 32) return twell::launch_gate_up_small<32, false>(x, Wg_s, Wu_s, a, s);
+    if (N <= 64) return twell::launch_gate_up_small<64, false>(x, Wg_s, Wu_s, a, s);
+    return twell::launch_gate_up_small<128, false>(x, Wg_s, Wu_s, a, s);
 }
 
 twell_status twell_host::down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
                                     int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= 0 || N > kSmallMaxN || fp % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+    if (N <= 0 || N > kTransposedMaxN || fp % 64 != 0) return TWELL_ERR_UNSUPPORTED;
     if (N <= 32) return twell::launch_down_small<32>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     if (N <= 64) return twell::launch_down_small<64>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     return twell::launch_down_small<128>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
