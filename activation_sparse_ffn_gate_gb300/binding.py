@@ -499,25 +499,32 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
 #   dense cuBLAS FFN                      0.365   0.366   0.367   0.366   0.366   0.366   0.369
 # The walk's time grows about linearly with the density, so the two cross near 0.45%. On the
 # 1.5B-like layer (0.5% kept) the union path is also the faster of the two for every batch of 32 to
-# 4096 tokens (us; dense in brackets):
+# 4096 tokens (us; dense in brackets; up to 128 tokens the union path's products run transposed):
 #   tokens      32     64     128    256    512    1024   2048    4096
-#   walk        38.6   40.7   44.5   53.3   65.5   88.8   120.6   180.8
-#   union       32.7   32.9   35.5   38.6   51.2   65.4   89.7    167.1
-#   dense      (32.7) (28.8) (31.6) (34.8) (46.0) (66.2) (109.0) (189.4)
-# so batches of up to 4096 tokens switch a little lower. The gathered tile-union path is never the
-# fastest under these densities; it stays available as path "tile_union".
+#   walk        38.2   40.7   50.3   61.0   67.3   89.9   122.6   184.8
+#   union       28.5   28.6   32.7   40.0   51.4   66.2   90.6    165.6
+#   dense      (33.1) (30.7) (32.7) (35.0) (48.8) (66.9) (110.9) (190.3)
+# so batches of up to 4096 tokens switch a little lower, and batches of up to UNION_ANY_DENSITY_MAX_N
+# tokens take the union path at every density: uniform layers of those shapes at 0.1% / 0.25% kept,
+#   64 tokens:  walk 30.8 / 33.0, union 26.8 / 27.3, dense 27.0 / 27.5
+#   128 tokens: walk 33.1 / 36.7, union 31.1 / 30.8, dense 29.9 / 29.4
+# The gathered tile-union path is never the fastest under these densities; it stays available as path
+# "tile_union".
 UNION_MIN_DENSITY = 0.0045
 UNION_MIN_DENSITY_SMALL_BATCH = 0.004
 SMALL_BATCH_MAX_N = 4096
+UNION_ANY_DENSITY_MAX_N = 128
 
 
 def choose_path(n_tokens: int, density: Optional[float]) -> str:
-    """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the walk below
-    UNION_MIN_DENSITY (UNION_MIN_DENSITY_SMALL_BATCH up to SMALL_BATCH_MAX_N tokens) or without a
-    density estimate; the union path (gate and up projection in one GEMM, down GEMM over all of
-    d_ff) above it."""
+    """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the union path
+    up to UNION_ANY_DENSITY_MAX_N tokens; above that the walk below UNION_MIN_DENSITY
+    (UNION_MIN_DENSITY_SMALL_BATCH up to SMALL_BATCH_MAX_N tokens) or without a density estimate,
+    the union path (gate and up projection in one GEMM, down GEMM over all of d_ff) above it."""
     if n_tokens <= DECODE_MAX_N:
         return "decode"
+    if n_tokens <= UNION_ANY_DENSITY_MAX_N:
+        return "union"
     limit = UNION_MIN_DENSITY_SMALL_BATCH if n_tokens <= SMALL_BATCH_MAX_N else UNION_MIN_DENSITY
     if density is None or density < limit:
         return "walk"

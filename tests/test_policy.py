@@ -19,8 +19,14 @@ def test_density_chooses_walk_or_union():
     assert binding.choose_path(8192, 0.5) == "union"
 
 
+def test_batches_up_to_128_tokens_take_the_union_path_at_any_density():
+    for n in (binding.DECODE_MAX_N + 1, 64, binding.UNION_ANY_DENSITY_MAX_N):
+        for d in (None, 0.0, 0.001, 0.005, 0.5):
+            assert binding.choose_path(n, d) == "union"
+
+
 def test_batches_up_to_4096_tokens_switch_at_a_lower_density():
-    for n in (binding.DECODE_MAX_N + 1, 64, 512, binding.SMALL_BATCH_MAX_N):
+    for n in (binding.UNION_ANY_DENSITY_MAX_N + 1, 512, binding.SMALL_BATCH_MAX_N):
         assert binding.choose_path(n, None) == "walk"
         assert binding.choose_path(n, 0.001) == "walk"
         assert binding.choose_path(n, 0.005) == "union"
