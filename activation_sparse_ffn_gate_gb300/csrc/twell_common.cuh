@@ -484,6 +484,7 @@ size_t gate_union_ws_bytes(int N, int d, int f);
 // whose fp32 partials are added in a fixed order in distributed shared memory.
 // With Wu_s == nullptr gate_up_small packs the TwELL only (the walk path's gate; H unused).
 constexpr int kTransposedMaxN = 128;
+constexpr int kDownSmallMaxN = 512;  // down_small serves this many tokens, in 128-token tiles above 128
 twell_status gate_up_small(const void* x, const void* Wg_s, const void* Wu_s, int N, int d, int f, int T,
                            const twell_packed* out, __half* H, int ldo, int32_t* dev_status, cudaStream_t s);
 twell_status down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,

@@ -190,7 +190,7 @@ int union_down_splits(int N, int d, int fp)
 twell_status union_down(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y, float* part,
                         int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= kTransposedMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    if (N <= kDownSmallMaxN) return down_small(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     const int ks = union_down_splits(N, d, fp);
     twell::GemmArgs g2{};
     g2.M = N;

@@ -20,9 +20,11 @@
 //      6-9 stages; at 64 tokens it runs at ~57 GB/s per SM (88 SMs: ~5 TB/s of HBM).
 //   At 256 tokens this orientation was slower than the SM-pair tiles (45 against 40 us on the
 //   1.5B-like layer: the N = 256 MMAs and 1 MB of x per CTA from L2), so it stops at 128.
-//   2. down_small_kernel: y^T = Wd16t_s H^T, one 128-row block of Wd16t_s (128 columns of y) per
-//      cluster of up to 8 CTAs, each a K range of f_pad; the fp32 partials meet in the cluster's
-//      shared memory and are added in rank order (a fixed order) into bf16 y.
+//   2. down_small_kernel: y^T = Wd16t_s H^T, one 128-row block of Wd16t_s (128 columns of y) and
+//      one tile of up to NP tokens per cluster of up to 8 CTAs, each a K range of f_pad; the fp32
+//      partials meet in the cluster's shared memory and are added in rank order (a fixed order)
+//      into bf16 y. It also serves the union path's down product for 129-512 tokens (128-token
+//      tiles), after the SM-pair gate + up GEMM.
 // Both launch as programmatic dependents of the kernel before them on the stream.
 #include <cooperative_groups.h>
 
@@ -306,6 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
 // in bf16.
 struct DownArgs {
     int N, d, fp, ks;
+    int m_tiles;  // 128-row blocks of Wd16t_s; cluster c takes block c % m_tiles of token tile c / m_tiles
     __nv_bfloat16* y;
     int32_t* status;
     uint64_t wait_limit_ns;
@@ -346,7 +349,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
     const int ks = a.ks;
     const int r = static_cast<int>(cluster.block_rank());
-    const int m0 = static_cast<int>(blockIdx.x) / ks * 128;
+    const int blk = static_cast<int>(blockIdx.x) / ks;
+    const int m0 = blk % a.m_tiles * 128, t0 = blk / a.m_tiles * NP;  // rows of Wd16t_s, first token
+    const int nt_here = min(NP, a.N - t0);
     const int kbs = a.fp / kBK;
     const int kb0 = kbs * r / ks, kb1 = kbs * (r + 1) / ks;  // non-empty: ks <= kbs
 
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     tma_load_2d(sa, &tmW, kb * kBK, m0, &full[stage]);
                 }
-                tma_load_2d(sa + C::A_BYTES, &tmH, kb * kBK, 0, &full[stage]);
+                tma_load_2d(sa + C::A_BYTES, &tmH, kb * kBK, t0, &full[stage]);
                 issued_mask |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) {
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         // rows [j0, j1) of the block (multiples of 4), four at a time: element e = token e / n4, rows
         // j0 + 4 (e % n4) .. + 3; consecutive threads read 16 consecutive bytes of each partial
         const int j0 = 128 * r / ks / 4 * 4, j1 = r + 1 == ks ? 128 : 128 * (r + 1) / ks / 4 * 4;
-        const int n4 = (j1 - j0) / 4, total = n4 * a.N;
+        const int n4 = (j1 - j0) / 4, total = n4 * nt_here;
         for (int e0 = threadIdx.x; e0 < total; e0 += 2 * kSmallThreads) {
             float4 v[2][kDownMaxCluster];
 #pragma unroll
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                         acc.w += v[b][i].w;
                     }
                 const int col = m0 + j0 + 4 * (e % n4);
-                __nv_bfloat16* o = a.y + static_cast<size_t>(e / n4) * a.d + col;
+                __nv_bfloat16* o = a.y + static_cast<size_t>(t0 + e / n4) * a.d + col;
                 if (col + 3 < a.d) {  // d is a multiple of 8: y rows are 16-byte aligned, col a multiple of 4
                     const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
                     uint2 w;
@@ -549,6 +554,7 @@ twell_status launch_down_small(const __half* H, const void* Wd16t_s, int N, int 
     twell_host::DevInfo di;
     if (twell_host::dev_info(&di) != TWELL_OK) return TWELL_ERR_CUDA;
     const int m_tiles = (d + 127) / 128;
+    const int blocks = m_tiles * ((N + NP - 1) / NP);  // (row block, token tile) pairs
     auto kern = down_small_kernel<NP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES)) !=
         cudaSuccess)
@@ -565,20 +571,20 @@ twell_status launch_down_small(const __half* H, const void* Wd16t_s, int N, int 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // K ranges per 128-row block: the largest cluster (up to 8) of which m_tiles fit on the GPU at
-    // once (clusters are placed within one GPC: fewer of 8 fit than SMs / 8); counts cached per size
+    // K ranges per block: the largest cluster (up to 8) of which all blocks fit on the GPU at once
+    // (clusters are placed within one GPC: fewer of 8 fit than SMs / 8); counts cached per size
     static int fit[kDownMaxCluster + 1][3] = {};
     const int slot = NP == 32 ? 0 : (NP == 64 ? 1 : 2);
     int ks = 1;
     for (int c = std::min(kDownMaxCluster, fp / kBK); c > 1; --c) {
         if (fit[c][slot] == 0) {
             attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-            cfg.gridDim = dim3(static_cast<unsigned>(c * m_tiles));
+            cfg.gridDim = dim3(static_cast<unsigned>(c * blocks));
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return TWELL_ERR_CUDA;
             fit[c][slot] = n > 0 ? n : -1;
         }
-        if (fit[c][slot] >= m_tiles) {
+        if (fit[c][slot] >= blocks) {
             ks = c;
             break;
         }
@@ -588,9 +594,9 @@ twell_status launch_down_small(const __half* H, const void* Wd16t_s, int N, int 
     if (st != TWELL_OK) return st;
     st = twell_host::make_tmap_bf16(&th, H, fp, N, fp, 64, NP);
     if (st != TWELL_OK) return st;
-    DownArgs a{N, d, fp, ks, static_cast<__nv_bfloat16*>(y), dev_status, twell_host::wait_limit_ns()};
+    DownArgs a{N, d, fp, ks, m_tiles, static_cast<__nv_bfloat16*>(y), dev_status, twell_host::wait_limit_ns()};
     attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
-    cfg.gridDim = dim3(static_cast<unsigned>(m_tiles * ks));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks * ks));
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, tw, th, a) != cudaSuccess) return TWELL_ERR_CUDA;
     return twell_host::launch_status();
@@ -631,8 +637,8 @@ twell_status twell_host::gate_up_small(const void* x, const void* Wg_s, const vo
 twell_status twell_host::down_small(const __half* H, const void* Wd16t_s, int N, int d, int f, int fp, void* y,
                                     int32_t* dev_status, cudaStream_t s)
 {
-    if (N <= 0 || N > kTransposedMaxN || fp % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+    if (N <= 0 || N > kDownSmallMaxN || fp % 64 != 0) return TWELL_ERR_UNSUPPORTED;
     if (N <= 32) return twell::launch_down_small<32>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
     if (N <= 64) return twell::launch_down_small<64>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
-    return twell::launch_down_small<128>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);
+    return twell::launch_down_small<128>(H, Wd16t_s, N, d, f, fp, y, dev_status, s);  // 128-token tiles
 }
