@@ -146,9 +146,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // a kernel launched as this one's programmatic dependent may be scheduled now (it waits for
-    // this grid to complete before it reads anything this grid writes)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // an extent read from the device is written by an earlier kernel: wait for it first
     if (g.pdl && (g.M_dyn != nullptr || g.K_dyn != nullptr)) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -221,6 +218,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (g.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous grid's writes are visible
+    // A kernel launched as this one's programmatic dependent may be scheduled now. It waits for this
+    // grid to complete before it reads what this grid writes; only after this point, when every
+    // kernel before this one has completed, so that it may read the weights before its own wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the even CTA's barriers, as shared::cluster addresses (PAIR)
     const uint32_t full_lead = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
     const uint32_t tempty_lead = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
