@@ -501,9 +501,9 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
 # 1.5B-like layer (0.5% kept) the union path is also the faster of the two for every batch of 32 to
 # 4096 tokens (us; dense in brackets; up to 128 tokens the union path's products run transposed):
 #   tokens      32     64     128    256    512    1024   2048    4096
-#   walk        35.3   39.2   50.1   54.2   65.0   89.9   121.8   183.9
-#   union       27.9   28.6   32.7   35.3   49.6   66.2   91.3    165.8
-#   dense      (32.9) (30.7) (32.5) (35.0) (47.0) (65.7) (110.3) (190.6)
+#   walk        37.7   38.3   46.1   51.5   65.9   89.1   121.2   185.3
+#   union       26.7   28.7   32.5   36.4   48.5   65.0   90.0    165.5
+#   dense      (31.7) (30.6) (32.7) (36.3) (46.5) (67.3) (111.2) (191.8)
 # so batches of up to 4096 tokens switch a little lower, and batches of up to UNION_ANY_DENSITY_MAX_N
 # tokens take the union path at every density: uniform layers of those shapes at 0.1% / 0.25% kept,
 #   64 tokens:  walk 30.8 / 33.0, union 26.8 / 27.3, dense 27.0 / 27.5

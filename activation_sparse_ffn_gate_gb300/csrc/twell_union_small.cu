@@ -37,6 +37,9 @@ namespace {
 
 constexpr int kSmallUnits = 64;        // hidden units per CTA
 constexpr int kSmallThreads = 192;     // warp 0 TMA, warp 1 TMEM + MMA, warps 2..5 epilogue
+// gate + up: the same roles, two more warps; after the main loop all eight pack (one token and
+// 32-unit half per thread for up to 128 tokens)
+constexpr int kGateUpThreads = 256;
 constexpr uint32_t kSmallRing = 196608;  // shared memory of the operand ring (and, after it, of g and u)
 
 template <int NP>
@@ -67,7 +70,7 @@ struct SmallArgs {
 // rest is not loaded (its products, in TMEM lanes 64-127, are never read); the epilogue packs the
 // TwELL only.
 template <int NP, bool GATE_ONLY>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGateUpThreads, 1)
     gate_up_small_kernel(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmU,
                          const __grid_constant__ CUtensorMap tmX, const SmallArgs a)
 {
@@ -178,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
             tc_commit<1>(drain);
             wait_bounded(drain, 0, nullptr, a.status, a.wait_limit_ns);
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------------ TMEM -> shared memory
         const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31: rows 0-63 hold g, 64-127 u
         int ok = 1;
@@ -209,25 +212,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     // T = 128: the cluster's two CTAs hold units [0, 64) and [64, 128) of tile blockIdx.x / 2; each
     // packs its own units, the second CTA's entries after the first's (its per-token counts, read
     // once from the first CTA's shared memory). T = 64: each CTA is a tile of its own.
-    // Epilogue thread: one 32-unit half hf of this CTA's units for tokens tb, tb + 64 (< N).
+    // Pack thread (all eight warps): one 32-unit half hf of this CTA's units for token tb (< N).
     const bool wide = a.T == 128;
     const bool second = wide && rank == 1;
     const int tile = wide ? blockIdx.x / 2 : blockIdx.x;
-    const int ew = warp - 2, hf = ew & 1, tb = 32 * (ew >> 1) + lane;
+    const int hf = warp & 1, tb = 32 * (warp >> 1) + lane;
+    constexpr int TSTEP = kGateUpThreads / 2;  // tokens per pass of all threads (N <= 128: one pass)
     const int uh = u0 + 32 * hf;  // global index of the half's first unit
     const int nin = min(max(a.f - uh, 0), 32);  // its units below f
     // 1. counts of kept units per token and half
-    if (have && warp >= 2) {
-        for (int t = tb; t < a.N; t += 64) {
+    if (have) {
+        for (int t = tb; t < a.N; t += TSTEP) {
             int c = 0;
 #pragma unroll 8
             for (int j = 0; j < 32; ++j) c += (j < nin && gs[(32 * hf + j) * GP + t] > 0.0f) ? 1 : 0;
             ch_s[hf * NP + t] = c;
         }
     }
-    if (have && warp >= 2) bar_or(1, 128, false);  // the four epilogue warps: ch_s is complete
-    if (wide && !second && have && warp >= 2 && hf == 0)
-        for (int t = tb; t < a.N; t += 64) cnt_s[t] = ch_s[t] + ch_s[NP + t];
+    if (have) bar_or(1, kGateUpThreads, false);  // ch_s is complete
+    if (wide && !second && have && hf == 0)
+        for (int t = tb; t < a.N; t += TSTEP) cnt_s[t] = ch_s[t] + ch_s[NP + t];
 
     // 2. per token and half: ReLU + TwELL in ascending unit order, as twell_gate_pack packs, and
     // h = a * u (a = the value as packed) as fp16, 16 bytes at a time
@@ -236,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
         __nv_bfloat16* vals16 = static_cast<__nv_bfloat16*>(a.vals);
         float* vals32 = static_cast<float*>(a.vals);
         bool over = false;
-        for (int t = tb; t < a.N; t += 64) {
+        for (int t = tb; t < a.N; t += TSTEP) {
             const int base = (second ? base_s[t] : 0) + (hf ? ch_s[t] : 0);
             const size_t slot = (static_cast<size_t>(t) * a.nt + tile) * static_cast<size_t>(a.T) + base;
             float gr[32], ur[32];  // all loads first: the stores below may not be moved above them
@@ -284,18 +288,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSmallThreads, 1)
     // memory, so no thread waits there for its stores to drain): the second CTA has read them,
     // so the first may exit.
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    if (!second && have && warp >= 2) pack();
+    if (!second && have) pack();
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (second) {
         have = have && !*cluster.map_shared_rank(const_cast<int*>(abort_flag), 0);
-        if (have && warp >= 2) {
+        if (have) {
             const int* peer_cnt = cluster.map_shared_rank(cnt_s, 0);
-            for (int t = static_cast<int>(threadIdx.x) - 64; t < a.N; t += 128) base_s[t] = peer_cnt[t];
-            bar_or(1, 128, false);  // base_s is complete (its loads have returned)
+            for (int t = static_cast<int>(threadIdx.x); t < a.N; t += kGateUpThreads) base_s[t] = peer_cnt[t];
+            bar_or(1, kGateUpThreads, false);  // base_s is complete (its loads have returned)
         }
     }
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-    if (second && have && warp >= 2) pack();
+    if (second && have) pack();
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
@@ -537,7 +541,7 @@ twell_status launch_gate_up_small(const void* x, const void* Wg_s, const void* W
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * static_cast<unsigned>((a.f + 127) / 128));
-    cfg.blockDim = dim3(kSmallThreads);
+    cfg.blockDim = dim3(kGateUpThreads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
