@@ -133,10 +133,11 @@ __global__ void __launch_bounds__(256) reduce_splits_bf16_kernel(const float* __
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// bytes of the split partials a call may need: K ranges up to kSplitMaxN tokens, the tail tiles' K
-// halves above
+// bytes of the split partials a call may need: none up to kDownSmallMaxN tokens (the down product
+// adds its partials on chip), K ranges up to kSplitMaxN tokens, the tail tiles' K halves above
 inline size_t split_bytes(int N, int d)
 {
+    if (N <= twell_host::kDownSmallMaxN) return 0;
     return N <= kSplitMaxN ? up256(static_cast<size_t>(kSplitMaxRows) * d * 4) : up256(kTailMax * kTailTileBytes);
 }
 

@@ -179,6 +179,12 @@ def test_gate_union_rejects_bad_arguments(lib):
     need = lib.twell_workspace_bytes(8, 4, 64, 256, 128, 0, 0)  # TWELL_OP_FFN_GATE_UNION_FWD
     assert need >= 4 * 256 * 2  # H [N, f_pad] fp16
     assert lib.twell_workspace_bytes(8, 3, 64, 1000, 128, 0, 0) >= 3 * 1024 * 2  # f_pad = 1024
+    # up to 512 tokens the down product adds its split partials on chip: H alone; from 513 tokens the
+    # SM-pair down GEMM's fp32 partials (up to 2048 rows of d_model) come on top
+    h = lambda N: (N * 5632 * 2 + 255) // 256 * 256  # noqa: E731
+    assert lib.twell_workspace_bytes(8, 512, 2048, 5632, 128, 0, 0) == h(512)
+    assert lib.twell_workspace_bytes(8, 513, 2048, 5632, 128, 0, 0) >= h(513) + 2048 * 2048 * 4
+    assert lib.twell_workspace_bytes(5, 512, 2048, 5632, 128, 0, 0) < lib.twell_workspace_bytes(5, 513, 2048, 5632, 128, 0, 0)
     call = lambda **kw: lib.twell_ffn_gate_union_fwd(  # noqa: E731
         ALIGNED, kw.get("wg", ALIGNED), ALIGNED, kw.get("wd", ALIGNED), kw.get("N", 4), kw.get("d", 64),
         kw.get("f", 256), kw.get("T", 128), kw.get("dt", 0), ctypes.byref(kw.get("p", p)), kw.get("y", ALIGNED),
