@@ -1,5 +1,6 @@
-// twell_union_small.cu -- the union path for batches of at most 128 tokens, with the weights on the
-// M side of the tensor-core products.
+// twell_union_small.cu -- tensor-core kernels for small batches with the weights on the M side of
+// the products: the union path's gate + up (and, gate only, the walk path's gate) for up to 128
+// tokens, and the union path's down product for up to 512 tokens.
 //
 // For a batch of N <= 128 tokens the union path's 256 x 256 SM-pair tiles put the tokens on the
 // 256-row side: at 64 tokens 75% of every MMA is padding rows, and each tile's tensor work outlasts
