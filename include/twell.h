@@ -232,9 +232,10 @@ TWELL_API twell_status twell_ffn_decode(const void* x, const void* Wg_s, const v
  * (tcgen05 GEMM on SM pairs, the product formed in its epilogue where the mask is set, h stored in
  * place as fp16: 11 significant bits); y = H Wd16_s (tcgen05 GEMM on SM pairs over f_pad, fp16
  * operands, bf16 y). Wd16t_s is the transpose of Wd_s converted once to fp16 ([d, f]:
- * twell_convert_f16_transposed), so that the down GEMM reads both operands K-major. For N <= 128
- * the down product runs transposed (y^T = Wd16t_s H^T, rows of Wd16t_s on the MMA's M side, K split
- * over a cluster of CTAs whose fp32 partials are added in a fixed order in shared memory).
+ * twell_convert_f16_transposed), so that the down GEMM reads both operands K-major. For N <= 512
+ * the down product runs transposed (y^T = Wd16t_s H^T, rows of Wd16t_s on the MMA's M side, tokens in
+ * tiles of up to 128, K split over a cluster of CTAs whose fp32 partials are added in a fixed order
+ * in shared memory).
  * bf16 x, Wu_s, y; d and f multiples of 8; x [N, d], Wu_s [f, d], Wd16t_s [d, f], y [N, d], device,
  * 16-byte aligned. ws: twell_workspace_bytes(TWELL_OP_FFN_UNION_FWD, N, d, f, ...) bytes (H and the
  * masks, 2.125 * N * f_pad bytes), required when N > 0. A corrupt TwELL entry (count above the tile
