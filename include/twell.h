@@ -255,7 +255,8 @@ TWELL_API twell_status twell_ffn_union_fwd(const void* x, const void* Wu_s, cons
  * significant bits; 0 where g <= 0) into the workspace; then y = H Wd16_s as in twell_ffn_union_fwd.
  * For N <= 128 both products run transposed, the weights on the MMA's M side and the tokens as its
  * N columns: each CTA stacks 64 units' Wg_s rows over their Wu_s rows, and two CTAs form one
- * 128-unit tile whose TwELL is the same, bit for bit.
+ * 128-unit tile whose TwELL is the same, bit for bit; up to N = 512 the down product runs
+ * transposed as in twell_ffn_union_fwd.
  * For layers whose density the walk no longer serves: the union of the units a tile of 128 tokens
  * keeps is then most of d_ff ([TC] §3: tensor cores for the heavy work).
  * bf16 x, Wg_s, Wu_s, y (dtype must be TWELL_BF16); d and f multiples of 8; T = 64 or 128 (else
