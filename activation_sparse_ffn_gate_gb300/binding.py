@@ -504,28 +504,38 @@ def twell_ffn_decode(x: torch.Tensor, Wg_s: torch.Tensor, Wu_s: torch.Tensor, Wd
 #   walk        37.7   38.3   46.1   51.5   65.9   89.1   121.2   185.3
 #   union       26.7   28.7   32.5   36.4   48.5   65.0   90.0    165.5
 #   dense      (31.7) (30.6) (32.7) (36.3) (46.5) (67.3) (111.2) (191.8)
-# so batches of up to 4096 tokens switch a little lower, and batches of up to UNION_ANY_DENSITY_MAX_N
-# tokens take the union path at every density: uniform layers of those shapes at 0.1% / 0.25% kept,
+# so batches of up to 4096 tokens switch a little lower, and smaller batches lower still; up to
+# UNION_ANY_DENSITY_MAX_N tokens the union path is taken at every density. Uniform layers of those
+# shapes at 0.1% / 0.25% kept:
 #   64 tokens:  walk 30.8 / 33.0, union 26.8 / 27.3, dense 27.0 / 27.5
 #   128 tokens: walk 33.1 / 36.7, union 31.1 / 30.8, dense 29.9 / 29.4
+#   256 tokens: walk 34.0 / 43.0, union 34.4 / 34.8, dense 32.8 / 32.9  (cross near 0.1%)
+#   512 tokens: walk 38.4 / 51.1, union 48.8 / 48.7, dense 45.6 / 45.3  (cross near 0.22%)
 # The gathered tile-union path is never the fastest under these densities; it stays available as path
 # "tile_union".
 UNION_MIN_DENSITY = 0.0045
 UNION_MIN_DENSITY_SMALL_BATCH = 0.004
 SMALL_BATCH_MAX_N = 4096
 UNION_ANY_DENSITY_MAX_N = 128
+# (largest batch, density from which the union path is taken) for batches between those sizes
+UNION_MIN_DENSITY_BY_BATCH = ((256, 0.001), (512, 0.002))
 
 
 def choose_path(n_tokens: int, density: Optional[float]) -> str:
     """The policy of ffn_forward(path="auto"): decode for at most DECODE_MAX_N tokens; the union path
-    up to UNION_ANY_DENSITY_MAX_N tokens; above that the walk below UNION_MIN_DENSITY
-    (UNION_MIN_DENSITY_SMALL_BATCH up to SMALL_BATCH_MAX_N tokens) or without a density estimate,
-    the union path (gate and up projection in one GEMM, down GEMM over all of d_ff) above it."""
+    up to UNION_ANY_DENSITY_MAX_N tokens; above that the walk below a density that grows with the
+    batch (UNION_MIN_DENSITY_BY_BATCH, then UNION_MIN_DENSITY_SMALL_BATCH up to SMALL_BATCH_MAX_N
+    tokens, then UNION_MIN_DENSITY) or without a density estimate, the union path (gate and up
+    projection in one GEMM, down GEMM over all of d_ff) from it on."""
     if n_tokens <= DECODE_MAX_N:
         return "decode"
     if n_tokens <= UNION_ANY_DENSITY_MAX_N:
         return "union"
     limit = UNION_MIN_DENSITY_SMALL_BATCH if n_tokens <= SMALL_BATCH_MAX_N else UNION_MIN_DENSITY
+    for max_n, d in UNION_MIN_DENSITY_BY_BATCH:
+        if n_tokens <= max_n:
+            limit = d
+            break
     if density is None or density < limit:
         return "walk"
     return "union"

@@ -25,8 +25,16 @@ def test_batches_up_to_128_tokens_take_the_union_path_at_any_density():
             assert binding.choose_path(n, d) == "union"
 
 
+def test_batches_of_129_to_512_tokens_switch_lower_still():
+    assert binding.choose_path(129, None) == "walk"
+    assert binding.choose_path(200, 0.0005) == "walk" and binding.choose_path(200, 0.001) == "union"
+    assert binding.choose_path(256, 0.0025) == "union"
+    assert binding.choose_path(512, 0.001) == "walk" and binding.choose_path(512, 0.0025) == "union"
+    assert binding.choose_path(513, 0.0025) == "walk"
+
+
 def test_batches_up_to_4096_tokens_switch_at_a_lower_density():
-    for n in (binding.UNION_ANY_DENSITY_MAX_N + 1, 512, binding.SMALL_BATCH_MAX_N):
+    for n in (513, 1024, binding.SMALL_BATCH_MAX_N):
         assert binding.choose_path(n, None) == "walk"
         assert binding.choose_path(n, 0.001) == "walk"
         assert binding.choose_path(n, 0.005) == "union"
