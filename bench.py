@@ -253,6 +253,22 @@ def _traffic(kernel):
     return rec.get("bytes_per_launch")
 
 
+def _union_down_launches(N, d, sm_count):
+    """Launches of the union path's down product, by the library's host rule: one kernel up to 512
+    tokens (K split over a cluster, partials added on chip); the SM-pair GEMM and a reduction of its
+    K-split partials up to 1024; above that the GEMM, plus a reduction of the K halves when the
+    partial last wave of 256 x 256 tiles is split (it fills at most half the SM pairs, at most 40
+    tiles)."""
+    if N <= 512:
+        return 1
+    if N <= 1024:
+        return 2
+    pairs = sm_count // 2
+    units = -(-N // 256) * -(-d // 256)
+    tail = units % pairs
+    return 2 if (units > pairs and 0 < tail and 2 * tail <= pairs and tail <= 40) else 1
+
+
 def run_ours(a, rank, world):
     import numpy as np
     import torch
@@ -683,11 +699,13 @@ def run_ours(a, rank, world):
                        "steps' layer calls (three streams, double-buffered device x and y)",
                 "serial": {"value": N / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
                            "how": "copy in, the layer, copy out one after the other on one stream"}},
-        # per step: gate + pack, then the walk's plan and the walk; or the union path's expand, up and
-        # down GEMMs; or the tile-union path's union bits, prefix, work list, expand, up and down GEMMs
-        # union path: gate + up GEMM and down GEMM, plus the split-K reduction for batches of up to 1024
-        "gpu_launches": ((3 if N <= 1024 else 2) if gate_union else {"walk": 3, "union": 4, "tile_union": 7}[a.path])
-                        * a.steps,
+        # per step: gate + pack, then the walk's zeroing, plan and walk; or the union path's gate + up
+        # GEMM (or gate + pack, expand and up GEMM) and its down product; or the tile-union path's gate,
+        # union bits, prefix, work list, expand, up and down GEMMs
+        "gpu_launches": (((1 if gate_union else 3)
+                          + _union_down_launches(N, d, torch.cuda.get_device_properties(dev).multi_processor_count))
+                         if a.path == "union"
+                         else {"walk": 4, "tile_union": 7}[a.path]) * a.steps,
         "path": a.path,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
